@@ -1,0 +1,246 @@
+"""Pins of the float64 oracle against things other than itself.
+
+Each test ties the oracle to a library routine (PyTorch float64
+scaled-dot-product attention, ``rms_norm``), a closed form, an exact
+invariant, a value printed on the pages, or an independent brute force.
+Together they make a dropped term, a wrong sign, a wrong group index, a
+wrong softmax scale, a transposed operand or a wrong mask fail somewhere.
+
+Sources: "Differential Attention in Large Language Models ..." (sections
+"The Mechanics of Attention Noise", "Differential Attention Architecture",
+"Learnable Lambda Re-parameterization", "Headwise Normalization") and the
+"Grouped Differential Attention" abstract.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from grouped_differential_attention_gb300 import workloads
+from oracle import ref_numpy
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def case(B, L, hs, hn, d, dv, seed=0, dtype="f32", lam_range=(0.2, 0.8)):
+    return workloads.make_prefill_inputs(
+        workloads.DIFF_F32_L128, B=B, L=L, h_s=hs, h_n=hn, d=d, dv=dv, seed=seed,
+        dtype=dtype, lam_range=lam_range)
+
+
+def sdpa64(q, k, v, causal):
+    """Library attention in float64; tensors are [B, L, H, D]."""
+    out = F.scaled_dot_product_attention(
+        q.double().permute(0, 2, 1, 3), k.double().permute(0, 2, 1, 3),
+        v.double().permute(0, 2, 1, 3), is_causal=causal)
+    return out.permute(0, 2, 1, 3).numpy()
+
+
+SHAPES = [  # B, L, hs, hn, d, dv
+    (1, 1, 2, 2, 8, 16),
+    (2, 7, 2, 1, 8, 16),
+    (1, 19, 6, 2, 16, 32),
+    (2, 33, 4, 4, 16, 32),
+    (1, 40, 8, 2, 32, 64),
+    (1, 24, 12, 4, 64, 128),
+]
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_lambda_zero_is_library_attention(oracle_mod, shape, causal):
+    """lambda = 0 leaves the signal map alone: softmax(Q1 K1^T / sqrt d) V."""
+    q1, k1, q2, k2, v, lam = case(*shape)
+    got = oracle_mod.prefill(q1, k1, q2, k2, v, torch.zeros_like(lam), 0.8,
+                             causal=causal, norm=False)
+    np.testing.assert_allclose(got, sdpa64(q1, k1, v, causal), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_difference_of_two_library_attentions(oracle_mod, shape, causal):
+    """Pre-norm output = SDPA(Q1,K1,V) - lambda_h SDPA(Q2_rep, K2_rep, V).
+
+    Q2/K2 repeated r times along heads (repeat_interleave) is grouped-query
+    sharing written out explicitly; this pins the group index g = h // r,
+    the per-head lambda, the 1/sqrt(d) scale and the mask of both maps.
+    """
+    B, L, hs, hn, d, dv = shape
+    q1, k1, q2, k2, v, lam = case(*shape, seed=3)
+    r = hs // hn
+    a = sdpa64(q1, k1, v, causal)
+    b = sdpa64(q2.repeat_interleave(r, dim=2), k2.repeat_interleave(r, dim=2), v, causal)
+    want = a - lam.double().numpy()[None, None, :, None] * b
+    got = oracle_mod.prefill(q1, k1, q2, k2, v, lam, 0.8, causal=causal, norm=False)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("eps", [1e-5, 1e-2])
+def test_norm_is_library_rms_norm(oracle_mod, eps):
+    """Epilogue = (1 - lambda_init) * rms_norm(o) with no gain, eps inside the root."""
+    q1, k1, q2, k2, v, lam = case(2, 21, 6, 3, 16, 48, seed=5)
+    lam_init = 0.37
+    pre = oracle_mod.prefill(q1, k1, q2, k2, v, lam, lam_init, eps=eps, norm=False)
+    got = oracle_mod.prefill(q1, k1, q2, k2, v, lam, lam_init, eps=eps, norm=True)
+    want = (1 - lam_init) * F.rms_norm(torch.from_numpy(pre), (pre.shape[-1],), eps=eps)
+    np.testing.assert_allclose(got, want.numpy(), rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_equal_maps_and_unit_lambda_cancel(oracle_mod, causal):
+    """Q2 = Q1, K2 = K1, h_s = h_n and lambda = 1: the difference map is exactly 0."""
+    q1, k1, _, _, v, lam = case(2, 30, 4, 4, 16, 32, seed=7)
+    ones = torch.ones_like(lam)
+    got = oracle_mod.prefill(q1, k1, q1, k1, v, ones, 0.8, causal=causal, norm=False)
+    assert np.all(got == 0.0)
+    # and a lambda != 1 leaves (1 - lambda) times plain attention
+    got = oracle_mod.prefill(q1, k1, q1, k1, v, 0.25 * ones, 0.8, causal=causal, norm=False)
+    np.testing.assert_allclose(got, 0.75 * sdpa64(q1, k1, v, causal), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_rows_of_each_map_sum_to_one(oracle_mod, causal):
+    """V = 1: every softmax row sums to 1, so the difference map rows sum to 1 - lambda_h.
+
+    Pre-norm output is 1 - lambda_h everywhere; with the norm on it is the
+    closed form (1 - lambda_init)(1 - lambda_h) / sqrt((1 - lambda_h)^2 + eps).
+    """
+    q1, k1, q2, k2, v, lam = case(1, 45, 6, 2, 16, 32, seed=9)
+    v = torch.ones_like(v)
+    lam_init, eps = 0.8, 1e-5
+    pre = oracle_mod.prefill(q1, k1, q2, k2, v, lam, lam_init, causal=causal, norm=False)
+    lam64 = lam.double().numpy()
+    np.testing.assert_allclose(pre, np.broadcast_to((1 - lam64)[None, None, :, None], pre.shape),
+                               rtol=0, atol=1e-14)
+    post = oracle_mod.prefill(q1, k1, q2, k2, v, lam, lam_init, causal=causal, norm=True)
+    closed = (1 - lam_init) * (1 - lam64) / np.sqrt((1 - lam64) ** 2 + eps)
+    np.testing.assert_allclose(post, np.broadcast_to(closed[None, None, :, None], post.shape),
+                               rtol=1e-14, atol=1e-14)
+
+
+def test_first_row_under_causal_mask(oracle_mod):
+    """Row 0 sees only key 0: y0 = (1-li)(1-lam) v0 / sqrt(mean(((1-lam) v0)^2) + eps)."""
+    q1, k1, q2, k2, v, lam = case(2, 17, 6, 3, 16, 32, seed=11)
+    lam_init, eps = 0.6, 1e-5
+    got = oracle_mod.prefill(q1, k1, q2, k2, v, lam, lam_init, causal=True, eps=eps)[:, 0]
+    v0 = v[:, 0].double().numpy()                            # [B, hs, dv]
+    o0 = (1 - lam.double().numpy())[None, :, None] * v0
+    want = (1 - lam_init) * o0 / np.sqrt(np.mean(o0 ** 2, axis=-1, keepdims=True) + eps)
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("norm", [True, False])
+@pytest.mark.parametrize("hn", [1, 2])
+@pytest.mark.parametrize("r", [1, 2, 3, 4])
+@pytest.mark.parametrize("L", [1, 5, 16])
+def test_loop_oracle_matches_dense_matrices(oracle_mod, L, r, hn, norm, causal):
+    """The C loop oracle and the NumPy dense-matrix oracle agree to 1e-12."""
+    hs = r * hn
+    q1, k1, q2, k2, v, lam = case(2, L, hs, hn, 8, 16, seed=L * 100 + r * 10 + hn)
+    got = oracle_mod.prefill(q1, k1, q2, k2, v, lam, 0.7, causal=causal, norm=norm)
+    want = ref_numpy.gda_dense(q1.numpy(), k1.numpy(), q2.numpy(), k2.numpy(), v.numpy(),
+                               lam.numpy(), 0.7, causal=causal, norm=norm)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_pins_notice_a_wrong_group_map(oracle_mod):
+    """Interleaved groups (h % h_n) instead of contiguous ones fail the repetition pin."""
+    B, L, hs, hn, d, dv = 1, 12, 6, 2, 8, 16
+    q1, k1, q2, k2, v, lam = case(B, L, hs, hn, d, dv, seed=13)
+    r = hs // hn
+    want = sdpa64(q1, k1, v, True) - lam.double().numpy()[None, None, :, None] * sdpa64(
+        q2.repeat_interleave(r, dim=2), k2.repeat_interleave(r, dim=2), v, True)
+    good = ref_numpy.gda_dense(q1.numpy(), k1.numpy(), q2.numpy(), k2.numpy(), v.numpy(),
+                               lam.numpy(), 0.8, norm=False)
+    bad = ref_numpy.gda_dense(q1.numpy(), k1.numpy(), q2.numpy(), k2.numpy(), v.numpy(),
+                              lam.numpy(), 0.8, norm=False, group_of=np.arange(hs) % hn)
+    np.testing.assert_allclose(good, want, rtol=0, atol=1e-12)
+    assert np.max(np.abs(bad - want)) > 1e-3
+
+
+def test_bf16_inputs_are_used_exactly(oracle_mod):
+    q1, k1, q2, k2, v, lam = case(1, 9, 4, 2, 16, 32, seed=15, dtype="bf16")
+    a = oracle_mod.prefill(q1, k1, q2, k2, v, lam, 0.8)
+    b = oracle_mod.prefill(q1.float(), k1.float(), q2.float(), k2.float(), v.float(), lam, 0.8)
+    assert np.array_equal(a, b)
+
+
+def test_sampled_rows_equal_full_rows(oracle_mod):
+    q1, k1, q2, k2, v, lam = case(2, 50, 6, 2, 16, 32, seed=17)
+    rows = [0, 1, 13, 49, 49, 7]
+    full = oracle_mod.prefill(q1, k1, q2, k2, v, lam, 0.8)
+    part = oracle_mod.prefill_rows(q1, k1, q2, k2, v, lam, 0.8, rows)
+    assert np.array_equal(part, full[:, rows])
+
+
+def _decode_case(B, Lcap, hs, hn, d, dv, seed):
+    w = workloads.GDA3_DECODE_B64
+    return workloads.make_decode_inputs(w, B=B, Lcap=Lcap, h_s=hs, h_n=hn, d=d, dv=dv,
+                                        seed=seed, len_range=(1, Lcap))
+
+
+@pytest.mark.parametrize("hs,hn", [(6, 2), (4, 4), (3, 1)])
+def test_decode_is_last_causal_row(oracle_mod, hs, hn):
+    """Decoding with the new token already in the cache equals prefill row len-1."""
+    B, Lcap, d, dv = 5, 23, 16, 32
+    q1, q2, k1c, k2c, vc, lens, lam = _decode_case(B, Lcap, hs, hn, d, dv, seed=hs * 7 + hn)
+    lens[0], lens[1] = 1, Lcap
+    got = oracle_mod.decode(q1, q2, k1c, k2c, vc, lens, lam, 0.8)
+    for b in range(B):
+        n = int(lens[b])
+        # place the decode query at row n-1 of a prefill over the first n cache rows
+        q1p = torch.zeros(1, n, hs, d, dtype=q1.dtype)
+        q2p = torch.zeros(1, n, hn, d, dtype=q2.dtype)
+        q1p[0, n - 1], q2p[0, n - 1] = q1[b], q2[b]
+        want = oracle_mod.prefill_rows(q1p, k1c[b:b + 1, :n], q2p, k2c[b:b + 1, :n],
+                                       vc[b:b + 1, :n], lam, 0.8, [n - 1])
+        np.testing.assert_allclose(got[b], want[0, 0], rtol=0, atol=1e-13)
+
+
+def test_decode_is_difference_of_library_attentions(oracle_mod):
+    B, Lcap, hs, hn, d, dv = 3, 31, 6, 2, 16, 32
+    q1, q2, k1c, k2c, vc, lens, lam = _decode_case(B, Lcap, hs, hn, d, dv, seed=21)
+    r = hs // hn
+    got = oracle_mod.decode(q1, q2, k1c, k2c, vc, lens, lam, 0.8, norm=False)
+    for b in range(B):
+        n = int(lens[b])
+        a = sdpa64(q1[b:b + 1, None], k1c[b:b + 1, :n], vc[b:b + 1, :n], False)[0, 0]
+        c = sdpa64(q2[b:b + 1, None].repeat_interleave(r, dim=2),
+                   k2c[b:b + 1, :n].repeat_interleave(r, dim=2), vc[b:b + 1, :n], False)[0, 0]
+        want = a - lam.double().numpy()[:, None] * c
+        np.testing.assert_allclose(got[b], want, rtol=0, atol=1e-12)
+
+
+def _golden_lambda_init():
+    rows = []
+    with open(os.path.join(HERE, "golden", "lambda_init_schedule.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                layer, value = line.split()
+                rows.append((layer, float(value)))
+    return rows
+
+
+def test_lambda_init_schedule_matches_page(oracle_mod):
+    import grouped_differential_attention_gb300 as gda
+    for layer, value in _golden_lambda_init():
+        if layer == "inf":
+            assert abs(oracle_mod.lambda_init_schedule(10_000) - value) < 1e-12
+            assert abs(gda.lambda_init_schedule(10_000) - value) < 1e-12
+        else:
+            assert abs(oracle_mod.lambda_init_schedule(int(layer)) - value) < 1e-15
+            assert abs(gda.lambda_init_schedule(int(layer)) - value) < 1e-15
+    # the layer-8 constant used by the 3:1 prefill workload
+    assert abs(oracle_mod.lambda_init_schedule(8) - workloads.LAMBDA_INIT_LAYER8) < 1e-15
+    assert abs(gda.lambda_init_schedule(8) - 0.8 + 0.6 * math.exp(-2.1)) < 1e-15
+
+
+def test_oracle_rejects_bad_shapes(oracle_mod):
+    q1, k1, q2, k2, v, lam = case(1, 4, 6, 4, 8, 16)   # 6 % 4 != 0
+    with pytest.raises(ValueError):
+        oracle_mod.prefill(q1, k1, q2, k2, v, lam, 0.8)
