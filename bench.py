@@ -1,0 +1,455 @@
+"""Benchmark of the grouped differential attention hot path on GB300.
+
+One JSON line on rank 0.  A step is one causal prefill of the 3:1 workload
+(B=4, L=2048, 12 signal + 4 noise heads, d=64, dv=128, bf16 I/O) through
+gda_attn_fwd; `value` is its throughput in TFLOP/s (causal-pair flop count
+below) with the inputs already in HBM; `decode` reports the 64-sequence
+split-KV decode in GB/s of KV cache read.  Inputs are synthetic (seeded
+normal tensors at the workloads' shapes).
+
+Flop count per causal (query, key) pair: 2 d (h_s + h_n) for the logits of
+every signal head and, once per noise head, of the shared noise map, plus
+2 * 2 dv h_s for applying both maps to V.  Pairs per sequence: L (L + 1) / 2.
+Decode bytes per cached position: 2 (h_s d + h_n d + h_s dv).
+
+`--impl reference` times the float64 CPU oracle instead (the reference arm:
+there is no reference implementation to run), each step evaluating a bounded
+sample of query rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "GDA causal prefill TFLOP/s (bf16) and decode HBM GB/s, % of GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_FILE = os.path.join(ROOT, "profiles", "prefill_tc_counters.json")
+KERNEL_SOURCES = ["grouped_differential_attention_gb300/csrc/gda_prefill_tc.cu",
+                  "grouped_differential_attention_gb300/csrc/gda_device.cuh"]
+N_INPUT_SETS = 4          # rotating input copies: 4 x 84 MB > 129 MB of L2
+
+
+# ------------------------------------------------------------------ helpers --
+
+def prefill_flops(B, L, hs, hn, d, dv, causal=True):
+    pairs = B * (L * (L + 1) // 2 if causal else L * L)
+    return pairs * (2 * d * (hs + hn) + 4 * dv * hs)
+
+
+def prefill_min_flops(B, L, hs, hn, d, dv):
+    return B * (L * (L + 1) // 2) * (2 * d * (hs + hn) + 2 * dv * hs)
+
+
+def row_flops(B, rows, hs, hn, d, dv):
+    """Causal-pair flops of the listed query rows (all batches and heads)."""
+    return sum(B * (i + 1) * (2 * d * (hs + hn) + 4 * dv * hs) for i in rows)
+
+
+def decode_bytes(lens, hs, hn, d, dv):
+    return int(sum(int(n) for n in lens)) * 2 * (hs * d + hn * d + hs * dv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {k: float(pk[k]) for k in FALLBACK_PEAKS}, "measured (MEASURED_PEAKS.json)"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback (no MEASURED_PEAKS.json)"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it matches the kernel."""
+    try:
+        with open(PROFILE_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None, None
+    if rec.get("kernel_hash") != kernel_hash():
+        return None, None
+    return rec.get("dram_bytes_per_launch"), rec.get("workload")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        target = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            target = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            target = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "25"]
+        if target:
+            cmd += ["-i", target]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            n += 1
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (host-side timing reduction only)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# -------------------------------------------------------------- oracle arms --
+
+def oracle_rows_throughput(w, rows_per_sample: int, target_s: float, seed: int = 0):
+    """Time the float64 oracle on samples of query rows of workload w (TFLOP/s)."""
+    import numpy as np
+    import oracle
+    from grouped_differential_attention_gb300 import workloads as W
+    inp = W.make_prefill_inputs(w, seed=seed)
+    rng = np.random.default_rng(1234)
+    done_flops, spent, nrows = 0, 0.0, 0
+    while spent < target_s:
+        rows = sorted(rng.choice(w.L, size=min(rows_per_sample, w.L), replace=False).tolist())
+        t0 = time.perf_counter()
+        oracle.prefill_rows(*inp, w.lambda_init, rows, causal=w.causal, eps=w.eps)
+        spent += time.perf_counter() - t0
+        done_flops += row_flops(w.B, rows, w.h_s, w.h_n, w.d, w.dv)
+        nrows += len(rows)
+    return done_flops / spent / 1e12, nrows, spent, oracle.max_threads()
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the float64 CPU oracle, as it stands, on host cores."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from grouped_differential_attention_gb300 import workloads as W
+    w = W.PREFILL_WORKLOADS[args.workload]
+    inp = W.make_prefill_inputs(w)
+    rng = np.random.default_rng(99)
+    rows_per_step = 1
+
+    def step():
+        rows = sorted(rng.choice(w.L, size=rows_per_step, replace=False).tolist())
+        oracle.prefill_rows(*inp, w.lambda_init, rows, causal=w.causal, eps=w.eps)
+        return row_flops(w.B, rows, w.h_s, w.h_n, w.d, w.dv)
+
+    for _ in range(args.warmup):
+        step()
+    flops = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        flops += step()
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = (f"{rows_per_step} query row(s) per step (all {w.B} sequences x {w.h_s} heads), "
+              f"rows drawn uniformly from the {w.L}-row causal workload")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) tensors at the workload's shapes)",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "h_s": w.h_s, "h_n": w.h_n, "d": w.d,
+                   "dv": w.dv, "causal": w.causal, "parallelism": "cpu oracle, OpenMP"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU arm --
+
+def run_gda(args, world, rank, local):
+    import grouped_differential_attention_gb300 as gda
+    from grouped_differential_attention_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = W.PREFILL_WORKLOADS[args.workload]
+    if w.dtype != "bf16":
+        raise SystemExit("bench.py times the bf16 tensor-core path")
+    peaks, peak_src = load_peaks()
+
+    # ---- inputs: N_INPUT_SETS rotating copies resident in HBM (weak scaling: seed = rank)
+    sets = []
+    for s in range(N_INPUT_SETS):
+        host = W.make_prefill_inputs(w, seed=rank * 100 + s) if s == 0 else None
+        if s == 0:
+            base = [t.to(dev) for t in host]
+            sets.append(base)
+        else:
+            sets.append([t.clone() for t in base])
+    out = torch.empty((w.B, w.L, w.h_s, w.dv), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        q1, k1, q2, k2, v, lam = sets[i % N_INPUT_SETS]
+        gda.gda_attn_fwd(q1, k1, q2, k2, v, lam, w.lambda_init, causal=w.causal, eps=w.eps,
+                         out=out)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    gda.gda_device_error(clear=True)
+
+    # ---- timed region: K prefill steps, device time from CUDA events on the launch stream
+    sampler = ClockSampler(dev.index)
+    time.sleep(0.05)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    prefill_ms = ev0.elapsed_time(ev1)
+
+    # ---- decode: 64 sequences over bf16 caches of 4096..8192 positions (> L2)
+    dw = W.GDA3_DECODE_B64
+    dinp = [t.to(dev) for t in W.make_decode_inputs(dw, seed=rank)]
+    lens_host = dinp[5].cpu()
+    dout = torch.empty((dw.B, dw.h_s, dw.dv), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(gda.gda_attn_decode_workspace_size(dw.B, dw.Lcap, dw.h_s, dw.h_n, dw.dv),
+                     dtype=torch.uint8, device=dev)
+
+    def dstep():
+        gda.gda_attn_decode(*dinp, dw.lambda_init, eps=dw.eps, out=dout, workspace=ws)
+
+    dec_steps = max(20, args.steps // 20)
+    for _ in range(max(3, args.warmup // 4)):
+        dstep()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev2.record(stream)
+    for _ in range(dec_steps):
+        dstep()
+    ev3.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    decode_ms = ev2.elapsed_time(ev3)
+    clocks = sampler.stop()
+    dev_err = gda.gda_device_error(clear=True)
+
+    # ---- end to end through the public API with pinned host buffers
+    host_in = [t.cpu().pin_memory() for t in sets[0]]
+    dev_in = sets[1]
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(10, min(args.steps, 200))
+
+    def e2e_step():
+        for hsrc, ddst in zip(host_in, dev_in):
+            ddst.copy_(hsrc, non_blocking=True)
+        q1, k1, q2, k2, v, lam = dev_in
+        gda.gda_attn_fwd(q1, k1, q2, k2, v, lam, w.lambda_init, causal=w.causal, eps=w.eps,
+                         out=out)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev4, ev5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev4.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ev5.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = ev4.elapsed_time(ev5)
+
+    # ---- reduce over ranks (max time), aggregate throughput over all ranks
+    prefill_ms = max_over_ranks(prefill_ms, world)
+    decode_ms = max_over_ranks(decode_ms, world)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    if rank != 0:
+        return
+
+    flops = prefill_flops(w.B, w.L, w.h_s, w.h_n, w.d, w.dv, w.causal)
+    ms_per_step = prefill_ms / args.steps
+    value = world * flops * args.steps / (prefill_ms * 1e-3) / 1e12
+    per_launch_s = ms_per_step * 1e-3
+    achieved = flops / per_launch_s / 1e12
+    traffic, traffic_wl = profiled_traffic()
+    dec_bytes = decode_bytes(lens_host, dw.h_s, dw.h_n, dw.d, dw.dv)
+    dec_ms_step = decode_ms / dec_steps
+    dec_gbs = dec_bytes / (dec_ms_step * 1e-3) / 1e9
+    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) tensors at the workload's shapes)",
+        "config": {
+            "workload": w.name, "B": w.B, "L": w.L, "h_s": w.h_s, "h_n": w.h_n, "d": w.d,
+            "dv": w.dv, "causal": w.causal, "lambda_init": w.lambda_init,
+            "flop_count": "causal pairs x (2d(h_s+h_n) + 4 dv h_s)",
+            "flops_per_step": flops,
+            "min_flops_per_step": prefill_min_flops(w.B, w.L, w.h_s, w.h_n, w.d, w.dv),
+            "l2": f"{N_INPUT_SETS} rotating input sets ({N_INPUT_SETS} x "
+                  f"{sum(t.numel() * t.element_size() for t in sets[0]) / 1e6:.0f} MB) > 129 MB L2",
+            "parallelism": f"{world} independent replica(s), no collective on the data path",
+        },
+        "roofline": {
+            "kernel": "gda_prefill_tc_kernel<64>",
+            "bound": "tensor",
+            "achieved": achieved,
+            "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"],
+            "traffic": traffic,
+            "traffic_workload": traffic_wl,
+            "peak_source": f"{peak_src}: dense bf16 burst (cuBLAS)",
+        },
+        "decode": {
+            "workload": dw.name,
+            "value": dec_gbs,
+            "unit": "GB/s",
+            "ms_per_step": dec_ms_step,
+            "steps": dec_steps,
+            "bytes_per_step": dec_bytes,
+            "gpu_launches": 2 * dec_steps,
+            "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
+                         "traffic": None, "peak_source": f"{peak_src}: HBM copy"},
+        },
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "device_error_word": dev_err,
+    }
+    if world == 1:
+        cpu_value, nrows, spent, cores = oracle_rows_throughput(w, rows_per_sample=8,
+                                                                target_s=args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": cpu_value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{nrows} query rows (all {w.B} sequences x {w.h_s} heads) of the same "
+                      f"workload, {spent:.1f} s of float64 oracle time"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    from grouped_differential_attention_gb300 import workloads as W
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["gda", "reference"], default="gda")
+    ap.add_argument("--workload", default=W.GDA3_PREFILL_L2048.name,
+                    choices=sorted(n for n, x in W.PREFILL_WORKLOADS.items() if x.dtype == "bf16"))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.gpus != world and world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_gda(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,6 +1,223 @@
-"""Grouped differential attention on GB300 (sm_103a): Python binding (WIP)."""
+"""Grouped differential attention on NVIDIA GB300 (sm_103a).
+
+Python binding of ``libgda.so`` (C ABI in ``include/gda.h``).  The functions
+below carry the C names and only marshal arguments: they check dtypes,
+shapes, devices and contiguity on the PyTorch side, then pass raw device
+pointers and the current CUDA stream to the library, whose kernels do every
+step of the computation.  There is no CPU or PyTorch fallback: if the
+library is missing, every call raises.
+
+Operation (see ``include/gda.h``): for signal head h with noise head
+g = h // (h_s // h_n),
+
+    y_h = (1 - lambda_init) * RMSNorm( (softmax(Q1_h K1_h^T / sqrt d)
+                                        - lambda_h softmax(Q2_g K2_g^T / sqrt d)) V_h )
+
+Layouts: q_sig, k_sig [B, L, h_s, d]; q_noise, k_noise [B, L, h_n, d];
+v and the output [B, L, h_s, dv]; lambda [h_s] float32.
+"""
+from __future__ import annotations
+
+import ctypes
 import math
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "GDAError", "gda_attn_fwd", "gda_attn_fwd_f32", "gda_attn_decode",
+    "gda_attn_decode_workspace_size", "gda_status_string", "gda_device_error",
+    "lambda_init_schedule", "library_path", "GDA_FLAG_NO_NORM",
+]
+
+GDA_OK = 0
+GDA_ERR_INVALID_ARG = -1
+GDA_ERR_UNSUPPORTED = -2
+GDA_ERR_MISALIGNED = -3
+GDA_ERR_WORKSPACE = -4
+GDA_ERR_CUDA = -5
+GDA_ERR_DEVICE_TIMEOUT = -6
+GDA_FLAG_NO_NORM = 0x1
+GDA_DEVERR_PREFILL_TIMEOUT = 0x1
+GDA_DEVERR_BAD_LENGTH = 0x2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libgda.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class GDAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {gda_status_string(status)} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with "
+                    "`python -m grouped_differential_attention_gb300.build`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P, I, F, U, Z = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint,
+                             ctypes.c_size_t)
+            fwd = [P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, F]
+            lib.gda_attn_fwd.argtypes = fwd + [P]
+            lib.gda_attn_fwd_ex.argtypes = fwd + [U, P]
+            lib.gda_attn_fwd_f32.argtypes = fwd + [P]
+            lib.gda_attn_fwd_f32_ex.argtypes = fwd + [U, P]
+            lib.gda_attn_decode_workspace_size.argtypes = [I, I, I, I, I]
+            lib.gda_attn_decode_workspace_size.restype = Z
+            lib.gda_attn_decode.argtypes = [P, P, P, P, P, P, P, F, P, I, I, I, I, I, I, F, P, Z, P]
+            lib.gda_status_string.argtypes = [I]
+            lib.gda_status_string.restype = ctypes.c_char_p
+            lib.gda_device_error.argtypes = [I]
+            for name in ("gda_attn_fwd", "gda_attn_fwd_ex", "gda_attn_fwd_f32",
+                         "gda_attn_fwd_f32_ex", "gda_attn_decode", "gda_device_error"):
+                getattr(lib, name).restype = I
+            _lib = lib
+    return _lib
+
+
+def gda_status_string(status: int) -> str:
+    return _load().gda_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != GDA_OK:
+        raise GDAError(rc, what)
+
+
+def _expect(t, name, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _prefill(entry, dtype, q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init, causal, eps,
+             out, flags):
+    dev = q_sig.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if q_sig.dim() != 4 or q_noise.dim() != 4 or v.dim() != 4:
+        raise ValueError("q_sig, q_noise and v must be 4-D [B, L, heads, dim]")
+    B, L, hs, d = q_sig.shape
+    hn = q_noise.shape[2]
+    dv = v.shape[3]
+    _expect(q_sig, "q_sig", dtype, (B, L, hs, d), dev)
+    _expect(k_sig, "k_sig", dtype, (B, L, hs, d), dev)
+    _expect(q_noise, "q_noise", dtype, (B, L, hn, d), dev)
+    _expect(k_noise, "k_noise", dtype, (B, L, hn, d), dev)
+    _expect(v, "v", dtype, (B, L, hs, dv), dev)
+    _expect(lam, "lam", torch.float32, (hs,), dev)
+    if out is None:
+        out = torch.empty((B, L, hs, dv), dtype=dtype, device=dev)
+    _expect(out, "out", dtype, (B, L, hs, dv), dev)
+    with torch.cuda.device(dev):
+        rc = entry(_ptr(q_sig), _ptr(k_sig), _ptr(q_noise), _ptr(k_noise), _ptr(v), _ptr(lam),
+                   float(lambda_init), _ptr(out), B, L, hs, hn, d, dv, int(bool(causal)),
+                   float(eps), int(flags), _stream(dev))
+    _check(rc, "gda prefill")
+    return out
+
+
+def gda_attn_fwd(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float, *,
+                 causal: bool = True, eps: float = 1e-5, out=None, flags: int = 0):
+    """bf16 prefill on the tensor cores (tcgen05/TMEM, TMA); returns ``out``."""
+    return _prefill(_load().gda_attn_fwd_ex, torch.bfloat16, q_sig, k_sig, q_noise, k_noise, v,
+                    lam, lambda_init, causal, eps, out, flags)
+
+
+def gda_attn_fwd_f32(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float, *,
+                     causal: bool = True, eps: float = 1e-5, out=None, flags: int = 0):
+    """float32 prefill on the CUDA cores; returns ``out``."""
+    return _prefill(_load().gda_attn_fwd_f32_ex, torch.float32, q_sig, k_sig, q_noise, k_noise,
+                    v, lam, lambda_init, causal, eps, out, flags)
+
+
+def gda_attn_decode_workspace_size(B: int, Lcap: int, h_s: int, h_n: int, dv: int) -> int:
+    return int(_load().gda_attn_decode_workspace_size(B, Lcap, h_s, h_n, dv))
+
+
+def gda_attn_decode(q_sig, q_noise, k_sig_cache, k_noise_cache, v_cache, cache_lens, lam,
+                    lambda_init: float, *, eps: float = 1e-5, out=None, workspace=None):
+    """bf16 decode of one query token per sequence over its KV cache; returns ``out``.
+
+    ``workspace`` (a CUDA uint8 tensor of at least
+    ``gda_attn_decode_workspace_size(...)`` bytes) is allocated here when not
+    given.
+    """
+    dev = q_sig.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if q_sig.dim() != 3 or k_sig_cache.dim() != 4 or v_cache.dim() != 4:
+        raise ValueError("bad ranks: q [B, heads, d], caches [B, Lcap, heads, dim]")
+    B, hs, d = q_sig.shape
+    hn = q_noise.shape[1]
+    Lcap = k_sig_cache.shape[1]
+    dv = v_cache.shape[3]
+    bf = torch.bfloat16
+    _expect(q_sig, "q_sig", bf, (B, hs, d), dev)
+    _expect(q_noise, "q_noise", bf, (B, hn, d), dev)
+    _expect(k_sig_cache, "k_sig_cache", bf, (B, Lcap, hs, d), dev)
+    _expect(k_noise_cache, "k_noise_cache", bf, (B, Lcap, hn, d), dev)
+    _expect(v_cache, "v_cache", bf, (B, Lcap, hs, dv), dev)
+    _expect(cache_lens, "cache_lens", torch.int32, (B,), dev)
+    _expect(lam, "lam", torch.float32, (hs,), dev)
+    if out is None:
+        out = torch.empty((B, hs, dv), dtype=bf, device=dev)
+    _expect(out, "out", bf, (B, hs, dv), dev)
+    need = gda_attn_decode_workspace_size(B, Lcap, hs, hn, dv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(dev):
+        rc = _load().gda_attn_decode(
+            _ptr(q_sig), _ptr(q_noise), _ptr(k_sig_cache), _ptr(k_noise_cache), _ptr(v_cache),
+            _ptr(cache_lens), _ptr(lam), float(lambda_init), _ptr(out), B, Lcap, hs, hn, d, dv,
+            float(eps), _ptr(workspace), ws_bytes, _stream(dev))
+    _check(rc, "gda decode")
+    return out
+
+
+def gda_device_error(clear: bool = True) -> int:
+    """Device error word of the current device (synchronises it); see include/gda.h."""
+    rc = _load().gda_device_error(int(bool(clear)))
+    if rc < 0:
+        raise GDAError(rc, "gda_device_error")
+    return rc
 
 
 def lambda_init_schedule(layer: int) -> float:
+    """lambda_init of 1-based layer ``layer``: 0.8 - 0.6 exp(-0.3 (layer - 1)).
+
+    The depth schedule of "Differential Attention in Large Language Models
+    ...", section "Learnable Lambda Re-parameterization" (0.2 in the first
+    layer, rising toward 0.8).  A host-side constant for a layer's call.
+    """
     return 0.8 - 0.6 * math.exp(-0.3 * (layer - 1))

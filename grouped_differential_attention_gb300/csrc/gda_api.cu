@@ -1,0 +1,235 @@
+// C ABI of libgda.so (declared in include/gda.h): argument validation,
+// device checks, TMA descriptor encoding and dispatch to the kernels.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "gda.h"
+#include "gda_internal.h"
+
+// Device error word (one per device that loads the library).  Kernels set
+// GDA_DEVERR_* bits here instead of trapping.
+__device__ unsigned g_gda_device_error;
+
+namespace gda {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    std::once_flag once;
+    int status = GDA_ERR_CUDA;     // GDA_OK once the device checked out
+    unsigned *err_word = nullptr;  // device address of g_gda_device_error
+};
+DeviceState g_dev[kMaxDevices];
+
+// Checks the current device once: compute capability 10.3 (GB300) and the
+// address of the error word.  Returns a gda_status and the word's address.
+int current_device(unsigned **err_word) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GDA_ERR_CUDA;
+    }
+    DeviceState &s = g_dev[dev];
+    std::call_once(s.once, [&s, dev]() {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            s.status = GDA_ERR_CUDA;
+            return;
+        }
+        if (major != 10 || minor != 3) {
+            s.status = GDA_ERR_UNSUPPORTED;
+            return;
+        }
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_gda_device_error) != cudaSuccess) {
+            cudaGetLastError();
+            s.status = GDA_ERR_CUDA;
+            return;
+        }
+        s.err_word = static_cast<unsigned *>(addr);
+        s.status = GDA_OK;
+    });
+    *err_word = s.err_word;
+    return s.status;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_prefill_common(const void *q1, const void *k1, const void *q2, const void *k2,
+                         const void *v, const float *lam, float lambda_init, const void *out, int B,
+                         int L, int hs, int hn, int d, int dv, int causal, float eps,
+                         unsigned flags) {
+    if (!q1 || !k1 || !q2 || !k2 || !v || !lam || !out) return GDA_ERR_INVALID_ARG;
+    if (B < 1 || L < 1 || hs < 1 || hn < 1 || d < 1 || dv < 1) return GDA_ERR_INVALID_ARG;
+    if (hs % hn != 0) return GDA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return GDA_ERR_INVALID_ARG;
+    if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(lambda_init)) return GDA_ERR_INVALID_ARG;
+    if (flags & ~GDA_FLAG_NO_NORM) return GDA_ERR_INVALID_ARG;
+    // element counts must fit the 64-bit index arithmetic with room to spare
+    const double elems = static_cast<double>(B) * L * (hs > hn ? hs : hn) * (d > dv ? d : dv);
+    if (elems > 9.0e15) return GDA_ERR_INVALID_ARG;
+    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+        !aligned16(lam) || !aligned16(out))
+        return GDA_ERR_MISALIGNED;
+    return GDA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+}  // namespace
+
+bool encode_tmap_4d_bf16(CUtensorMap *map, const void *base, const uint64_t dims[4],
+                         const uint64_t strides_bytes[3], const uint32_t box[4]) {
+    std::call_once(g_encode_once, []() {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    if (!g_encode) return false;
+    cuuint64_t gdim[4] = {dims[0], dims[1], dims[2], dims[3]};
+    cuuint64_t gstr[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+    cuuint32_t bdim[4] = {box[0], box[1], box[2], box[3]};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), gdim,
+                                gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace gda
+
+using namespace gda;
+
+extern "C" {
+
+int gda_attn_fwd_ex(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,
+                    const void *v, const float *lambda, float lambda_init, void *out, int B, int L,
+                    int h_s, int h_n, int d, int dv, int causal, float eps, unsigned flags,
+                    gda_stream_t stream) {
+    int st = check_prefill_common(q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L,
+                                  h_s, h_n, d, dv, causal, eps, flags);
+    if (st != GDA_OK) return st;
+    if (!(d == 64 || d == 128) || !(dv == 128 || dv == 256)) return GDA_ERR_UNSUPPORTED;
+    unsigned *err = nullptr;
+    st = current_device(&err);
+    if (st != GDA_OK) return st;
+    PrefillArgs a{q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L, h_s, h_n,
+                  d, dv, causal, eps, flags, err};
+    return launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gda_attn_fwd(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,
+                 const void *v, const float *lambda, float lambda_init, void *out, int B, int L,
+                 int h_s, int h_n, int d, int dv, int causal, float eps, gda_stream_t stream) {
+    return gda_attn_fwd_ex(q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L, h_s,
+                           h_n, d, dv, causal, eps, 0u, stream);
+}
+
+int gda_attn_fwd_f32_ex(const float *q_sig, const float *k_sig, const float *q_noise,
+                        const float *k_noise, const float *v, const float *lambda,
+                        float lambda_init, float *out, int B, int L, int h_s, int h_n, int d,
+                        int dv, int causal, float eps, unsigned flags, gda_stream_t stream) {
+    int st = check_prefill_common(q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L,
+                                  h_s, h_n, d, dv, causal, eps, flags);
+    if (st != GDA_OK) return st;
+    if (d > 256 || dv % 32 != 0 || dv > 256) return GDA_ERR_UNSUPPORTED;
+    if (h_s > 65535 || B > 65535) return GDA_ERR_UNSUPPORTED;
+    unsigned *err = nullptr;
+    st = current_device(&err);
+    if (st != GDA_OK) return st;
+    PrefillArgs a{q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L, h_s, h_n,
+                  d, dv, causal, eps, flags, err};
+    return launch_prefill_f32(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gda_attn_fwd_f32(const float *q_sig, const float *k_sig, const float *q_noise,
+                     const float *k_noise, const float *v, const float *lambda, float lambda_init,
+                     float *out, int B, int L, int h_s, int h_n, int d, int dv, int causal,
+                     float eps, gda_stream_t stream) {
+    return gda_attn_fwd_f32_ex(q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L,
+                               h_s, h_n, d, dv, causal, eps, 0u, stream);
+}
+
+size_t gda_attn_decode_workspace_size(int B, int Lcap, int h_s, int h_n, int dv) {
+    if (B < 1 || Lcap < 1 || h_s < 1 || h_n < 1 || dv < 1 || h_s % h_n != 0) return 0;
+    return decode_plan(B, Lcap, h_s, h_n, dv).bytes;
+}
+
+int gda_attn_decode(const void *q_sig, const void *q_noise, const void *k_sig_cache,
+                    const void *k_noise_cache, const void *v_cache, const int *cache_lens,
+                    const float *lambda, float lambda_init, void *out, int B, int Lcap, int h_s,
+                    int h_n, int d, int dv, float eps, void *workspace, size_t workspace_bytes,
+                    gda_stream_t stream) {
+    if (!q_sig || !q_noise || !k_sig_cache || !k_noise_cache || !v_cache || !cache_lens || !lambda ||
+        !out)
+        return GDA_ERR_INVALID_ARG;
+    if (B < 1 || Lcap < 1 || h_s < 1 || h_n < 1 || d < 1 || dv < 1 || h_s % h_n != 0)
+        return GDA_ERR_INVALID_ARG;
+    if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(lambda_init)) return GDA_ERR_INVALID_ARG;
+    if (static_cast<double>(B) * Lcap * h_s * (d > dv ? d : dv) > 9.0e15) return GDA_ERR_INVALID_ARG;
+    if (!(d == 64 || d == 128) || !(dv == 64 || dv == 128 || dv == 256)) return GDA_ERR_UNSUPPORTED;
+    if ((h_s * d + h_n * d + h_s * dv) / 8 > 1024 || h_s + h_n > 128 || B > 65535)
+        return GDA_ERR_UNSUPPORTED;
+    if (!aligned16(q_sig) || !aligned16(q_noise) || !aligned16(k_sig_cache) ||
+        !aligned16(k_noise_cache) || !aligned16(v_cache) || !aligned16(cache_lens) ||
+        !aligned16(lambda) || !aligned16(out))
+        return GDA_ERR_MISALIGNED;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < gda_attn_decode_workspace_size(B, Lcap, h_s, h_n, dv))
+        return GDA_ERR_WORKSPACE;
+    unsigned *err = nullptr;
+    const int st = current_device(&err);
+    if (st != GDA_OK) return st;
+    DecodeArgs a{q_sig, q_noise, k_sig_cache, k_noise_cache, v_cache, cache_lens, lambda, lambda_init,
+                 out, B, Lcap, h_s, h_n, d, dv, eps, workspace, workspace_bytes, err};
+    return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *gda_status_string(int status) {
+    switch (status) {
+        case GDA_OK: return "success";
+        case GDA_ERR_INVALID_ARG: return "invalid argument";
+        case GDA_ERR_UNSUPPORTED: return "unsupported configuration or device";
+        case GDA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case GDA_ERR_WORKSPACE: return "workspace missing or too small";
+        case GDA_ERR_CUDA: return "CUDA runtime or driver error";
+        case GDA_ERR_DEVICE_TIMEOUT: return "a kernel wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int gda_device_error(int clear) {
+    unsigned *err = nullptr;
+    const int st = current_device(&err);
+    if (st != GDA_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return GDA_ERR_CUDA;
+    }
+    unsigned v = 0;
+    if (cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GDA_ERR_CUDA;
+    }
+    if (clear && cudaMemset(err, 0, sizeof(unsigned)) != cudaSuccess) {
+        cudaGetLastError();
+        return GDA_ERR_CUDA;
+    }
+    return static_cast<int>(v & 0x7fffffffu);
+}
+
+}  // extern "C"

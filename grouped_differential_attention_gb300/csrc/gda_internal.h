@@ -1,0 +1,56 @@
+// Internal host-side interface between the C ABI (gda_api.cu) and the kernel
+// translation units.  Not installed, not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace gda {
+
+struct PrefillArgs {
+    const void *q1, *k1, *q2, *k2, *v;   // see include/gda.h for layouts
+    const float *lambda;
+    float lambda_init;
+    void *out;
+    int B, L, hs, hn, d, dv;
+    int causal;
+    float eps;
+    unsigned flags;
+    unsigned *dev_err;                  // device error word of the current device
+};
+
+struct DecodeArgs {
+    const void *q1, *q2, *k1c, *k2c, *vc;
+    const int *lens;
+    const float *lambda;
+    float lambda_init;
+    void *out;
+    int B, Lcap, hs, hn, d, dv;
+    float eps;
+    void *workspace;
+    size_t workspace_bytes;
+    unsigned *dev_err;
+};
+
+// Each launcher validates nothing (the ABI layer did) and returns a
+// gda_status value.
+int launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
+int launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream);
+int launch_decode(const DecodeArgs &a, cudaStream_t stream);
+
+// Split plan of the decode kernel (positions per split and split count).
+struct DecodePlan {
+    int chunk;        // cache positions handled by one CTA
+    int splits;       // ceil(Lcap / chunk)
+    size_t bytes;     // workspace bytes
+};
+DecodePlan decode_plan(int B, int Lcap, int hs, int hn, int dv);
+
+// 4-D bf16 tensor map, 128-byte swizzle, dims/box innermost first, strides
+// in bytes for dims 1..3.  Returns false if the driver rejects it.
+bool encode_tmap_4d_bf16(CUtensorMap *map, const void *base, const uint64_t dims[4],
+                         const uint64_t strides_bytes[3], const uint32_t box[4]);
+
+}  // namespace gda

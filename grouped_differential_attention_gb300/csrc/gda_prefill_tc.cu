@@ -1,0 +1,539 @@
+// Causal (or full) grouped differential attention prefill for sm_103a:
+// TMA-staged bf16 tiles, tcgen05 MMAs accumulating in TMEM, two online
+// softmax states and the fused difference + headwise RMSNorm epilogue.
+//
+// What it computes: for signal head h with noise head g = h / (h_s / h_n),
+//   o = softmax(Q1_h K1_h^T / sqrt d) V_h - lambda_h softmax(Q2_g K2_g^T / sqrt d) V_h
+//   y = (1 - lambda_init) o / sqrt(mean(o^2) + eps)
+// ("Differential Attention in Large Language Models ...", sections
+// "Differential Attention Architecture" and "Headwise Normalization";
+// noise-head sharing from the "Grouped Differential Attention" abstract).
+// Both maps are normalised before the subtraction, so the kernel carries two
+// running (max, sum) states and two float32 accumulators per query row; no
+// L x L map ever leaves the SM.
+//
+// CTA = (query tile of 128 rows, batch b, signal head h, dv slice of 128).
+// 10 warps:
+//   warp 0      TMA producer (one elected lane): Q1/Q2 once, then a ring of
+//               stages each holding a K1, K2 and V tile;
+//   warp 1      TMEM allocator and MMA issuer (one elected lane);
+//   warps 2-5   softmax of the signal map  (thread = query row = TMEM lane);
+//   warps 6-9   softmax of the noise map.
+// TMEM (512 columns): O1 [0,128) | O2 [128,256) | S1 [256,256+BN) |
+// S2 [256+BN,256+2BN).  P (bf16) overwrites the first BN/2 columns of its S
+// tile and feeds the PV MMA straight from TMEM.  The two maps ping-pong:
+// while one softmax group works, the tensor core runs the other map's PV and
+// next QK.  A row's running max is only moved when it grows by more than
+// 2^8 (in exp2 units), and only then is its accumulator rescaled.
+// dv = 256 is split over a 2-CTA cluster; the two CTAs exchange the per-row
+// sum of squares through distributed shared memory for the RMSNorm.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <cmath>
+
+#include "gda.h"
+#include "gda_device.cuh"
+#include "gda_internal.h"
+
+namespace gda {
+namespace {
+
+constexpr int kBM = 128;          // query rows per CTA (= TMEM lanes)
+constexpr int kDVS = 128;         // dv columns per CTA
+constexpr int kThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <int D> struct TcCfg;
+template <> struct TcCfg<64> { static constexpr int BN = 128, STAGES = 2; };
+template <> struct TcCfg<128> { static constexpr int BN = 64, STAGES = 3; };
+
+struct Ctrl {
+    uint64_t q_full;
+    uint64_t kv_full[4];
+    uint64_t kv_empty[4];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_done[2];
+    uint64_t mma_idle;
+    uint32_t tmem_base;
+    int abort_flag;
+    float l_row[2][kBM];
+    float ss_part[2][kBM];
+    float ss_peer[kBM];
+};
+
+template <int D> struct Layout {
+    static constexpr int BN = TcCfg<D>::BN;
+    static constexpr int S = TcCfg<D>::STAGES;
+    static constexpr int Q_BYTES = kBM * D * 2;
+    static constexpr int K_BYTES = BN * D * 2;
+    static constexpr int V_BYTES = BN * kDVS * 2;
+    static constexpr int STAGE_BYTES = 2 * K_BYTES + V_BYTES;
+    static constexpr int OFF_Q1 = 0;
+    static constexpr int OFF_Q2 = Q_BYTES;
+    static constexpr int OFF_ST = 2 * Q_BYTES;
+    static constexpr int TILES = OFF_ST + S * STAGE_BYTES;
+    static constexpr int TOTAL = TILES + (int)((sizeof(Ctrl) + 1023) / 1024) * 1024 + 1024;
+    static_assert(TOTAL <= 232448, "shared memory budget");
+    static_assert(256 + 2 * BN <= 512, "TMEM budget");
+};
+
+struct TcParams {
+    const float *lambda;
+    __nv_bfloat16 *out;
+    unsigned *err;
+    float lambda_init, eps, scale_log2;
+    int B, L, hs, hn, dv, causal, nslices, nqt, no_norm;
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32(const float *local, uint32_t peer, float v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(peer));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+// Wait used while winding down: ignores the abort flag, still bounded.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
+    int dummy = 0;
+    mbar_wait(bar, parity, err, GDA_DEVERR_PREFILL_TIMEOUT, &dummy);
+}
+
+// Whole-warp wait: every lane polls, the result is agreed by vote so the
+// warp stays converged for the .sync.aligned tcgen05 instructions after it.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsigned *err,
+                                          volatile int *abort) {
+    bool ok = mbar_wait(bar, parity, err, GDA_DEVERR_PREFILL_TIMEOUT, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t qa, uint32_t ka) {
+    using LY = Layout<D>;
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, LY::BN, 0);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+        const uint32_t blk = k / 4, sub = (k % 4) * 32;
+        const uint64_t a = smem_desc_sw128(qa + blk * (kBM * 128) + sub, 16, 1024);
+        const uint64_t b = smem_desc_sw128(ka + blk * (LY::BN * 128) + sub, 16, 1024);
+        mma_ss(tS, a, b, idesc, k > 0 ? 1u : 0u);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t va, bool acc) {
+    using LY = Layout<D>;
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kDVS, 1);
+#pragma unroll
+    for (int k = 0; k < LY::BN / 16; ++k) {
+        // V stage: two [BN x 64] column blocks, rows of 128 B, 128-B swizzle.
+        // MN-major B: 8-row K groups 1024 B apart, 64-column N blocks BN*128 B apart.
+        const uint64_t b = smem_desc_sw128(va + k * 2048, LY::BN * 128, 1024);
+        mma_ts(tO, tP + k * 8, b, idesc, (acc || k > 0) ? 1u : 0u);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
+                      const __grid_constant__ CUtensorMap tmK1,
+                      const __grid_constant__ CUtensorMap tmQ2,
+                      const __grid_constant__ CUtensorMap tmK2,
+                      const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+    using LY = Layout<D>;
+    constexpr int BN = LY::BN;
+    constexpr int S = LY::S;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Ctrl *ctl = reinterpret_cast<Ctrl *>(smem + LY::TILES);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    // ---- work item: longest (last) query tiles are launched first
+    int c = blockIdx.x;
+    const int slice = c % p.nslices;
+    c /= p.nslices;
+    const int h = c % p.hs;
+    c /= p.hs;
+    const int b = c % p.B;
+    c /= p.B;
+    const int qt = p.nqt - 1 - c;
+    const int q0 = qt * kBM;
+    const int g = h / (p.hs / p.hn);
+    const int kv_end = p.causal ? min(p.L, q0 + kBM) : p.L;
+    const int nkv = (kv_end + BN - 1) / BN;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&ctl->q_full, 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&ctl->kv_full[s], 1);
+            mbar_init(&ctl->kv_empty[s], 1);
+        }
+        for (int m = 0; m < 2; ++m) {
+            mbar_init(&ctl->s_full[m], 1);
+            mbar_init(&ctl->p_full[m], 128);
+            mbar_init(&ctl->o_done[m], 1);
+        }
+        mbar_init(&ctl->mma_idle, 1);
+        ctl->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (p.nslices == 2) cluster_sync_all();   // peer CTA is running before any DSMEM access
+    const uint32_t tmem = ctl->tmem_base;
+    volatile int *abort_flag = &ctl->abort_flag;
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        if (elect_one()) {
+            tma_prefetch_desc(&tmQ1);
+            tma_prefetch_desc(&tmK1);
+            tma_prefetch_desc(&tmQ2);
+            tma_prefetch_desc(&tmK2);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(&ctl->q_full, 2 * LY::Q_BYTES);
+#pragma unroll
+            for (int blk = 0; blk < D / 64; ++blk) {
+                tma_load_4d(smem + LY::OFF_Q1 + blk * kBM * 128, &tmQ1, &ctl->q_full, blk * 64, h, q0, b);
+                tma_load_4d(smem + LY::OFF_Q2 + blk * kBM * 128, &tmQ2, &ctl->q_full, blk * 64, g, q0, b);
+            }
+            int issued = 0;
+            for (int j = 0; j < nkv; ++j) {
+                const int st = j % S;
+                if (j >= S && !mbar_wait(&ctl->kv_empty[st], ((j / S) - 1) & 1, p.err,
+                                         GDA_DEVERR_PREFILL_TIMEOUT, abort_flag))
+                    break;
+                uint8_t *sb = smem + LY::OFF_ST + st * LY::STAGE_BYTES;
+                mbar_arrive_expect_tx(&ctl->kv_full[st], LY::STAGE_BYTES);
+#pragma unroll
+                for (int blk = 0; blk < D / 64; ++blk) {
+                    tma_load_4d(sb + blk * BN * 128, &tmK1, &ctl->kv_full[st], blk * 64, h, j * BN, b);
+                    tma_load_4d(sb + LY::K_BYTES + blk * BN * 128, &tmK2, &ctl->kv_full[st], blk * 64, g, j * BN, b);
+                }
+#pragma unroll
+                for (int blk = 0; blk < kDVS / 64; ++blk)
+                    tma_load_4d(sb + 2 * LY::K_BYTES + blk * BN * 128, &tmV, &ctl->kv_full[st],
+                                slice * kDVS + blk * 64, h, j * BN, b);
+                ++issued;
+            }
+            // our own copies must land before the CTA may exit
+            drain_wait(&ctl->q_full, 0, p.err);
+            for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
+                drain_wait(&ctl->kv_full[j % S], (j / S) & 1, p.err);
+        }
+        __syncwarp();
+        if (p.nslices == 2) cluster_sync_all();
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        if (elect_one()) {
+            const uint32_t tO1 = tmem, tO2 = tmem + 128;
+            const uint32_t tS1 = tmem + 256, tS2 = tmem + 256 + BN;
+            const uint32_t q1a = smem_u32(smem + LY::OFF_Q1);
+            const uint32_t q2a = smem_u32(smem + LY::OFF_Q2);
+            const uint32_t st0 = smem_u32(smem + LY::OFF_ST);
+            bool ok = mbar_wait(&ctl->q_full, 0, p.err, GDA_DEVERR_PREFILL_TIMEOUT, abort_flag) &&
+                      mbar_wait(&ctl->kv_full[0], 0, p.err, GDA_DEVERR_PREFILL_TIMEOUT, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_qk<D>(tS1, q1a, st0);
+                mma_commit(&ctl->s_full[0]);
+                issue_qk<D>(tS2, q2a, st0 + LY::K_BYTES);
+                mma_commit(&ctl->s_full[1]);
+            }
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int st = j % S;
+                const uint32_t sb = st0 + st * LY::STAGE_BYTES;
+                const bool more = j + 1 < nkv;
+                const uint32_t sb1 = st0 + ((j + 1) % S) * LY::STAGE_BYTES;
+                // signal map: PV1(j), then QK1(j+1) into the freed S1 tile
+                if (!mbar_wait(&ctl->p_full[0], j & 1, p.err, GDA_DEVERR_PREFILL_TIMEOUT, abort_flag)) break;
+                tc_fence_after();
+                issue_pv<D>(tO1, tS1, sb + 2 * LY::K_BYTES, j > 0);
+                mma_commit(&ctl->o_done[0]);
+                if (more) {
+                    if (!mbar_wait(&ctl->kv_full[(j + 1) % S], ((j + 1) / S) & 1, p.err,
+                                   GDA_DEVERR_PREFILL_TIMEOUT, abort_flag))
+                        break;
+                    tc_fence_after();
+                    issue_qk<D>(tS1, q1a, sb1);
+                    mma_commit(&ctl->s_full[0]);
+                }
+                // noise map: PV2(j), release the stage, then QK2(j+1)
+                if (!mbar_wait(&ctl->p_full[1], j & 1, p.err, GDA_DEVERR_PREFILL_TIMEOUT, abort_flag)) break;
+                tc_fence_after();
+                issue_pv<D>(tO2, tS2, sb + 2 * LY::K_BYTES, j > 0);
+                mma_commit(&ctl->o_done[1]);
+                mma_commit(&ctl->kv_empty[st]);
+                if (more) {
+                    issue_qk<D>(tS2, q2a, sb1 + LY::K_BYTES);
+                    mma_commit(&ctl->s_full[1]);
+                }
+            }
+            // every issued MMA completes before TMEM is released
+            mma_commit(&ctl->mma_idle);
+            drain_wait(&ctl->mma_idle, 0, p.err);
+        }
+        __syncwarp();
+        if (p.nslices == 2) cluster_sync_all();
+    } else {
+        // ================================================= softmax groups
+        const int m = (warp - 2) / 4;             // 0: signal map, 1: noise map
+        const int quarter = warp % 4;             // TMEM lanes this warp may touch
+        const int row = quarter * 32 + lane;      // query row in the tile
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem + 256 + m * BN + lane_off;
+        const uint32_t tOm = tmem + m * 128 + lane_off;
+        const int qrow = q0 + row;
+        const int last_key = p.causal ? min(qrow, p.L - 1) : p.L - 1;
+        const float sl2 = p.scale_log2;
+        float m_ref = -INFINITY;
+        float l = 0.f;
+        bool ok = true;
+
+        for (int j = 0; j < nkv; ++j) {
+            if (!warp_wait(&ctl->s_full[m], j & 1, p.err, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const int k0 = j * BN;
+            const bool need_mask = (p.causal && k0 + BN - 1 > q0) || (k0 + BN > p.L);
+            // pass 1: row maximum of the raw logits
+            float mx = -INFINITY;
+#pragma unroll
+            for (int cch = 0; cch < BN / 32; ++cch) {
+                uint32_t r[32];
+                tmem_ld32(tS + cch * 32, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float s = __uint_as_float(r[e]);
+                    if (need_mask && k0 + cch * 32 + e > last_key) s = -INFINITY;
+                    mx = fmaxf(mx, s);
+                }
+            }
+            const float mx_s = mx * sl2;
+            float alpha = 1.f;
+            bool rescale = false;
+            if (j == 0) {
+                m_ref = mx_s;
+            } else if (mx_s > m_ref + kRescaleThreshold) {
+                alpha = fast_exp2(m_ref - mx_s);
+                m_ref = mx_s;
+                rescale = true;
+            }
+            l *= alpha;
+            // pass 2: P = 2^(s*scale - m_ref) as bf16 over the consumed S columns
+#pragma unroll
+            for (int cch = 0; cch < BN / 32; ++cch) {
+                uint32_t r[32];
+                tmem_ld32(tS + cch * 32, r);
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int kj = k0 + cch * 32 + e;
+                    float p0 = fast_exp2(fmaf(__uint_as_float(r[e]), sl2, -m_ref));
+                    float p1 = fast_exp2(fmaf(__uint_as_float(r[e + 1]), sl2, -m_ref));
+                    if (need_mask) {
+                        if (kj > last_key) p0 = 0.f;
+                        if (kj + 1 > last_key) p1 = 0.f;
+                    }
+                    l += p0 + p1;
+                    pk[e / 2] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tS + cch * 16, pk);
+            }
+            tmem_st_wait();
+            if (__any_sync(0xffffffffu, rescale)) {
+                // the accumulator may only be touched once PV(j-1) has completed
+                if (!warp_wait(&ctl->o_done[m], (j - 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int cch = 0; cch < kDVS / 32; ++cch) {
+                    uint32_t r[32];
+                    tmem_ld32(tOm + cch * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                    tmem_st32(tOm + cch * 32, r);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            mbar_arrive(&ctl->p_full[m]);
+        }
+
+        // ---------------------------------------------------- epilogue
+        ctl->l_row[m][row] = l;
+        named_bar_sync(1, 256);
+        const float l1 = ctl->l_row[0][row];
+        const float l2 = ctl->l_row[1][row];
+        ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
+        if (ok) ok = warp_wait(&ctl->o_done[0], (nkv - 1) & 1, p.err, abort_flag);
+        if (ok) ok = warp_wait(&ctl->o_done[1], (nkv - 1) & 1, p.err, abort_flag);
+        tc_fence_after();
+        const float lam = p.lambda[h];
+        const float inv1 = 1.f / l1;
+        const float c2 = lam / l2;
+        const uint32_t tO1 = tmem + lane_off, tO2 = tmem + 128 + lane_off;
+        const int col0 = m * 64;                  // this group's half of the slice
+        float ss = 0.f;
+        if (ok) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t r1[32], r2[32];
+                tmem_ld32(tO1 + col0 + cc * 32, r1);
+                tmem_ld32(tO2 + col0 + cc * 32, r2);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float o = __uint_as_float(r1[e]) * inv1 - __uint_as_float(r2[e]) * c2;
+                    ss = fmaf(o, o, ss);
+                }
+            }
+        }
+        ctl->ss_part[m][row] = ss;
+        named_bar_sync(1, 256);
+        float ss_tot = ctl->ss_part[0][row] + ctl->ss_part[1][row];
+        if (p.nslices == 2) {
+            if (m == 0) st_cluster_f32(&ctl->ss_peer[row], cluster_ctarank() ^ 1u, ss_tot);
+            cluster_sync_all();
+            ss_tot += ctl->ss_peer[row];
+        }
+        const float yscale =
+            p.no_norm ? 1.f : (1.f - p.lambda_init) * rsqrtf(ss_tot / static_cast<float>(p.dv) + p.eps);
+        if (ok) {
+            __nv_bfloat16 *orow =
+                p.out + ((static_cast<size_t>(b) * p.L + qrow) * p.hs + h) * p.dv + slice * kDVS + col0;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t r1[32], r2[32];
+                tmem_ld32(tO1 + col0 + cc * 32, r1);
+                tmem_ld32(tO2 + col0 + cc * 32, r2);
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float y0 = (__uint_as_float(r1[e]) * inv1 - __uint_as_float(r2[e]) * c2) * yscale;
+                    const float y1 = (__uint_as_float(r1[e + 1]) * inv1 - __uint_as_float(r2[e + 1]) * c2) * yscale;
+                    pk[e / 2] = pack_bf16x2(y0, y1);
+                }
+                if (qrow < p.L) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                }
+            }
+        }
+    }
+
+    // ---- teardown: all TMEM traffic of this CTA is complete past this barrier
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+int launch_impl(const PrefillArgs &a, cudaStream_t stream) {
+    using LY = Layout<D>;
+    CUtensorMap mQ1, mK1, mQ2, mK2, mV;
+    const uint64_t B = a.B, L = a.L, hs = a.hs, hn = a.hn, d = a.d, dv = a.dv;
+    {
+        const uint64_t dims[4] = {d, hs, L, B};
+        const uint64_t str[3] = {d * 2, hs * d * 2, L * hs * d * 2};
+        const uint32_t boxq[4] = {64, 1, kBM, 1};
+        const uint32_t boxk[4] = {64, 1, (uint32_t)LY::BN, 1};
+        if (!encode_tmap_4d_bf16(&mQ1, a.q1, dims, str, boxq)) return GDA_ERR_CUDA;
+        if (!encode_tmap_4d_bf16(&mK1, a.k1, dims, str, boxk)) return GDA_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[4] = {d, hn, L, B};
+        const uint64_t str[3] = {d * 2, hn * d * 2, L * hn * d * 2};
+        const uint32_t boxq[4] = {64, 1, kBM, 1};
+        const uint32_t boxk[4] = {64, 1, (uint32_t)LY::BN, 1};
+        if (!encode_tmap_4d_bf16(&mQ2, a.q2, dims, str, boxq)) return GDA_ERR_CUDA;
+        if (!encode_tmap_4d_bf16(&mK2, a.k2, dims, str, boxk)) return GDA_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[4] = {dv, hs, L, B};
+        const uint64_t str[3] = {dv * 2, hs * dv * 2, L * hs * dv * 2};
+        const uint32_t box[4] = {64, 1, (uint32_t)LY::BN, 1};
+        if (!encode_tmap_4d_bf16(&mV, a.v, dims, str, box)) return GDA_ERR_CUDA;
+    }
+    TcParams p;
+    p.lambda = a.lambda;
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
+    p.err = a.dev_err;
+    p.lambda_init = a.lambda_init;
+    p.eps = a.eps;
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.d)));
+    p.B = a.B;
+    p.L = a.L;
+    p.hs = a.hs;
+    p.hn = a.hn;
+    p.dv = a.dv;
+    p.causal = a.causal;
+    p.nslices = a.dv / kDVS;
+    p.nqt = (a.L + kBM - 1) / kBM;
+    p.no_norm = (a.flags & GDA_FLAG_NO_NORM) ? 1 : 0;
+
+    auto kern = gda_prefill_tc_kernel<D>;
+    static bool attr_set = false;   // per process; the attribute is per function
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL) !=
+            cudaSuccess)
+            return GDA_ERR_CUDA;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
+            return GDA_ERR_CUDA;
+        attr_set = true;
+    }
+    const long long grid = static_cast<long long>(p.nqt) * a.B * a.hs * p.nslices;
+    if (grid <= 0 || grid > 0x7fffffffLL) return GDA_ERR_UNSUPPORTED;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = LY::TOTAL;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.nslices;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mQ1, mK1, mQ2, mK2, mV, p);
+    return e == cudaSuccess ? GDA_OK : GDA_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
+    if (a.d == 64) return launch_impl<64>(a, stream);
+    if (a.d == 128) return launch_impl<128>(a, stream);
+    return GDA_ERR_UNSUPPORTED;
+}
+
+}  // namespace gda

@@ -1,0 +1,164 @@
+/*
+ * gda.h -- C ABI of the grouped differential attention library (libgda.so)
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * THE OPERATION
+ *   Grouped differential attention ("Grouped Differential Attention",
+ *   arXiv 2510.06949, abstract) splits the heads of a layer into h_s signal
+ *   heads and h_n <= h_s noise-control heads, h_s a multiple of h_n.  Noise
+ *   head g is shared by the r = h_s / h_n consecutive signal heads
+ *   h = g*r .. g*r + r - 1 (grouped-query style repetition).  For signal head h
+ *   with noise head g = h / r it computes, per query row,
+ *
+ *     o_h = ( softmax(Q1_h K1_h^T / sqrt(d)) - lambda_h * softmax(Q2_g K2_g^T / sqrt(d)) ) V_h
+ *     y_h = (1 - lambda_init) * o_h / sqrt(mean_over_dv(o_h^2) + eps)
+ *
+ *   which is the differential attention operator and its headwise
+ *   normalisation of "Differential Attention in Large Language Models: How
+ *   Denoising Subtraction Eliminates Attention Noise and Outlier
+ *   Activations" (sections "Differential Attention Architecture" and
+ *   "Headwise Normalization"), with the second map taken from the shared
+ *   noise head.  With h_s == h_n it is plain differential attention.  The
+ *   RMSNorm has no learnable gain.  Both softmaxes are normalised before the
+ *   subtraction; the subtraction and the norm are done in float32.
+ *
+ * LAYOUT (all tensors dense, row-major, innermost dimension last)
+ *   q_sig, k_sig : [B, L, h_s, d]      signal queries / keys   (Q1, K1)
+ *   q_noise, k_noise : [B, L, h_n, d]  noise queries / keys    (Q2, K2)
+ *   v            : [B, L, h_s, dv]     values (dv is the 2d of the pages)
+ *   lambda       : [h_s] float32       per signal head; a layer-wide lambda
+ *                                      is the case of equal entries
+ *   out          : [B, L, h_s, dv]     same dtype as the inputs
+ *   Causal masking lets query i see keys 0..i.
+ *
+ * OWNERSHIP AND ASYNCHRONY
+ *   Every pointer is owned by the caller and must stay valid until the work
+ *   enqueued on `stream` has finished.  Device pointers must be device
+ *   memory of the current CUDA device.  The library allocates no device
+ *   memory in these calls; the decode call uses the caller's workspace.  Calls
+ *   only enqueue work on `stream` (NULL = the legacy default stream) and
+ *   return; kernel faults surface at the caller's next synchronisation.
+ *   The library keeps per-device state: a device error word (see
+ *   gda_device_error) and cached driver entry points.
+ *
+ * ERRORS
+ *   Every call returns a gda_status.  Arguments are validated before any
+ *   CUDA call is made; invalid arguments return without enqueuing work.
+ *   Nothing is thrown across the ABI.
+ */
+#ifndef GDA_H
+#define GDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *gda_stream_t;
+
+typedef enum {
+    GDA_OK = 0,
+    GDA_ERR_INVALID_ARG = -1,    /* null pointer, non-positive size, h_s % h_n != 0, ... */
+    GDA_ERR_UNSUPPORTED = -2,    /* valid but not implemented: head dims, device arch */
+    GDA_ERR_MISALIGNED = -3,     /* a pointer is not 16-byte aligned */
+    GDA_ERR_WORKSPACE = -4,      /* decode workspace null or too small */
+    GDA_ERR_CUDA = -5,           /* a CUDA runtime/driver call failed (incl. no device) */
+    GDA_ERR_DEVICE_TIMEOUT = -6  /* a kernel gave up waiting (see gda_device_error) */
+} gda_status;
+
+/* Flags for the *_ex entry points. */
+#define GDA_FLAG_NO_NORM 0x1u    /* return o_h (pre-norm, float32 difference) instead of y_h */
+
+/*
+ * Prefill / full-sequence forward, bf16 I/O, float32 accumulation.
+ *   Inputs and out: bf16 device tensors in the layout above.
+ *   lambda: float32 device array [h_s].
+ *   Supported: d in {64, 128}; dv in {128, 256}; B, L >= 1; h_s % h_n == 0;
+ *   every pointer 16-byte aligned; device sm_103 (GB300).  causal in {0, 1}.
+ *   Output is rounded once to bf16 (round to nearest even).
+ * Computed by hand-written tcgen05/TMA kernels; uses no workspace.
+ */
+int gda_attn_fwd(const void *q_sig, const void *k_sig, const void *q_noise,
+                 const void *k_noise, const void *v, const float *lambda,
+                 float lambda_init, void *out, int B, int L, int h_s, int h_n,
+                 int d, int dv, int causal, float eps, gda_stream_t stream);
+
+/* gda_attn_fwd with flags (GDA_FLAG_NO_NORM). */
+int gda_attn_fwd_ex(const void *q_sig, const void *k_sig, const void *q_noise,
+                    const void *k_noise, const void *v, const float *lambda,
+                    float lambda_init, void *out, int B, int L, int h_s, int h_n,
+                    int d, int dv, int causal, float eps, unsigned flags,
+                    gda_stream_t stream);
+
+/*
+ * Prefill with float32 I/O and float32 arithmetic on the CUDA cores.
+ *   Same layout and meaning as gda_attn_fwd, every tensor float32.
+ *   Supported: 1 <= d <= 256; dv in {32, 64, ..., 256} (multiple of 32).
+ */
+int gda_attn_fwd_f32(const float *q_sig, const float *k_sig, const float *q_noise,
+                     const float *k_noise, const float *v, const float *lambda,
+                     float lambda_init, float *out, int B, int L, int h_s, int h_n,
+                     int d, int dv, int causal, float eps, gda_stream_t stream);
+
+/* gda_attn_fwd_f32 with flags (GDA_FLAG_NO_NORM). */
+int gda_attn_fwd_f32_ex(const float *q_sig, const float *k_sig, const float *q_noise,
+                        const float *k_noise, const float *v, const float *lambda,
+                        float lambda_init, float *out, int B, int L, int h_s, int h_n,
+                        int d, int dv, int causal, float eps, unsigned flags,
+                        gda_stream_t stream);
+
+/*
+ * Bytes of device workspace gda_attn_decode needs for these sizes (it holds
+ * the per-split partial softmax states).  Returns 0 for invalid sizes.
+ */
+size_t gda_attn_decode_workspace_size(int B, int Lcap, int h_s, int h_n, int dv);
+
+/*
+ * Decode: one new query token per sequence attends over its key/value cache
+ * (the operation above for the last row of a causal prefill; the caller has
+ * already appended the new token, so sequence b attends to cache rows
+ * 0 .. cache_lens[b]-1).
+ *   q_sig [B, h_s, d], q_noise [B, h_n, d]                       bf16
+ *   k_sig_cache [B, Lcap, h_s, d], k_noise_cache [B, Lcap, h_n, d],
+ *   v_cache [B, Lcap, h_s, dv]                                   bf16
+ *   cache_lens [B] int32 device array, 1 <= cache_lens[b] <= Lcap
+ *   lambda [h_s] float32 device; out [B, h_s, dv] bf16.
+ *   workspace: device memory of at least
+ *   gda_attn_decode_workspace_size(B, Lcap, h_s, h_n, dv) bytes, 16-byte
+ *   aligned, owned by the caller; its contents need no initialisation.
+ *   Two decode calls that are in flight at the same time need two
+ *   workspaces.  A length outside [1, Lcap] is clamped on the device and
+ *   reported through gda_device_error (GDA_DEVERR_BAD_LENGTH).
+ *   Supported: d in {64, 128}; dv in {64, 128, 256};
+ *   (h_s*d + h_n*d + h_s*dv) / 8 <= 1024.
+ * Split-KV kernel with 16-byte coalesced cache loads plus a combine kernel.
+ */
+int gda_attn_decode(const void *q_sig, const void *q_noise, const void *k_sig_cache,
+                    const void *k_noise_cache, const void *v_cache, const int *cache_lens,
+                    const float *lambda, float lambda_init, void *out, int B, int Lcap,
+                    int h_s, int h_n, int d, int dv, float eps, void *workspace,
+                    size_t workspace_bytes, gda_stream_t stream);
+
+/* Static English description of a gda_status value. */
+const char *gda_status_string(int status);
+
+/* Bits of the device error word. */
+#define GDA_DEVERR_PREFILL_TIMEOUT 0x1u  /* a prefill pipeline wait ran out */
+#define GDA_DEVERR_BAD_LENGTH      0x2u  /* a decode cache length was outside [1, Lcap] */
+
+/*
+ * Reads the error word of the current device (synchronises the device
+ * first).  Kernels never trap: a pipeline wait that runs out (about one
+ * second) sets a bit here and the kernel returns.  If clear != 0 the word is
+ * reset to 0 after reading.  Returns the word (>= 0) or GDA_ERR_CUDA.
+ */
+int gda_device_error(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDA_H */

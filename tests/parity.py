@@ -1,0 +1,53 @@
+"""Tolerances of the GPU-vs-oracle comparisons.
+
+bf16 I/O with float32 accumulation: |got - ref| <= 3e-3 + 2e-2 |ref|,
+elementwise.  float32 path: |got - ref| <= 1e-4 (|ref| + rms_row(ref)), the
+row RMS taken over the head's dv values (a pure relative bound is undefined
+at the zero crossings of the output).
+"""
+import numpy as np
+
+BF16_ATOL = 3e-3
+BF16_RTOL = 2e-2
+F32_REL = 1e-4
+
+
+def _np(x):
+    if hasattr(x, "detach"):
+        x = x.detach().float().cpu().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def bf16_worst(got, ref):
+    got, ref = _np(got), _np(ref)
+    bound = BF16_ATOL + BF16_RTOL * np.abs(ref)
+    ratio = np.abs(got - ref) / bound
+    ratio = np.where(np.isfinite(got), ratio, np.inf)
+    return float(ratio.max()) if ratio.size else 0.0
+
+
+def assert_bf16_close(got, ref, what=""):
+    got, ref = _np(got), _np(ref)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    bound = BF16_ATOL + BF16_RTOL * np.abs(ref)
+    err = np.abs(got - ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.unravel_index(np.argmax(np.where(bad, err / bound, 0)), err.shape)
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} elements outside 3e-3 + 2e-2|ref|; "
+            f"worst at {idx}: got {got[idx]!r} ref {ref[idx]!r}")
+
+
+def assert_f32_close(got, ref, what=""):
+    got, ref = _np(got), _np(ref)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
+    bound = F32_REL * (np.abs(ref) + rms)
+    err = np.abs(got - ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.unravel_index(np.argmax(np.where(bad, err / bound, 0)), err.shape)
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} elements outside 1e-4(|ref|+rms_row); "
+            f"worst at {idx}: got {got[idx]!r} ref {ref[idx]!r}")

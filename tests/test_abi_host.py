@@ -1,0 +1,141 @@
+"""Host-side checks of the C ABI: the library builds for sm_103a, loads
+without a GPU, exports every symbol of include/gda.h, and rejects bad
+arguments with the documented status codes before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gda.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA = 0, -1, -2, -3, -4, -5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from grouped_differential_attention_gb300 import build
+    path = build.build()
+    import grouped_differential_attention_gb300 as gda
+    assert os.path.samefile(path, gda.library_path())
+    return gda._load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("gda_attn_fwd", "gda_attn_fwd_f32", "gda_attn_decode",
+              "gda_attn_decode_workspace_size", "gda_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_is_built_for_sm103a(lib):
+    from grouped_differential_attention_gb300 import build
+    flags = build.compile_flags()
+    i = flags.index("-gencode")
+    assert flags[i + 1] == "arch=compute_103a,code=sm_103a"
+    assert flags.count("-gencode") == 1
+
+
+def test_status_strings(lib):
+    import grouped_differential_attention_gb300 as gda
+    assert gda.gda_status_string(0) == "success"
+    for code in (-1, -2, -3, -4, -5, -6):
+        assert gda.gda_status_string(code) not in ("success", "unknown status")
+    assert gda.gda_status_string(42) == "unknown status"
+
+
+A = 0x10000  # fake, 16-byte aligned addresses: never dereferenced on these paths
+
+
+def fwd(lib, entry="gda_attn_fwd", ptrs=None, B=1, L=128, hs=6, hn=2, d=64, dv=128, causal=1,
+        eps=1e-5, lam_init=0.8):
+    p = ptrs or [A, A + 16, A + 32, A + 48, A + 64, A + 80, A + 96]
+    q1, k1, q2, k2, v, lam, out = (ctypes.c_void_p(x) if x is not None else None for x in p)
+    return getattr(lib, entry)(q1, k1, q2, k2, v, lam, ctypes.c_float(lam_init), out, B, L, hs, hn,
+                               d, dv, causal, ctypes.c_float(eps), None)
+
+
+@pytest.mark.parametrize("entry", ["gda_attn_fwd", "gda_attn_fwd_f32"])
+def test_prefill_rejects_bad_arguments(lib, entry):
+    assert fwd(lib, entry, ptrs=[None, A, A, A, A, A, A]) == INVALID
+    assert fwd(lib, entry, ptrs=[A, A, A, A, A, A, None]) == INVALID
+    assert fwd(lib, entry, B=0) == INVALID
+    assert fwd(lib, entry, L=0) == INVALID
+    assert fwd(lib, entry, hs=6, hn=4) == INVALID
+    assert fwd(lib, entry, causal=2) == INVALID
+    assert fwd(lib, entry, eps=-1.0) == INVALID
+    assert fwd(lib, entry, eps=float("nan")) == INVALID
+    assert fwd(lib, entry, lam_init=float("inf")) == INVALID
+    assert fwd(lib, entry, ptrs=[A, A, A + 8, A, A, A, A]) == MISALIGNED
+    assert fwd(lib, entry, ptrs=[A, A, A, A, A, A + 4, A]) == MISALIGNED
+
+
+def test_prefill_rejects_unsupported_dims(lib):
+    assert fwd(lib, d=96) == UNSUPPORTED
+    assert fwd(lib, dv=64) == UNSUPPORTED
+    assert fwd(lib, "gda_attn_fwd_f32", dv=48) == UNSUPPORTED
+    assert fwd(lib, "gda_attn_fwd_f32", d=512) == UNSUPPORTED
+
+
+def test_ex_rejects_unknown_flags(lib):
+    P = [ctypes.c_void_p(A)] * 5
+    rc = lib.gda_attn_fwd_ex(*P, ctypes.c_void_p(A), ctypes.c_float(0.8), ctypes.c_void_p(A),
+                             1, 128, 6, 2, 64, 128, 1, ctypes.c_float(1e-5), 0x80, None)
+    assert rc == INVALID
+
+
+def decode(lib, ws_bytes=None, ws=A, B=4, Lcap=256, hs=6, hn=2, d=64, dv=128, ptrs=None):
+    need = lib.gda_attn_decode_workspace_size(B, Lcap, hs, hn, dv)
+    p = ptrs or [A] * 8
+    q1, q2, k1, k2, v, lens, lam, out = (ctypes.c_void_p(x) if x is not None else None for x in p)
+    return lib.gda_attn_decode(q1, q2, k1, k2, v, lens, lam, ctypes.c_float(0.8), out, B, Lcap, hs,
+                               hn, d, dv, ctypes.c_float(1e-5),
+                               ctypes.c_void_p(ws) if ws is not None else None,
+                               need if ws_bytes is None else ws_bytes, None)
+
+
+def test_decode_workspace_size(lib):
+    n = lib.gda_attn_decode_workspace_size(64, 8192, 12, 4, 128)
+    # per split: 12 heads x 2 accumulators x 128 floats, plus (m, l) for 16 heads
+    assert n >= 64 * (12 * 2 * 128 + 16 * 2) * 4
+    assert n % 16 == 0
+    assert lib.gda_attn_decode_workspace_size(0, 8192, 12, 4, 128) == 0
+    assert lib.gda_attn_decode_workspace_size(64, 8192, 12, 5, 128) == 0
+
+
+def test_decode_rejects_bad_arguments(lib):
+    assert decode(lib, ptrs=[A] * 5 + [None, A, A]) == INVALID
+    assert decode(lib, hs=6, hn=4) == INVALID
+    assert decode(lib, d=96) == UNSUPPORTED
+    assert decode(lib, dv=96) == UNSUPPORTED
+    assert decode(lib, ptrs=[A, A, A, A, A + 2, A, A, A]) == MISALIGNED
+    assert decode(lib, ws=None) == WORKSPACE
+    assert decode(lib, ws_bytes=16) == WORKSPACE
+    assert decode(lib, ws=A + 8) == WORKSPACE
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_call_without_a_gpu_reports_cuda_error(lib):
+    assert fwd(lib) == CUDA
+    assert decode(lib) == CUDA
+
+
+def test_binding_checks_tensors_before_the_library():
+    import grouped_differential_attention_gb300 as gda
+    x = torch.zeros(1, 4, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        gda.gda_attn_fwd(x, x, x, x, torch.zeros(1, 4, 2, 128, dtype=torch.bfloat16),
+                         torch.zeros(2), 0.8)

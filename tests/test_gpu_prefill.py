@@ -1,0 +1,165 @@
+"""GPU parity of the prefill paths against the float64 oracle (same seeded inputs).
+
+bf16 path (tcgen05/TMA kernel): |err| <= 3e-3 + 2e-2|ref| elementwise.
+f32 path (CUDA-core kernel): |err| <= 1e-4 (|ref| + rms_row(ref)).
+Small cases are compared on every element (several 128-row tiles, ragged
+tails, L = 1, non-causal, d = 128 with dv split over a CTA pair); the
+full-size workloads are compared on sampled rows plus properties that hold at
+any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import grouped_differential_attention_gb300 as gda
+from grouped_differential_attention_gb300 import workloads as W
+from parity import assert_bf16_close, assert_f32_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device_error_word_stays_clear():
+    from grouped_differential_attention_gb300 import build
+    build.build()
+    gda.gda_device_error(clear=True)
+    yield
+    assert gda.gda_device_error(clear=True) == 0
+
+
+def to_cuda(ts):
+    return [t.cuda() for t in ts]
+
+
+def run_bf16(inputs, lam_init, causal=True, eps=1e-5, flags=0):
+    out = gda.gda_attn_fwd(*to_cuda(inputs), lam_init, causal=causal, eps=eps, flags=flags)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def run_f32(inputs, lam_init, causal=True, eps=1e-5, flags=0):
+    out = gda.gda_attn_fwd_f32(*to_cuda(inputs), lam_init, causal=causal, eps=eps, flags=flags)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+SMALL_BF16 = [  # B, L, h_s, h_n, d, dv, causal
+    (1, 1, 2, 2, 64, 128, True),
+    (1, 128, 3, 1, 64, 128, True),
+    (2, 300, 6, 2, 64, 128, True),
+    (1, 129, 4, 4, 64, 128, False),
+    (2, 257, 12, 4, 64, 128, True),
+    (1, 520, 3, 1, 64, 128, True),
+    (1, 200, 4, 1, 128, 256, True),
+    (1, 131, 8, 2, 128, 128, False),
+    (2, 64, 2, 1, 128, 256, False),
+    (1, 390, 4, 2, 128, 128, True),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL_BF16, ids=lambda s: "B%dL%dhs%dhn%dd%ddv%d%s" % (
+    s[0], s[1], s[2], s[3], s[4], s[5], "c" if s[6] else "f"))
+def test_prefill_bf16_matches_oracle(oracle_mod, shape):
+    B, L, hs, hn, d, dv, causal = shape
+    inp = W.make_prefill_inputs(W.GDA3_PREFILL_L2048, B=B, L=L, h_s=hs, h_n=hn, d=d, dv=dv,
+                                seed=1000 + L + hs)
+    got = run_bf16(inp, 0.8, causal)
+    ref = oracle_mod.prefill(*inp, 0.8, causal=causal)
+    assert_bf16_close(got, ref, str(shape))
+
+
+def _sample_rows(L, n, seed):
+    g = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, 129, L // 2, L - 2, L - 1]
+    rest = g.choice(L, size=max(0, n - len(fixed)), replace=False)
+    return sorted(set(int(r) for r in fixed + list(rest) if 0 <= r < L))
+
+
+@pytest.mark.parametrize("w,nrows", [(W.GDA3_PREFILL_L2048, 64), (W.GDA4_PREFILL_L8192, 20),
+                                     (W.GDA3_PREFILL_L32768, 12)], ids=lambda x: getattr(x, "name", str(x)))
+def test_prefill_full_size_sampled_rows(oracle_mod, w, nrows):
+    inp = W.make_prefill_inputs(w)
+    got = run_bf16(inp, w.lambda_init, w.causal, w.eps)
+    assert torch.isfinite(got.float()).all()
+    rows = _sample_rows(w.L, nrows, seed=7)
+    ref = oracle_mod.prefill_rows(*inp, w.lambda_init, rows, causal=w.causal, eps=w.eps)
+    assert_bf16_close(got[:, rows], ref, w.name)
+
+
+def test_prefill_bf16_unit_values_closed_form():
+    """V = 1 at the full 3:1 size: every output element is (1-li)(1-lam)/sqrt((1-lam)^2+eps)."""
+    w = W.GDA3_PREFILL_L2048
+    q1, k1, q2, k2, v, lam = W.make_prefill_inputs(w)
+    v = torch.ones_like(v)
+    got = run_bf16((q1, k1, q2, k2, v, lam), w.lambda_init, True, w.eps).double()
+    lam64 = lam.double()
+    closed = (1 - w.lambda_init) * (1 - lam64) / torch.sqrt((1 - lam64) ** 2 + w.eps)
+    assert_bf16_close(got, closed[None, None, :, None].expand_as(got).numpy(), "V=1 closed form")
+
+
+@pytest.mark.parametrize("d,dv", [(64, 128), (128, 256)])
+def test_prefill_bf16_equal_maps_cancel_exactly(d, dv):
+    """Q2 = Q1, K2 = K1, h_s = h_n, lambda = 1: the pre-norm output is exactly 0."""
+    q1, k1, _, _, v, lam = W.make_prefill_inputs(W.GDA3_PREFILL_L2048, B=2, L=333, h_s=4, h_n=4,
+                                                 d=d, dv=dv, seed=5)
+    got = run_bf16((q1, k1, q1, k1, v, torch.ones_like(lam)), 0.8, flags=gda.GDA_FLAG_NO_NORM)
+    assert torch.count_nonzero(got) == 0
+
+
+def test_prefill_bf16_no_norm_matches_oracle(oracle_mod):
+    inp = W.make_prefill_inputs(W.GDA3_PREFILL_L2048, B=1, L=260, h_s=6, h_n=2, seed=9)
+    got = run_bf16(inp, 0.8, flags=gda.GDA_FLAG_NO_NORM)
+    ref = oracle_mod.prefill(*inp, 0.8, norm=False)
+    assert_bf16_close(got, ref, "pre-norm")
+
+
+def test_prefill_bf16_first_row_closed_form():
+    q1, k1, q2, k2, v, lam = W.make_prefill_inputs(W.GDA3_PREFILL_L2048, B=2, L=150, h_s=6, h_n=3,
+                                                   seed=13)
+    got = run_bf16((q1, k1, q2, k2, v, lam), 0.6)[:, 0].double()
+    o0 = (1 - lam.double())[None, :, None] * v[:, 0].double()
+    want = 0.4 * o0 / torch.sqrt((o0 ** 2).mean(-1, keepdim=True) + 1e-5)
+    assert_bf16_close(got, want.numpy(), "row 0")
+
+
+def test_prefill_bf16_writes_nothing_outside_its_output():
+    inp = W.make_prefill_inputs(W.GDA3_PREFILL_L2048, B=1, L=130, h_s=3, h_n=1, seed=17)
+    q1, k1, q2, k2, v, lam = to_cuda(inp)
+    n = v.numel()
+    guard = torch.full((n + 2 * 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = guard[4096:4096 + n].view_as(v)
+    gda.gda_attn_fwd(q1, k1, q2, k2, v, lam, 0.8, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(guard[:4096] == 7.0) and torch.all(guard[4096 + n:] == 7.0)
+
+
+def test_prefill_f32_diff_attention_workload(oracle_mod):
+    w = W.DIFF_F32_L128
+    inp = W.make_prefill_inputs(w)
+    got = run_f32(inp, w.lambda_init, w.causal, w.eps)
+    ref = oracle_mod.prefill(*inp, w.lambda_init, causal=w.causal, eps=w.eps)
+    assert_f32_close(got, ref, w.name)
+
+
+SMALL_F32 = [  # B, L, h_s, h_n, d, dv, causal
+    (1, 1, 2, 2, 64, 128, True),
+    (2, 37, 6, 2, 64, 128, True),
+    (1, 129, 6, 3, 64, 128, False),
+    (1, 70, 4, 1, 128, 256, True),
+    (2, 45, 3, 3, 24, 96, True),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL_F32)
+def test_prefill_f32_matches_oracle(oracle_mod, shape):
+    B, L, hs, hn, d, dv, causal = shape
+    inp = W.make_prefill_inputs(W.DIFF_F32_L128, B=B, L=L, h_s=hs, h_n=hn, d=d, dv=dv, seed=L)
+    got = run_f32(inp, 0.7, causal)
+    ref = oracle_mod.prefill(*inp, 0.7, causal=causal)
+    assert_f32_close(got, ref, str(shape))
+
+
+def test_prefill_f32_equal_maps_cancel():
+    q1, k1, _, _, v, lam = W.make_prefill_inputs(W.DIFF_F32_L128, B=1, L=77, h_s=2, h_n=2, seed=3)
+    got = run_f32((q1, k1, q1, k1, v, torch.ones_like(lam)), 0.8, flags=gda.GDA_FLAG_NO_NORM)
+    assert torch.count_nonzero(got) == 0
