@@ -73,7 +73,10 @@ __device__ __forceinline__ int clamp_len(int len, int Lcap, unsigned *err) {
 template <int D, int kTile, int kMaxThreads, int kMinBlocks>
 __global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
 gda_decode_split_kernel(const DecParams p) {
-    __shared__ float sc[kMaxHeads][kTile];   // scores, then weights
+    // scores, then weights; double-buffered by tile parity because the K
+    // threads write tile t+1's scores before the barrier that the V threads
+    // of tile t pass after reading tile t's weights
+    __shared__ float sc_buf[2][kMaxHeads][kTile];
     __shared__ float alpha_s[kMaxHeads];
 
     const int split = blockIdx.x, b = blockIdx.y;
@@ -141,7 +144,8 @@ gda_decode_split_kernel(const DecParams p) {
         }
     };
 
-    auto process_tile = [&](const uint4 (&buf)[kTile], int pos0) {
+    auto process_tile = [&](const uint4 (&buf)[kTile], int pos0, int par) {
+        float (*sc)[kTile] = sc_buf[par];
         // Every lane of the warp takes part in the shuffles (a warp may hold
         // both K and V chunks); head groups of CPH lanes are CPH-aligned and
         // the K/V boundary is a multiple of CPH, so sums never mix roles.
@@ -200,8 +204,8 @@ gda_decode_split_kernel(const DecParams p) {
                 }
             }
         }
-        // the next tile's score writes happen after this tile's readers pass
-        // the next __syncthreads, so no barrier is needed here
+        // alpha_s is rewritten only after the next tile's first barrier, which
+        // every V thread reaches after its reads above
     };
 
     const int ntiles = (pos_end - pos_begin + kTile - 1) / kTile;
@@ -210,10 +214,10 @@ gda_decode_split_kernel(const DecParams p) {
     for (int tile = 0; tile < ntiles; tile += 2) {
         const int pa = pos_begin + tile * kTile;
         if (tile + 1 < ntiles) load_tile(bufB, pa + kTile);
-        process_tile(bufA, pa);
+        process_tile(bufA, pa, 0);
         if (tile + 1 >= ntiles) break;
         if (tile + 2 < ntiles) load_tile(bufA, pa + 2 * kTile);
-        process_tile(bufB, pa + kTile);
+        process_tile(bufB, pa + kTile, 1);
     }
 
     // ---- partial state of this split

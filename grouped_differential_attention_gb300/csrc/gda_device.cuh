@@ -60,14 +60,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// try_wait with a suspend-time hint: the waiting warp is parked (not
+// spinning on issue slots) until the phase completes or ~0.5 ms pass.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(500000u)
         : "memory");
     return ok != 0;
 }
@@ -82,7 +84,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((it & 63u) == 0u) {
+        if ((it & 3u) == 0u) {
             if (*abort) return false;
             if (global_timer_ns() - t0 > kWaitTimeoutNs) {
                 atomicOr(err, code);

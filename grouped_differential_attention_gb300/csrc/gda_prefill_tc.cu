@@ -314,20 +314,25 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
             tc_fence_after();
             const int k0 = j * BN;
             const bool need_mask = (p.causal && k0 + BN - 1 > q0) || (k0 + BN > p.L);
-            // pass 1: row maximum of the raw logits
-            float mx = -INFINITY;
+            // the whole S row of this thread, one TMEM round trip
+            uint32_t r[BN];
 #pragma unroll
-            for (int cch = 0; cch < BN / 32; ++cch) {
-                uint32_t r[32];
-                tmem_ld32(tS + cch * 32, r);
-                tmem_ld_wait();
+            for (int cch = 0; cch < BN / 32; ++cch)
+                tmem_ld32(tS + cch * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[cch * 32]));
+            tmem_ld_wait();
+            if (need_mask) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float s = __uint_as_float(r[e]);
-                    if (need_mask && k0 + cch * 32 + e > last_key) s = -INFINITY;
-                    mx = fmaxf(mx, s);
-                }
+                for (int e = 0; e < BN; ++e)
+                    if (k0 + e > last_key) r[e] = __float_as_uint(-INFINITY);
             }
+            // row maximum: 8 independent chains, then a tree
+            float mx8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(r[i]);
+#pragma unroll
+            for (int e = 8; e < BN; ++e) mx8[e % 8] = fmaxf(mx8[e % 8], __uint_as_float(r[e]));
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float mx_s = mx * sl2;
             float alpha = 1.f;
             bool rescale = false;
@@ -338,28 +343,25 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                 m_ref = mx_s;
                 rescale = true;
             }
-            l *= alpha;
-            // pass 2: P = 2^(s*scale - m_ref) as bf16 over the consumed S columns
+            // P = 2^(s*scale - m_ref) (hidden keys hold -inf and give 0), bf16
+            // pairs written over the consumed S columns; 8 partial row sums
+            float ps[8];
 #pragma unroll
-            for (int cch = 0; cch < BN / 32; ++cch) {
-                uint32_t r[32];
-                tmem_ld32(tS + cch * 32, r);
-                tmem_ld_wait();
-                uint32_t pk[16];
+            for (int i = 0; i < 8; ++i) ps[i] = 0.f;
+            const float neg_m = -m_ref;
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int kj = k0 + cch * 32 + e;
-                    float p0 = fast_exp2(fmaf(__uint_as_float(r[e]), sl2, -m_ref));
-                    float p1 = fast_exp2(fmaf(__uint_as_float(r[e + 1]), sl2, -m_ref));
-                    if (need_mask) {
-                        if (kj > last_key) p0 = 0.f;
-                        if (kj + 1 > last_key) p1 = 0.f;
-                    }
-                    l += p0 + p1;
+            for (int cch = 0; cch < BN / 64; ++cch) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(r[cch * 64 + e]), sl2, neg_m));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(r[cch * 64 + e + 1]), sl2, neg_m));
+                    ps[(e / 2) % 8] += p0 + p1;
                     pk[e / 2] = pack_bf16x2(p0, p1);
                 }
-                tmem_st16(tS + cch * 16, pk);
+                tmem_st32(tS + cch * 32, pk);
             }
+            l = l * alpha + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
             tmem_st_wait();
             if (__any_sync(0xffffffffu, rescale)) {
                 // the accumulator may only be touched once PV(j-1) has completed
@@ -404,7 +406,7 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                 tmem_ld_wait();
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float o = __uint_as_float(r1[e]) * inv1 - __uint_as_float(r2[e]) * c2;
+                    const float o = __fmul_rn(__uint_as_float(r1[e]), inv1) - __fmul_rn(__uint_as_float(r2[e]), c2);
                     ss = fmaf(o, o, ss);
                 }
             }
@@ -431,8 +433,12 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const float y0 = (__uint_as_float(r1[e]) * inv1 - __uint_as_float(r2[e]) * c2) * yscale;
-                    const float y1 = (__uint_as_float(r1[e + 1]) * inv1 - __uint_as_float(r2[e + 1]) * c2) * yscale;
+                    // both products rounded before the subtraction (no FMA
+                    // contraction), so equal maps with lambda = 1 cancel exactly
+                    const float y0 = (__fmul_rn(__uint_as_float(r1[e]), inv1) -
+                                      __fmul_rn(__uint_as_float(r2[e]), c2)) * yscale;
+                    const float y1 = (__fmul_rn(__uint_as_float(r1[e + 1]), inv1) -
+                                      __fmul_rn(__uint_as_float(r2[e + 1]), c2)) * yscale;
                     pk[e / 2] = pack_bf16x2(y0, y1);
                 }
                 if (qrow < p.L) {

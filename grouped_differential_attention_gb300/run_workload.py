@@ -1,0 +1,60 @@
+"""Run one named workload a few times through the public API (for profilers).
+
+    python -m grouped_differential_attention_gb300.run_workload prefill \
+        gda_3to1_prefill_bf16_B4_L2048_h12+4_d64_dv128 --launches 3
+    python -m grouped_differential_attention_gb300.run_workload decode --launches 3
+
+Inputs are the seeded synthetic tensors of ``workloads``; prints the mean
+device time per launch measured with CUDA events (not meaningful under a
+profiler).
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+import torch
+
+import grouped_differential_attention_gb300 as gda
+from grouped_differential_attention_gb300 import workloads as W
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("kind", choices=["prefill", "decode"])
+    ap.add_argument("workload", nargs="?", default=None)
+    ap.add_argument("--launches", type=int, default=3)
+    args = ap.parse_args(argv)
+    dev = torch.device("cuda:0")
+    if args.kind == "prefill":
+        w = W.PREFILL_WORKLOADS[args.workload or W.GDA3_PREFILL_L2048.name]
+        inp = [t.to(dev) for t in W.make_prefill_inputs(w)]
+        fn = gda.gda_attn_fwd if w.dtype == "bf16" else gda.gda_attn_fwd_f32
+        out = torch.empty((w.B, w.L, w.h_s, w.dv), dtype=inp[0].dtype, device=dev)
+
+        def launch():
+            fn(*inp, w.lambda_init, causal=w.causal, eps=w.eps, out=out)
+    else:
+        w = W.GDA3_DECODE_B64
+        inp = [t.to(dev) for t in W.make_decode_inputs(w)]
+        out = torch.empty((w.B, w.h_s, w.dv), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(gda.gda_attn_decode_workspace_size(w.B, w.Lcap, w.h_s, w.h_n, w.dv),
+                         dtype=torch.uint8, device=dev)
+
+        def launch():
+            gda.gda_attn_decode(*inp, w.lambda_init, eps=w.eps, out=out, workspace=ws)
+
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.launches):
+        launch()
+    e1.record()
+    torch.cuda.synchronize()
+    err = gda.gda_device_error(clear=True)
+    print(f"{w.name}: {e0.elapsed_time(e1) / args.launches:.4f} ms per launch, device error word {err}")
+    return 0 if err == 0 else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())
