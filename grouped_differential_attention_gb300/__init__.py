@@ -50,7 +50,10 @@ _lib = None
 
 class GDAError(RuntimeError):
     def __init__(self, status: int, what: str):
-        super().__init__(f"{what}: {gda_status_string(status)} (status {status})")
+        extra = ""
+        if status == GDA_ERR_CUDA:
+            extra = f", cudaError {_load().gda_last_cuda_error()}"
+        super().__init__(f"{what}: {gda_status_string(status)} (status {status}{extra})")
         self.status = status
 
 
@@ -80,6 +83,8 @@ def _load():
             lib.gda_status_string.argtypes = [I]
             lib.gda_status_string.restype = ctypes.c_char_p
             lib.gda_device_error.argtypes = [I]
+            lib.gda_last_cuda_error.argtypes = []
+            lib.gda_last_cuda_error.restype = I
             for name in ("gda_attn_fwd", "gda_attn_fwd_ex", "gda_attn_fwd_f32",
                          "gda_attn_fwd_f32_ex", "gda_attn_decode", "gda_device_error"):
                 getattr(lib, name).restype = I

@@ -81,10 +81,18 @@ int check_prefill_common(const void *q1, const void *k1, const void *q2, const v
     return GDA_OK;
 }
 
+thread_local int g_last_cuda_error = 0;
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
 }  // namespace
+
+int record_cuda_error(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    cudaGetLastError();   // do not leak a launch error into the caller's next check
+    return GDA_ERR_CUDA;
+}
 
 bool encode_tmap_4d_bf16(CUtensorMap *map, const void *base, const uint64_t dims[4],
                          const uint64_t strides_bytes[3], const uint32_t box[4]) {
@@ -211,6 +219,8 @@ const char *gda_status_string(int status) {
         default: return "unknown status";
     }
 }
+
+int gda_last_cuda_error(void) { return g_last_cuda_error; }
 
 int gda_device_error(int clear) {
     unsigned *err = nullptr;

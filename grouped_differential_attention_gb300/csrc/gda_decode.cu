@@ -341,9 +341,11 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
         gda_decode_split_kernel<128, 2, 1024, 1><<<grid, threads, 0, stream>>>(p);
     else
         return GDA_ERR_UNSUPPORTED;
-    if (cudaGetLastError() != cudaSuccess) return GDA_ERR_CUDA;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return record_cuda_error(e);
     gda_decode_combine_kernel<<<dim3(a.hs, a.B), a.dv, 0, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? GDA_OK : GDA_ERR_CUDA;
+    e = cudaGetLastError();
+    return e == cudaSuccess ? GDA_OK : record_cuda_error(e);
 }
 
 }  // namespace gda

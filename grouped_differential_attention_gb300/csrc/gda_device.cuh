@@ -260,6 +260,50 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// max(a, b, c) in one instruction (three-input max.f32).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (a0, a1) = (a0 * b0 + c0, a1 * b1 + c1) as one packed fma.rn.f32x2.
+__device__ __forceinline__ void ffma2(float &a0, float &a1, float b0, float b1, float c0, float c1) {
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mov.b64 y, {%2, %3};\n\t"
+        "mov.b64 z, {%4, %5};\n\t"
+        "fma.rn.f32x2 x, x, y, z;\n\t"
+        "mov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// (a0, a1) += (b0, b1) as one packed add.f32x2.
+__device__ __forceinline__ void fadd2(float &a0, float &a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 x, y;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mov.b64 y, {%2, %3};\n\t"
+        "add.f32x2 x, x, y;\n\t"
+        "mov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+
+// Pack the upper halves of two 32-bit words into one word, `lo` in the low
+// half (a byte permute on the integer pipe).
+__device__ __forceinline__ uint32_t pack_hi16(uint32_t lo, uint32_t hi) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+
+// Bits of a non-negative float rounded to bf16 precision (half-way cases
+// away from zero) in the upper 16 bits; one integer add, no conversion unit.
+__device__ __forceinline__ uint32_t round_bf16_bits(float x) {
+    return __float_as_uint(x) + 0x8000u;
+}
+
 // Pack two floats into bf16x2 (round to nearest even); `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -34,6 +34,10 @@ struct DecodeArgs {
     unsigned *dev_err;
 };
 
+// Remembers `e` as this thread's last CUDA error (see gda_last_cuda_error),
+// clears the runtime's sticky-free error state and returns GDA_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 // Each launcher validates nothing (the ABI layer did) and returns a
 // gda_status value.
 int launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);

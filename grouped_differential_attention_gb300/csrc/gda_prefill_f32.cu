@@ -171,14 +171,16 @@ template <int NV>
 int launch_nv(const F32Params &p, cudaStream_t stream) {
     const size_t smem = sizeof(float) * (2 * kRows * p.d + 2 * kKeys * (p.d + 1) + kKeys * p.dv);
     auto kern = gda_prefill_f32_kernel<NV>;
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-            cudaSuccess)
-        return GDA_ERR_CUDA;
+    if (smem > 48 * 1024) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return record_cuda_error(e);
+    }
     dim3 grid((p.L + kRows - 1) / kRows, p.hs, p.B);
     if (grid.y > 65535 || grid.z > 65535) return GDA_ERR_UNSUPPORTED;
     kern<<<grid, kThreadsF32, smem, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? GDA_OK : GDA_ERR_CUDA;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GDA_OK : record_cuda_error(e);
 }
 
 }  // namespace

@@ -14,17 +14,21 @@
 //
 // CTA = (query tile of 128 rows, batch b, signal head h, dv slice of 128).
 // 10 warps:
-//   warp 0      TMA producer (one elected lane): Q1/Q2 once, then a ring of
-//               stages each holding a K1, K2 and V tile;
-//   warp 1      TMEM allocator and MMA issuer (one elected lane);
-//   warps 2-5   softmax of the signal map  (thread = query row = TMEM lane);
-//   warps 6-9   softmax of the noise map.
-// TMEM (512 columns): O1 [0,128) | O2 [128,256) | S1 [256,256+BN) |
-// S2 [256+BN,256+2BN).  P (bf16) overwrites the first BN/2 columns of its S
-// tile and feeds the PV MMA straight from TMEM.  The two maps ping-pong:
-// while one softmax group works, the tensor core runs the other map's PV and
-// next QK.  A row's running max is only moved when it grows by more than
-// 2^8 (in exp2 units), and only then is its accumulator rescaled.
+//   warp 0       TMA producer (one elected lane): Q1/Q2 once, then a ring of
+//                K stages (K1 and K2 tiles) and a ring of V stages;
+//   warp 1       TMEM allocator and MMA issuer (one elected lane);
+//   warps 2-5    softmax of the signal map, warps 6-9 of the noise map
+//                (thread = query row = TMEM lane).  The TMEM load of the next
+//                S tile is issued before the current tile's exponentials, so
+//                its latency hides under them.
+// KV tiles are 64 keys.  TMEM (512 columns): O1 [0,128) | O2 [128,256) |
+// S1 tiles [256,320) [320,384) | S2 tiles [384,448) [448,512): each map's S
+// is double-buffered, so QK(j+2) runs on the tensor core while the softmax
+// of tile j+1 runs, and the softmax warps never wait on their own map's PV.
+// P overwrites the first 32 columns of its S tile and feeds the PV MMA
+// straight from TMEM.  P is rounded to bf16 with an integer add and a byte
+// permute, leaving the special-function unit to the exponentials.  A row's running max only moves when it grows by
+// more than 2^8 (exp2 units); only then is its accumulator rescaled.
 // dv = 256 is split over a 2-CTA cluster; the two CTAs exchange the per-row
 // sum of squares through distributed shared memory for the RMSNorm.
 #include <cuda.h>
@@ -42,42 +46,47 @@ namespace {
 
 constexpr int kBM = 128;          // query rows per CTA (= TMEM lanes)
 constexpr int kDVS = 128;         // dv columns per CTA
-constexpr int kThreads = 320;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = 32 * (2 + kSoftmaxWarps);
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <int D> struct TcCfg;
-template <> struct TcCfg<64> { static constexpr int BN = 128, STAGES = 2; };
-template <> struct TcCfg<128> { static constexpr int BN = 64, STAGES = 3; };
+template <> struct TcCfg<64> { static constexpr int BN = 64, KS = 4, VS = 4; };
+template <> struct TcCfg<128> { static constexpr int BN = 64, KS = 3, VS = 3; };
 
 struct Ctrl {
     uint64_t q_full;
-    uint64_t kv_full[4];
-    uint64_t kv_empty[4];
-    uint64_t s_full[2];
-    uint64_t p_full[2];
-    uint64_t o_done[2];
+    uint64_t k_full[4], k_empty[4];
+    uint64_t v_full[4], v_empty[4];
+    uint64_t s_full[2][2];      // [map][S buffer]
+    uint64_t p_full[2][2];      // [map][S buffer]
+    uint64_t o_done[2];         // [map]: one phase per PV
+    uint64_t o_final;           // every MMA of the CTA has completed
     uint64_t mma_idle;
     uint32_t tmem_base;
     int abort_flag;
-    float l_row[2][kBM];
-    float ss_part[2][kBM];
+    float l_row[2][kBM];        // [map][row]
+    float ss_part[2][kBM];      // [warpgroup][row]
     float ss_peer[kBM];
 };
 
 template <int D> struct Layout {
     static constexpr int BN = TcCfg<D>::BN;
-    static constexpr int S = TcCfg<D>::STAGES;
+    static constexpr int KS = TcCfg<D>::KS;
+    static constexpr int VS = TcCfg<D>::VS;
     static constexpr int Q_BYTES = kBM * D * 2;
-    static constexpr int K_BYTES = BN * D * 2;
-    static constexpr int V_BYTES = BN * kDVS * 2;
-    static constexpr int STAGE_BYTES = 2 * K_BYTES + V_BYTES;
+    static constexpr int K_BYTES = BN * D * 2;          // one of K1 / K2
+    static constexpr int KST_BYTES = 2 * K_BYTES;       // K stage: K1 then K2
+    static constexpr int V_BYTES = BN * kDVS * 2;       // V stage
     static constexpr int OFF_Q1 = 0;
     static constexpr int OFF_Q2 = Q_BYTES;
-    static constexpr int OFF_ST = 2 * Q_BYTES;
-    static constexpr int TILES = OFF_ST + S * STAGE_BYTES;
+    static constexpr int OFF_K = 2 * Q_BYTES;
+    static constexpr int OFF_V = OFF_K + KS * KST_BYTES;
+    static constexpr int TILES = OFF_V + VS * V_BYTES;
     static constexpr int TOTAL = TILES + (int)((sizeof(Ctrl) + 1023) / 1024) * 1024 + 1024;
     static_assert(TOTAL <= 232448, "shared memory budget");
-    static_assert(256 + 2 * BN <= 512, "TMEM budget");
+    static_assert(256 + 4 * BN <= 512, "TMEM budget");
+    static_assert(KS <= 4 && VS <= 4, "barrier arrays");
 };
 
 struct TcParams {
@@ -110,11 +119,16 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, unsig
     mbar_wait(bar, parity, err, GDA_DEVERR_PREFILL_TIMEOUT, &dummy);
 }
 
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, unsigned *err,
+                                         volatile int *abort) {
+    return mbar_wait(bar, parity, err, GDA_DEVERR_PREFILL_TIMEOUT, abort);
+}
+
 // Whole-warp wait: every lane polls, the result is agreed by vote so the
 // warp stays converged for the .sync.aligned tcgen05 instructions after it.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsigned *err,
                                           volatile int *abort) {
-    bool ok = mbar_wait(bar, parity, err, GDA_DEVERR_PREFILL_TIMEOUT, abort);
+    bool ok = wait_bar(bar, parity, err, abort);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -124,6 +138,7 @@ __device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t qa, uint32_t ka) 
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, LY::BN, 0);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
+        // K-major, 128-byte swizzle: 64-element column blocks, 8-row groups 1 KiB apart
         const uint32_t blk = k / 4, sub = (k % 4) * 32;
         const uint64_t a = smem_desc_sw128(qa + blk * (kBM * 128) + sub, 16, 1024);
         const uint64_t b = smem_desc_sw128(ka + blk * (LY::BN * 128) + sub, 16, 1024);
@@ -153,7 +168,8 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                       const __grid_constant__ CUtensorMap tmV, const TcParams p) {
     using LY = Layout<D>;
     constexpr int BN = LY::BN;
-    constexpr int S = LY::S;
+    constexpr int KS = LY::KS;
+    constexpr int VS = LY::VS;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -178,15 +194,22 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl->q_full, 1);
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&ctl->kv_full[s], 1);
-            mbar_init(&ctl->kv_empty[s], 1);
+        for (int s = 0; s < KS; ++s) {
+            mbar_init(&ctl->k_full[s], 1);
+            mbar_init(&ctl->k_empty[s], 1);
+        }
+        for (int s = 0; s < VS; ++s) {
+            mbar_init(&ctl->v_full[s], 1);
+            mbar_init(&ctl->v_empty[s], 1);
         }
         for (int m = 0; m < 2; ++m) {
-            mbar_init(&ctl->s_full[m], 1);
-            mbar_init(&ctl->p_full[m], 128);
+            for (int bb = 0; bb < 2; ++bb) {
+                mbar_init(&ctl->s_full[m][bb], 1);
+                mbar_init(&ctl->p_full[m][bb], 128);
+            }
             mbar_init(&ctl->o_done[m], 1);
         }
+        mbar_init(&ctl->o_final, 1);
         mbar_init(&ctl->mma_idle, 1);
         ctl->abort_flag = 0;
         fence_mbar_init();
@@ -216,29 +239,51 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                 tma_load_4d(smem + LY::OFF_Q1 + blk * kBM * 128, &tmQ1, &ctl->q_full, blk * 64, h, q0, b);
                 tma_load_4d(smem + LY::OFF_Q2 + blk * kBM * 128, &tmQ2, &ctl->q_full, blk * 64, g, q0, b);
             }
-            int issued = 0;
-            for (int j = 0; j < nkv; ++j) {
-                const int st = j % S;
-                if (j >= S && !mbar_wait(&ctl->kv_empty[st], ((j / S) - 1) & 1, p.err,
-                                         GDA_DEVERR_PREFILL_TIMEOUT, abort_flag))
-                    break;
-                uint8_t *sb = smem + LY::OFF_ST + st * LY::STAGE_BYTES;
-                mbar_arrive_expect_tx(&ctl->kv_full[st], LY::STAGE_BYTES);
+            auto load_k = [&](int j) {
+                const int st = j % KS;
+                uint8_t *sb = smem + LY::OFF_K + st * LY::KST_BYTES;
+                mbar_arrive_expect_tx(&ctl->k_full[st], LY::KST_BYTES);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk) {
-                    tma_load_4d(sb + blk * BN * 128, &tmK1, &ctl->kv_full[st], blk * 64, h, j * BN, b);
-                    tma_load_4d(sb + LY::K_BYTES + blk * BN * 128, &tmK2, &ctl->kv_full[st], blk * 64, g, j * BN, b);
+                    tma_load_4d(sb + blk * BN * 128, &tmK1, &ctl->k_full[st], blk * 64, h, j * BN, b);
+                    tma_load_4d(sb + LY::K_BYTES + blk * BN * 128, &tmK2, &ctl->k_full[st], blk * 64, g,
+                                j * BN, b);
                 }
+            };
+            auto load_v = [&](int j) {
+                const int st = j % VS;
+                uint8_t *sb = smem + LY::OFF_V + st * LY::V_BYTES;
+                mbar_arrive_expect_tx(&ctl->v_full[st], LY::V_BYTES);
 #pragma unroll
                 for (int blk = 0; blk < kDVS / 64; ++blk)
-                    tma_load_4d(sb + 2 * LY::K_BYTES + blk * BN * 128, &tmV, &ctl->kv_full[st],
-                                slice * kDVS + blk * 64, h, j * BN, b);
-                ++issued;
+                    tma_load_4d(sb + blk * BN * 128, &tmV, &ctl->v_full[st], slice * kDVS + blk * 64, h,
+                                j * BN, b);
+            };
+            // K runs two tiles ahead of V (QK(j+2) is issued right after PV(j))
+            int k_issued = 0, v_issued = 0;
+            for (int t = 0; t < 2 && t < nkv; ++t) {
+                load_k(t);
+                k_issued = t + 1;
+            }
+            for (int j = 0; j < nkv; ++j) {
+                if (j + 2 < nkv) {
+                    const int jk = j + 2;
+                    if (jk >= KS && !wait_bar(&ctl->k_empty[jk % KS], ((jk / KS) - 1) & 1, p.err, abort_flag))
+                        break;
+                    load_k(jk);
+                    k_issued = jk + 1;
+                }
+                if (j >= VS && !wait_bar(&ctl->v_empty[j % VS], ((j / VS) - 1) & 1, p.err, abort_flag))
+                    break;
+                load_v(j);
+                v_issued = j + 1;
             }
             // our own copies must land before the CTA may exit
             drain_wait(&ctl->q_full, 0, p.err);
-            for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
-                drain_wait(&ctl->kv_full[j % S], (j / S) & 1, p.err);
+            for (int j = (k_issued > KS ? k_issued - KS : 0); j < k_issued; ++j)
+                drain_wait(&ctl->k_full[j % KS], (j / KS) & 1, p.err);
+            for (int j = (v_issued > VS ? v_issued - VS : 0); j < v_issued; ++j)
+                drain_wait(&ctl->v_full[j % VS], (j / VS) & 1, p.err);
         }
         __syncwarp();
         if (p.nslices == 2) cluster_sync_all();
@@ -246,47 +291,53 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
         // ================================================= MMA issuer
         if (elect_one()) {
             const uint32_t tO1 = tmem, tO2 = tmem + 128;
-            const uint32_t tS1 = tmem + 256, tS2 = tmem + 256 + BN;
+            const uint32_t tS1 = tmem + 256, tS2 = tmem + 256 + 2 * BN;   // + buffer * BN
             const uint32_t q1a = smem_u32(smem + LY::OFF_Q1);
             const uint32_t q2a = smem_u32(smem + LY::OFF_Q2);
-            const uint32_t st0 = smem_u32(smem + LY::OFF_ST);
-            bool ok = mbar_wait(&ctl->q_full, 0, p.err, GDA_DEVERR_PREFILL_TIMEOUT, abort_flag) &&
-                      mbar_wait(&ctl->kv_full[0], 0, p.err, GDA_DEVERR_PREFILL_TIMEOUT, abort_flag);
-            if (ok) {
+            const uint32_t k0a = smem_u32(smem + LY::OFF_K);
+            const uint32_t v0a = smem_u32(smem + LY::OFF_V);
+            bool ok = wait_bar(&ctl->q_full, 0, p.err, abort_flag);
+            // QK of the first two tiles fill both S buffers of both maps
+            for (int t = 0; ok && t < 2 && t < nkv; ++t) {
+                if (!wait_bar(&ctl->k_full[t % KS], (t / KS) & 1, p.err, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                issue_qk<D>(tS1, q1a, st0);
-                mma_commit(&ctl->s_full[0]);
-                issue_qk<D>(tS2, q2a, st0 + LY::K_BYTES);
-                mma_commit(&ctl->s_full[1]);
+                const uint32_t ka = k0a + (t % KS) * LY::KST_BYTES;
+                issue_qk<D>(tS1 + t * BN, q1a, ka);
+                mma_commit(&ctl->s_full[0][t]);
+                issue_qk<D>(tS2 + t * BN, q2a, ka + LY::K_BYTES);
+                mma_commit(&ctl->s_full[1][t]);
+                mma_commit(&ctl->k_empty[t % KS]);
             }
             for (int j = 0; ok && j < nkv; ++j) {
-                const int st = j % S;
-                const uint32_t sb = st0 + st * LY::STAGE_BYTES;
-                const bool more = j + 1 < nkv;
-                const uint32_t sb1 = st0 + ((j + 1) % S) * LY::STAGE_BYTES;
-                // signal map: PV1(j), then QK1(j+1) into the freed S1 tile
-                if (!mbar_wait(&ctl->p_full[0], j & 1, p.err, GDA_DEVERR_PREFILL_TIMEOUT, abort_flag)) break;
+                const int bb = j & 1;
+                const uint32_t va = v0a + (j % VS) * LY::V_BYTES;
+                const int jn = j + 2;                       // next tile for this S buffer
+                const bool more = jn < nkv;
+                const uint32_t kan = k0a + (jn % KS) * LY::KST_BYTES;
+                // signal map: PV1(j), then QK1(j+2) into the S1 buffer PV1(j) just read
+                if (!wait_bar(&ctl->p_full[0][bb], (j >> 1) & 1, p.err, abort_flag)) break;
+                if (!wait_bar(&ctl->v_full[j % VS], (j / VS) & 1, p.err, abort_flag)) break;
                 tc_fence_after();
-                issue_pv<D>(tO1, tS1, sb + 2 * LY::K_BYTES, j > 0);
+                issue_pv<D>(tO1, tS1 + bb * BN, va, j > 0);
                 mma_commit(&ctl->o_done[0]);
                 if (more) {
-                    if (!mbar_wait(&ctl->kv_full[(j + 1) % S], ((j + 1) / S) & 1, p.err,
-                                   GDA_DEVERR_PREFILL_TIMEOUT, abort_flag))
-                        break;
+                    if (!wait_bar(&ctl->k_full[jn % KS], (jn / KS) & 1, p.err, abort_flag)) break;
                     tc_fence_after();
-                    issue_qk<D>(tS1, q1a, sb1);
-                    mma_commit(&ctl->s_full[0]);
+                    issue_qk<D>(tS1 + bb * BN, q1a, kan);
+                    mma_commit(&ctl->s_full[0][bb]);
                 }
-                // noise map: PV2(j), release the stage, then QK2(j+1)
-                if (!mbar_wait(&ctl->p_full[1], j & 1, p.err, GDA_DEVERR_PREFILL_TIMEOUT, abort_flag)) break;
+                // noise map: PV2(j), release V(j), then QK2(j+2) and release K(j+2)
+                if (!wait_bar(&ctl->p_full[1][bb], (j >> 1) & 1, p.err, abort_flag)) break;
                 tc_fence_after();
-                issue_pv<D>(tO2, tS2, sb + 2 * LY::K_BYTES, j > 0);
+                issue_pv<D>(tO2, tS2 + bb * BN, va, j > 0);
                 mma_commit(&ctl->o_done[1]);
-                mma_commit(&ctl->kv_empty[st]);
+                mma_commit(&ctl->v_empty[j % VS]);
                 if (more) {
-                    issue_qk<D>(tS2, q2a, sb1 + LY::K_BYTES);
-                    mma_commit(&ctl->s_full[1]);
+                    issue_qk<D>(tS2 + bb * BN, q2a, kan + LY::K_BYTES);
+                    mma_commit(&ctl->s_full[1][bb]);
+                    mma_commit(&ctl->k_empty[jn % KS]);
                 }
+                if (j == nkv - 1) mma_commit(&ctl->o_final);
             }
             // every issued MMA completes before TMEM is released
             mma_commit(&ctl->mma_idle);
@@ -300,7 +351,7 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
         const int quarter = warp % 4;             // TMEM lanes this warp may touch
         const int row = quarter * 32 + lane;      // query row in the tile
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem + 256 + m * BN + lane_off;
+        const uint32_t tSm = tmem + 256 + m * 2 * BN + lane_off;   // + buffer * BN
         const uint32_t tOm = tmem + m * 128 + lane_off;
         const int qrow = q0 + row;
         const int last_key = p.causal ? min(qrow, p.L - 1) : p.L - 1;
@@ -309,30 +360,40 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
         float l = 0.f;
         bool ok = true;
 
-        for (int j = 0; j < nkv; ++j) {
-            if (!warp_wait(&ctl->s_full[m], j & 1, p.err, abort_flag)) { ok = false; break; }
+        // r holds the current tile's S row; the next tile's row is requested
+        // into the same registers once the exponentials have consumed them, so
+        // its TMEM latency overlaps the P-store wait and the barrier arrive.
+        uint32_t r[BN];
+        if (warp_wait(&ctl->s_full[m][0], 0, p.err, abort_flag)) {
             tc_fence_after();
-            const int k0 = j * BN;
-            const bool need_mask = (p.causal && k0 + BN - 1 > q0) || (k0 + BN > p.L);
-            // the whole S row of this thread, one TMEM round trip
-            uint32_t r[BN];
 #pragma unroll
             for (int cch = 0; cch < BN / 32; ++cch)
-                tmem_ld32(tS + cch * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[cch * 32]));
+                tmem_ld32(tSm + cch * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[cch * 32]));
             tmem_ld_wait();
+        } else {
+            ok = false;
+        }
+        for (int j = 0; ok && j < nkv; ++j) {
+            const uint32_t tS = tSm + (j & 1) * BN;
+            const int k0 = j * BN;
+            const bool need_mask = (p.causal && k0 + BN - 1 > q0) || (k0 + BN > p.L);
             if (need_mask) {
 #pragma unroll
                 for (int e = 0; e < BN; ++e)
                     if (k0 + e > last_key) r[e] = __float_as_uint(-INFINITY);
             }
-            // row maximum: 8 independent chains, then a tree
-            float mx8[8];
+            // row maximum: three-input max over 4 independent chains
+            float mx4[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(r[i]);
+            for (int i = 0; i < 4; ++i) mx4[i] = __uint_as_float(r[i]);
 #pragma unroll
-            for (int e = 8; e < BN; ++e) mx8[e % 8] = fmaxf(mx8[e % 8], __uint_as_float(r[e]));
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            for (int e = 4; e + 8 <= BN; e += 8)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    mx4[i] = max3f(mx4[i], __uint_as_float(r[e + 2 * i]), __uint_as_float(r[e + 2 * i + 1]));
+            float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+#pragma unroll
+            for (int e = 4 + ((BN - 4) / 8) * 8; e < BN; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
             const float mx_s = mx * sl2;
             float alpha = 1.f;
             bool rescale = false;
@@ -343,59 +404,82 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                 m_ref = mx_s;
                 rescale = true;
             }
-            // P = 2^(s*scale - m_ref) (hidden keys hold -inf and give 0), bf16
-            // pairs written over the consumed S columns; 8 partial row sums
-            float ps[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ps[i] = 0.f;
+            // P = 2^(s*scale - m_ref) (hidden keys hold -inf and give 0)
             const float neg_m = -m_ref;
+            float sa = 0.f, sb = 0.f, sc = 0.f, sd = 0.f;
 #pragma unroll
-            for (int cch = 0; cch < BN / 64; ++cch) {
-                uint32_t pk[32];
+            for (int hh = 0; hh < BN / 32; ++hh) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(r[cch * 64 + e]), sl2, neg_m));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(r[cch * 64 + e + 1]), sl2, neg_m));
-                    ps[(e / 2) % 8] += p0 + p1;
-                    pk[e / 2] = pack_bf16x2(p0, p1);
+                for (int e = 0; e < 32; e += 4) {
+                    float x0 = __uint_as_float(r[hh * 32 + e]), x1 = __uint_as_float(r[hh * 32 + e + 1]);
+                    float x2 = __uint_as_float(r[hh * 32 + e + 2]), x3 = __uint_as_float(r[hh * 32 + e + 3]);
+                    ffma2(x0, x1, sl2, sl2, neg_m, neg_m);
+                    ffma2(x2, x3, sl2, sl2, neg_m, neg_m);
+                    x0 = fast_exp2(x0);
+                    x1 = fast_exp2(x1);
+                    x2 = fast_exp2(x2);
+                    x3 = fast_exp2(x3);
+                    fadd2(sa, sb, x0, x1);
+                    fadd2(sc, sd, x2, x3);
+                    pk[e / 2] = pack_hi16(round_bf16_bits(x0), round_bf16_bits(x1));
+                    pk[e / 2 + 1] = pack_hi16(round_bf16_bits(x2), round_bf16_bits(x3));
                 }
-                tmem_st32(tS + cch * 32, pk);
+                tmem_st16(tS + hh * 16, pk);
             }
-            l = l * alpha + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
+            l = l * alpha + ((sa + sb) + (sc + sd));
+            // request the next S tile into r
+            const bool more = j + 1 < nkv;
+            if (more) {
+                if (!warp_wait(&ctl->s_full[m][(j + 1) & 1], ((j + 1) >> 1) & 1, p.err, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tSn = tSm + ((j + 1) & 1) * BN;
+#pragma unroll
+                for (int cch = 0; cch < BN / 32; ++cch)
+                    tmem_ld32(tSn + cch * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[cch * 32]));
+            }
             tmem_st_wait();
             if (__any_sync(0xffffffffu, rescale)) {
                 // the accumulator may only be touched once PV(j-1) has completed
-                if (!warp_wait(&ctl->o_done[m], (j - 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                if (!warp_wait(&ctl->o_done[m], (j - 1) & 1, p.err, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
 #pragma unroll
                 for (int cch = 0; cch < kDVS / 32; ++cch) {
-                    uint32_t r[32];
-                    tmem_ld32(tOm + cch * 32, r);
+                    uint32_t o[32];
+                    tmem_ld32(tOm + cch * 32, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                    tmem_st32(tOm + cch * 32, r);
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(tOm + cch * 32, o);
                 }
                 tmem_st_wait();
             }
             tc_fence_before();
-            mbar_arrive(&ctl->p_full[m]);
+            mbar_arrive(&ctl->p_full[m][j & 1]);
+            if (more) tmem_ld_wait();
         }
+        // drain any TMEM load still in flight after an early exit
+        tmem_ld_wait();
 
         // ---------------------------------------------------- epilogue
         ctl->l_row[m][row] = l;
-        named_bar_sync(1, 256);
+        named_bar_sync(1, 32 * kSoftmaxWarps);
         const float l1 = ctl->l_row[0][row];
         const float l2 = ctl->l_row[1][row];
         ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
-        if (ok) ok = warp_wait(&ctl->o_done[0], (nkv - 1) & 1, p.err, abort_flag);
-        if (ok) ok = warp_wait(&ctl->o_done[1], (nkv - 1) & 1, p.err, abort_flag);
+        if (ok) ok = warp_wait(&ctl->o_final, 0, p.err, abort_flag);
         tc_fence_after();
         const float lam = p.lambda[h];
         const float inv1 = 1.f / l1;
         const float c2 = lam / l2;
         const uint32_t tO1 = tmem + lane_off, tO2 = tmem + 128 + lane_off;
-        const int col0 = m * 64;                  // this group's half of the slice
+        const int col0 = m * 64;                  // this warpgroup's 64 columns of the slice
         float ss = 0.f;
         if (ok) {
 #pragma unroll
@@ -412,7 +496,7 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
             }
         }
         ctl->ss_part[m][row] = ss;
-        named_bar_sync(1, 256);
+        named_bar_sync(1, 32 * kSoftmaxWarps);
         float ss_tot = ctl->ss_part[0][row] + ctl->ss_part[1][row];
         if (p.nslices == 2) {
             if (m == 0) st_cluster_f32(&ctl->ss_peer[row], cluster_ctarank() ^ 1u, ss_tot);
@@ -506,15 +590,8 @@ int launch_impl(const PrefillArgs &a, cudaStream_t stream) {
     p.no_norm = (a.flags & GDA_FLAG_NO_NORM) ? 1 : 0;
 
     auto kern = gda_prefill_tc_kernel<D>;
-    static bool attr_set = false;   // per process; the attribute is per function
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL) !=
-            cudaSuccess)
-            return GDA_ERR_CUDA;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
-            return GDA_ERR_CUDA;
-        attr_set = true;
-    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL);
+    if (e != cudaSuccess) return record_cuda_error(e);
     const long long grid = static_cast<long long>(p.nqt) * a.B * a.hs * p.nslices;
     if (grid <= 0 || grid > 0x7fffffffLL) return GDA_ERR_UNSUPPORTED;
 
@@ -530,8 +607,8 @@ int launch_impl(const PrefillArgs &a, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mQ1, mK1, mQ2, mK2, mV, p);
-    return e == cudaSuccess ? GDA_OK : GDA_ERR_CUDA;
+    e = cudaLaunchKernelEx(&cfg, kern, mQ1, mK1, mQ2, mK2, mV, p);
+    return e == cudaSuccess ? GDA_OK : record_cuda_error(e);
 }
 
 }  // namespace

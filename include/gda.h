@@ -145,6 +145,12 @@ int gda_attn_decode(const void *q_sig, const void *q_noise, const void *k_sig_ca
 /* Static English description of a gda_status value. */
 const char *gda_status_string(int status);
 
+/*
+ * cudaError_t value of the most recent CUDA failure that made a call of this
+ * thread return GDA_ERR_CUDA (0 if none).  For diagnostics only.
+ */
+int gda_last_cuda_error(void);
+
 /* Bits of the device error word. */
 #define GDA_DEVERR_PREFILL_TIMEOUT 0x1u  /* a prefill pipeline wait ran out */
 #define GDA_DEVERR_BAD_LENGTH      0x2u  /* a decode cache length was outside [1, Lcap] */
