@@ -28,7 +28,7 @@ import torch
 __all__ = [
     "GDAError", "gda_attn_fwd", "gda_attn_fwd_f32", "gda_attn_decode",
     "gda_attn_decode_workspace_size", "gda_status_string", "gda_device_error",
-    "lambda_init_schedule", "library_path", "GDA_FLAG_NO_NORM",
+    "lambda_init_schedule", "library_path", "GDA_FLAG_NO_NORM", "gda_attn_decode_noalloc",
 ]
 
 GDA_OK = 0
@@ -82,6 +82,8 @@ def _load():
             lib.gda_attn_decode.argtypes = [P, P, P, P, P, P, P, F, P, I, I, I, I, I, I, F, P, Z, P]
             lib.gda_status_string.argtypes = [I]
             lib.gda_status_string.restype = ctypes.c_char_p
+            lib.gda_attn_decode_noalloc.argtypes = [P, P, P, P, P, P, P, F, P, I, I, I, I, I, I, F, P]
+            lib.gda_attn_decode_noalloc.restype = I
             lib.gda_device_error.argtypes = [I]
             lib.gda_last_cuda_error.argtypes = []
             lib.gda_last_cuda_error.restype = I
@@ -207,6 +209,38 @@ def gda_attn_decode(q_sig, q_noise, k_sig_cache, k_noise_cache, v_cache, cache_l
             _ptr(cache_lens), _ptr(lam), float(lambda_init), _ptr(out), B, Lcap, hs, hn, d, dv,
             float(eps), _ptr(workspace), ws_bytes, _stream(dev))
     _check(rc, "gda decode")
+    return out
+
+
+def gda_attn_decode_noalloc(q_sig, q_noise, k_sig_cache, k_noise_cache, v_cache, cache_lens,
+                            lam, lambda_init: float, *, eps: float = 1e-5, out=None):
+    """Decode without a workspace: the library's fixed scratch array holds the split partials.
+
+    For callers that cannot allocate device memory.  Calls that overlap on
+    the GPU race on the shared scratch array; see include/gda.h.
+    """
+    dev = q_sig.device
+    B, hs, d = q_sig.shape
+    hn = q_noise.shape[1]
+    Lcap = k_sig_cache.shape[1]
+    dv = v_cache.shape[3]
+    bf = torch.bfloat16
+    _expect(q_sig, "q_sig", bf, (B, hs, d), dev)
+    _expect(q_noise, "q_noise", bf, (B, hn, d), dev)
+    _expect(k_sig_cache, "k_sig_cache", bf, (B, Lcap, hs, d), dev)
+    _expect(k_noise_cache, "k_noise_cache", bf, (B, Lcap, hn, d), dev)
+    _expect(v_cache, "v_cache", bf, (B, Lcap, hs, dv), dev)
+    _expect(cache_lens, "cache_lens", torch.int32, (B,), dev)
+    _expect(lam, "lam", torch.float32, (hs,), dev)
+    if out is None:
+        out = torch.empty((B, hs, dv), dtype=bf, device=dev)
+    _expect(out, "out", bf, (B, hs, dv), dev)
+    with torch.cuda.device(dev):
+        rc = _load().gda_attn_decode_noalloc(
+            _ptr(q_sig), _ptr(q_noise), _ptr(k_sig_cache), _ptr(k_noise_cache), _ptr(v_cache),
+            _ptr(cache_lens), _ptr(lam), float(lambda_init), _ptr(out), B, Lcap, hs, hn, d, dv,
+            float(eps), _stream(dev))
+    _check(rc, "gda decode (no allocation)")
     return out
 
 

@@ -88,6 +88,8 @@ std::once_flag g_encode_once;
 
 }  // namespace
 
+int device_state(unsigned **err_word) { return current_device(err_word); }
+
 int record_cuda_error(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
     cudaGetLastError();   // do not leak a launch error into the caller's next check

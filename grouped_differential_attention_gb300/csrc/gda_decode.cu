@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 #include <cmath>
+#include <mutex>
 
 #include "gda.h"
 #include "gda_device.cuh"
@@ -349,3 +350,73 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
 }
 
 }  // namespace gda
+
+// ------------------------------------------------------------------------
+// Decode without any device allocation.
+//
+// Some callers cannot hand this library a workspace: for instance a plugin
+// or serving loop that owns no allocator (the host framework holds all
+// device memory in its own pool), or code that must never call cudaMalloc /
+// cudaFree because those calls can synchronise the device and stall other
+// work.  For them the decode's split partials live in one fixed scratch
+// array that is part of the library itself.  The array is a file-scope
+// __device__ object: every device that loads the library keeps its
+// GDA_DECODE_SCRATCH_BYTES until the process exits.  Host code may not use
+// the array's name as a pointer (on the host it is only a stand-in), so the
+// device address is fetched once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_decode_scratch[GDA_DECODE_SCRATCH_BYTES];
+
+namespace gda {
+namespace {
+constexpr int kScratchDevices = 64;
+struct ScratchState {
+    std::once_flag once;
+    void *ptr = nullptr;
+    int status = GDA_ERR_CUDA;
+};
+ScratchState g_scratch[kScratchDevices];
+
+// Device address of the scratch array on the current device (set up on the
+// first call for that device, with the device current).
+int scratch_address(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kScratchDevices) {
+        cudaGetLastError();
+        return GDA_ERR_CUDA;
+    }
+    ScratchState &s = g_scratch[dev];
+    std::call_once(s.once, [&s]() {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+        if (e != cudaSuccess) {
+            s.status = record_cuda_error(e);
+            return;
+        }
+        s.ptr = ptr;
+        s.status = GDA_OK;
+    });
+    *out = s.ptr;
+    return s.status;
+}
+}  // namespace
+
+}  // namespace gda
+
+extern "C" int gda_attn_decode_noalloc(const void *q_sig, const void *q_noise, const void *k_sig_cache,
+                                       const void *k_noise_cache, const void *v_cache,
+                                       const int *cache_lens, const float *lambda, float lambda_init,
+                                       void *out, int B, int Lcap, int h_s, int h_n, int d, int dv,
+                                       float eps, gda_stream_t stream) {
+    const size_t need = gda_attn_decode_workspace_size(B, Lcap, h_s, h_n, dv);
+    if (need > static_cast<size_t>(GDA_DECODE_SCRATCH_BYTES)) return GDA_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    if (need > 0) {
+        const int st = gda::scratch_address(&scratch);
+        if (st != GDA_OK) return st;
+    }
+    // invalid sizes (need == 0) are reported by the regular entry point
+    return gda_attn_decode(q_sig, q_noise, k_sig_cache, k_noise_cache, v_cache, cache_lens, lambda,
+                           lambda_init, out, B, Lcap, h_s, h_n, d, dv, eps, scratch,
+                           static_cast<size_t>(GDA_DECODE_SCRATCH_BYTES), stream);
+}
+

@@ -38,6 +38,10 @@ struct DecodeArgs {
 // clears the runtime's sticky-free error state and returns GDA_ERR_CUDA.
 int record_cuda_error(cudaError_t e);
 
+// Checks the current device (GB300, compute capability 10.3) once and
+// returns a gda_status plus the address of its device error word.
+int device_state(unsigned **err_word);
+
 // Each launcher validates nothing (the ABI layer did) and returns a
 // gda_status value.
 int launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);

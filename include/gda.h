@@ -142,6 +142,33 @@ int gda_attn_decode(const void *q_sig, const void *q_noise, const void *k_sig_ca
                     int h_s, int h_n, int d, int dv, float eps, void *workspace,
                     size_t workspace_bytes, gda_stream_t stream);
 
+/*
+ * Decode that allocates nothing and takes no workspace.  No counterpart on
+ * the pages: it exists for callers that cannot allocate device memory, such
+ * as a plugin or serving loop whose host framework owns all device memory in
+ * its own pool, or code that must not call cudaMalloc/cudaFree because those
+ * calls can synchronise the device.
+ *   Same arguments, layouts and result as gda_attn_decode, minus the
+ *   workspace.  The split partials go to a scratch array inside the library,
+ *   GDA_DECODE_SCRATCH_BYTES (32 MiB) per device, held by every device that
+ *   loads the library until the process exits.
+ *   Returns GDA_ERR_WORKSPACE if gda_attn_decode_workspace_size(B, Lcap, h_s,
+ *   h_n, dv) exceeds GDA_DECODE_SCRATCH_BYTES (e.g. 64 sequences of up to
+ *   8192 cached positions with 12 + 4 heads and dv = 128 need about 25 MB).
+ *   The first call on a device looks up the scratch array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   Every call shares the one array and it keeps the last call's contents
+ *   (the kernels write every value they later read, so nothing needs
+ *   clearing).  Calls whose work overlaps on the GPU, on any streams, race
+ *   on the array and produce wrong results: serialise them.
+ */
+#define GDA_DECODE_SCRATCH_BYTES (32u << 20)
+int gda_attn_decode_noalloc(const void *q_sig, const void *q_noise, const void *k_sig_cache,
+                            const void *k_noise_cache, const void *v_cache, const int *cache_lens,
+                            const float *lambda, float lambda_init, void *out, int B, int Lcap,
+                            int h_s, int h_n, int d, int dv, float eps, gda_stream_t stream);
+
 /* Static English description of a gda_status value. */
 const char *gda_status_string(int status);
 
