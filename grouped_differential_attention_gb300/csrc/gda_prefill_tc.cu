@@ -18,17 +18,20 @@
 //                K stages (K1 and K2 tiles) and a ring of V stages;
 //   warp 1       TMEM allocator and MMA issuer (one elected lane);
 //   warps 2-5    softmax of the signal map, warps 6-9 of the noise map
-//                (thread = query row = TMEM lane).  The TMEM load of the next
-//                S tile is issued before the current tile's exponentials, so
-//                its latency hides under them.
+//                (thread = query row = TMEM lane).  The next S tile's row is
+//                requested from TMEM as soon as the current row's exponentials
+//                are done, so its latency overlaps the P-store wait and the
+//                barrier arrive.
 // KV tiles are 64 keys.  TMEM (512 columns): O1 [0,128) | O2 [128,256) |
 // S1 tiles [256,320) [320,384) | S2 tiles [384,448) [448,512): each map's S
 // is double-buffered, so QK(j+2) runs on the tensor core while the softmax
 // of tile j+1 runs, and the softmax warps never wait on their own map's PV.
 // P overwrites the first 32 columns of its S tile and feeds the PV MMA
 // straight from TMEM.  P is rounded to bf16 with an integer add and a byte
-// permute, leaving the special-function unit to the exponentials.  A row's running max only moves when it grows by
-// more than 2^8 (exp2 units); only then is its accumulator rescaled.
+// permute, leaving the special-function unit (which also executes the bf16
+// conversion instruction) to the exponentials.  A row's running max only
+// moves when it grows by more than 2^8 (exp2 units); only then is its
+// accumulator rescaled.
 // dv = 256 is split over a 2-CTA cluster; the two CTAs exchange the per-row
 // sum of squares through distributed shared memory for the RMSNorm.
 #include <cuda.h>
@@ -369,7 +372,8 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
 #pragma unroll
             for (int cch = 0; cch < BN / 32; ++cch)
                 tmem_ld32(tSm + cch * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[cch * 32]));
-            tmem_ld_wait();
+            tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+            reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         } else {
             ok = false;
         }
@@ -462,7 +466,10 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
             }
             tc_fence_before();
             mbar_arrive(&ctl->p_full[m][j & 1]);
-            if (more) tmem_ld_wait();
+            if (more) {
+                tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+            }
         }
         // drain any TMEM load still in flight after an early exit
         tmem_ld_wait();
