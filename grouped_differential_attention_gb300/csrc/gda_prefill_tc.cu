@@ -12,7 +12,11 @@
 // running (max, sum) states and two float32 accumulators per query row; no
 // L x L map ever leaves the SM.
 //
-// CTA = (query tile of 128 rows, batch b, signal head h, dv slice of 128).
+// Persistent: one CTA per SM (a CTA pair per two SMs for dv = 256) walks a
+// list of work items (query tile of 128 rows, batch b, signal head h; the
+// pair splits dv into two 128-column slices).  Barriers and TMEM are set up
+// once; the next item's Q load and first two QK MMAs overlap the current
+// item's epilogue.
 // 10 warps:
 //   warp 0       TMA producer (one elected lane): Q1/Q2 once, then a ring of
 //                K stages (K1 and K2 tiles) and a ring of V stages;
@@ -33,7 +37,8 @@
 // moves when it grows by more than 2^8 (exp2 units); only then is its
 // accumulator rescaled.
 // dv = 256 is split over a 2-CTA cluster; the two CTAs exchange the per-row
-// sum of squares through distributed shared memory for the RMSNorm.
+// sum of squares through distributed shared memory (remote store plus remote
+// mbarrier arrive) for the RMSNorm.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -58,19 +63,21 @@ template <> struct TcCfg<64> { static constexpr int BN = 64, KS = 4, VS = 4; };
 template <> struct TcCfg<128> { static constexpr int BN = 64, KS = 3, VS = 3; };
 
 struct Ctrl {
-    uint64_t q_full;
+    uint64_t q_full, q_empty;
     uint64_t k_full[4], k_empty[4];
     uint64_t v_full[4], v_empty[4];
     uint64_t s_full[2][2];      // [map][S buffer]
     uint64_t p_full[2][2];      // [map][S buffer]
     uint64_t o_done[2];         // [map]: one phase per PV
-    uint64_t o_final;           // every MMA of the CTA has completed
+    uint64_t o_final;           // every MMA of the current item has completed
+    uint64_t o_free;            // the epilogue has read the accumulators
+    uint64_t peer_bar[2];       // peer CTA's sum of squares arrived (dv = 256)
     uint64_t mma_idle;
     uint32_t tmem_base;
     int abort_flag;
     float l_row[2][kBM];        // [map][row]
     float ss_part[2][kBM];      // [warpgroup][row]
-    float ss_peer[kBM];
+    float ss_peer[2][kBM];
 };
 
 template <int D> struct Layout {
@@ -162,6 +169,79 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t va, 
     }
 }
 
+// Work item = (query tile, batch, signal head); item 0 is the longest (last
+// query tile).  Persistent CTAs (or CTA pairs for dv = 256) take items in a
+// snake order: round r takes item r*G + c for even r and r*G + G-1-c for odd
+// r (G CTAs or pairs, c this CTA's index), which evens out the causal lengths.
+struct Item {
+    int b, h, g, q0, nkv;
+};
+
+__device__ __forceinline__ bool item_of(const TcParams &p, int r, int G, int cid, int bn, Item &it) {
+    const int nitems = p.nqt * p.B * p.hs;
+    const int k = (r & 1) ? (G - 1 - cid) : cid;
+    const long long idx = static_cast<long long>(r) * G + k;
+    if (idx >= nitems) return false;
+    const int i = static_cast<int>(idx);
+    const int qt = p.nqt - 1 - i / (p.B * p.hs);
+    const int rem = i % (p.B * p.hs);
+    it.b = rem / p.hs;
+    it.h = rem % p.hs;
+    it.g = it.h / (p.hs / p.hn);
+    it.q0 = qt * kBM;
+    const int kv_end = p.causal ? min(p.L, it.q0 + kBM) : p.L;
+    it.nkv = (kv_end + bn - 1) / bn;
+    return true;
+}
+
+// OR of `pred` over the `count` threads that reach named barrier `id`.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return out != 0;
+}
+
+// Arrive on the peer CTA's mbarrier (release at cluster scope: the data
+// stored to the peer before this arrive is visible to its waiter).
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t *local_bar, uint32_t peer) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_bar)), "r"(peer));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+// Bounded wait with acquire at cluster scope (pairs with mbar_arrive_remote).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, unsigned *err,
+                                                  volatile int *abort) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((it & 15u) == 15u) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+                atomicOr(err, GDA_DEVERR_PREFILL_TIMEOUT);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
@@ -180,23 +260,13 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
     Ctrl *ctl = reinterpret_cast<Ctrl *>(smem + LY::TILES);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-
-    // ---- work item: longest (last) query tiles are launched first
-    int c = blockIdx.x;
-    const int slice = c % p.nslices;
-    c /= p.nslices;
-    const int h = c % p.hs;
-    c /= p.hs;
-    const int b = c % p.B;
-    c /= p.B;
-    const int qt = p.nqt - 1 - c;
-    const int q0 = qt * kBM;
-    const int g = h / (p.hs / p.hn);
-    const int kv_end = p.causal ? min(p.L, q0 + kBM) : p.L;
-    const int nkv = (kv_end + BN - 1) / BN;
+    const int slice = blockIdx.x % p.nslices;
+    const int cid = blockIdx.x / p.nslices;
+    const int G = gridDim.x / p.nslices;
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl->q_full, 1);
+        mbar_init(&ctl->q_empty, 1);
         for (int s = 0; s < KS; ++s) {
             mbar_init(&ctl->k_full[s], 1);
             mbar_init(&ctl->k_empty[s], 1);
@@ -211,8 +281,10 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                 mbar_init(&ctl->p_full[m][bb], 128);
             }
             mbar_init(&ctl->o_done[m], 1);
+            mbar_init(&ctl->peer_bar[m], 128);
         }
         mbar_init(&ctl->o_final, 1);
+        mbar_init(&ctl->o_free, 32 * kSoftmaxWarps);
         mbar_init(&ctl->mma_idle, 1);
         ctl->abort_flag = 0;
         fence_mbar_init();
@@ -236,60 +308,76 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
             tma_prefetch_desc(&tmQ2);
             tma_prefetch_desc(&tmK2);
             tma_prefetch_desc(&tmV);
-            mbar_arrive_expect_tx(&ctl->q_full, 2 * LY::Q_BYTES);
-#pragma unroll
-            for (int blk = 0; blk < D / 64; ++blk) {
-                tma_load_4d(smem + LY::OFF_Q1 + blk * kBM * 128, &tmQ1, &ctl->q_full, blk * 64, h, q0, b);
-                tma_load_4d(smem + LY::OFF_Q2 + blk * kBM * 128, &tmQ2, &ctl->q_full, blk * 64, g, q0, b);
-            }
-            auto load_k = [&](int j) {
-                const int st = j % KS;
-                uint8_t *sb = smem + LY::OFF_K + st * LY::KST_BYTES;
-                mbar_arrive_expect_tx(&ctl->k_full[st], LY::KST_BYTES);
+            uint32_t kt = 0, vt = 0;           // K / V tiles issued so far (all items)
+            int nq = 0;                        // Q loads issued
+            bool ok = true;
+            Item it;
+            for (int r = 0; ok && item_of(p, r, G, cid, BN, it); ++r) {
+                // Q of the previous item must have been read by its last QK
+                if (r > 0 && !wait_bar(&ctl->q_empty, (r - 1) & 1, p.err, abort_flag)) break;
+                mbar_arrive_expect_tx(&ctl->q_full, 2 * LY::Q_BYTES);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk) {
-                    tma_load_4d(sb + blk * BN * 128, &tmK1, &ctl->k_full[st], blk * 64, h, j * BN, b);
-                    tma_load_4d(sb + LY::K_BYTES + blk * BN * 128, &tmK2, &ctl->k_full[st], blk * 64, g,
-                                j * BN, b);
+                    tma_load_4d(smem + LY::OFF_Q1 + blk * kBM * 128, &tmQ1, &ctl->q_full, blk * 64, it.h,
+                                it.q0, it.b);
+                    tma_load_4d(smem + LY::OFF_Q2 + blk * kBM * 128, &tmQ2, &ctl->q_full, blk * 64, it.g,
+                                it.q0, it.b);
                 }
-            };
-            auto load_v = [&](int j) {
-                const int st = j % VS;
-                uint8_t *sb = smem + LY::OFF_V + st * LY::V_BYTES;
-                mbar_arrive_expect_tx(&ctl->v_full[st], LY::V_BYTES);
+                ++nq;
+                auto load_k = [&](int j) -> bool {
+                    const uint32_t gk = kt + j;
+                    const int st = gk % KS;
+                    if (gk >= KS && !wait_bar(&ctl->k_empty[st], ((gk / KS) - 1) & 1, p.err, abort_flag))
+                        return false;
+                    uint8_t *sb = smem + LY::OFF_K + st * LY::KST_BYTES;
+                    mbar_arrive_expect_tx(&ctl->k_full[st], LY::KST_BYTES);
 #pragma unroll
-                for (int blk = 0; blk < kDVS / 64; ++blk)
-                    tma_load_4d(sb + blk * BN * 128, &tmV, &ctl->v_full[st], slice * kDVS + blk * 64, h,
-                                j * BN, b);
-            };
-            // K runs two tiles ahead of V (QK(j+2) is issued right after PV(j))
-            int k_issued = 0, v_issued = 0;
-            for (int t = 0; t < 2 && t < nkv; ++t) {
-                load_k(t);
-                k_issued = t + 1;
-            }
-            for (int j = 0; j < nkv; ++j) {
-                if (j + 2 < nkv) {
-                    const int jk = j + 2;
-                    if (jk >= KS && !wait_bar(&ctl->k_empty[jk % KS], ((jk / KS) - 1) & 1, p.err, abort_flag))
-                        break;
-                    load_k(jk);
-                    k_issued = jk + 1;
+                    for (int blk = 0; blk < D / 64; ++blk) {
+                        tma_load_4d(sb + blk * BN * 128, &tmK1, &ctl->k_full[st], blk * 64, it.h, j * BN, it.b);
+                        tma_load_4d(sb + LY::K_BYTES + blk * BN * 128, &tmK2, &ctl->k_full[st], blk * 64, it.g,
+                                    j * BN, it.b);
+                    }
+                    return true;
+                };
+                auto load_v = [&](int j) -> bool {
+                    const uint32_t gv = vt + j;
+                    const int st = gv % VS;
+                    if (gv >= VS && !wait_bar(&ctl->v_empty[st], ((gv / VS) - 1) & 1, p.err, abort_flag))
+                        return false;
+                    uint8_t *sb = smem + LY::OFF_V + st * LY::V_BYTES;
+                    mbar_arrive_expect_tx(&ctl->v_full[st], LY::V_BYTES);
+#pragma unroll
+                    for (int blk = 0; blk < kDVS / 64; ++blk)
+                        tma_load_4d(sb + blk * BN * 128, &tmV, &ctl->v_full[st], slice * kDVS + blk * 64, it.h,
+                                    j * BN, it.b);
+                    return true;
+                };
+                // K runs two tiles ahead of V (QK(j+2) is issued right after PV(j))
+                int kdone = 0, vdone = 0;
+                for (int t = 0; ok && t < 2 && t < it.nkv; ++t) {
+                    ok = load_k(t);
+                    if (ok) ++kdone;
                 }
-                if (j >= VS && !wait_bar(&ctl->v_empty[j % VS], ((j / VS) - 1) & 1, p.err, abort_flag))
-                    break;
-                load_v(j);
-                v_issued = j + 1;
+                for (int j = 0; ok && j < it.nkv; ++j) {
+                    if (j + 2 < it.nkv) {
+                        ok = load_k(j + 2);
+                        if (!ok) break;
+                        ++kdone;
+                    }
+                    ok = load_v(j);
+                    if (ok) ++vdone;
+                }
+                kt += kdone;
+                vt += vdone;
             }
             // our own copies must land before the CTA may exit
-            drain_wait(&ctl->q_full, 0, p.err);
-            for (int j = (k_issued > KS ? k_issued - KS : 0); j < k_issued; ++j)
+            if (nq > 0) drain_wait(&ctl->q_full, (nq - 1) & 1, p.err);
+            for (uint32_t j = (kt > KS ? kt - KS : 0); j < kt; ++j)
                 drain_wait(&ctl->k_full[j % KS], (j / KS) & 1, p.err);
-            for (int j = (v_issued > VS ? v_issued - VS : 0); j < v_issued; ++j)
+            for (uint32_t j = (vt > VS ? vt - VS : 0); j < vt; ++j)
                 drain_wait(&ctl->v_full[j % VS], (j / VS) & 1, p.err);
         }
         __syncwarp();
-        if (p.nslices == 2) cluster_sync_all();
     } else if (warp == 1) {
         // ================================================= MMA issuer
         if (elect_one()) {
@@ -299,55 +387,74 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
             const uint32_t q2a = smem_u32(smem + LY::OFF_Q2);
             const uint32_t k0a = smem_u32(smem + LY::OFF_K);
             const uint32_t v0a = smem_u32(smem + LY::OFF_V);
-            bool ok = wait_bar(&ctl->q_full, 0, p.err, abort_flag);
-            // QK of the first two tiles fill both S buffers of both maps
-            for (int t = 0; ok && t < 2 && t < nkv; ++t) {
-                if (!wait_bar(&ctl->k_full[t % KS], (t / KS) & 1, p.err, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t ka = k0a + (t % KS) * LY::KST_BYTES;
-                issue_qk<D>(tS1 + t * BN, q1a, ka);
-                mma_commit(&ctl->s_full[0][t]);
-                issue_qk<D>(tS2 + t * BN, q2a, ka + LY::K_BYTES);
-                mma_commit(&ctl->s_full[1][t]);
-                mma_commit(&ctl->k_empty[t % KS]);
-            }
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int bb = j & 1;
-                const uint32_t va = v0a + (j % VS) * LY::V_BYTES;
-                const int jn = j + 2;                       // next tile for this S buffer
-                const bool more = jn < nkv;
-                const uint32_t kan = k0a + (jn % KS) * LY::KST_BYTES;
-                // signal map: PV1(j), then QK1(j+2) into the S1 buffer PV1(j) just read
-                if (!wait_bar(&ctl->p_full[0][bb], (j >> 1) & 1, p.err, abort_flag)) break;
-                if (!wait_bar(&ctl->v_full[j % VS], (j / VS) & 1, p.err, abort_flag)) break;
-                tc_fence_after();
-                issue_pv<D>(tO1, tS1 + bb * BN, va, j > 0);
-                mma_commit(&ctl->o_done[0]);
-                if (more) {
-                    if (!wait_bar(&ctl->k_full[jn % KS], (jn / KS) & 1, p.err, abort_flag)) break;
+            uint32_t kt = 0, vt = 0, gt = 0;
+            bool ok = true;
+            Item it;
+            for (int r = 0; ok && item_of(p, r, G, cid, BN, it); ++r) {
+                const int nkv = it.nkv;
+                if (!wait_bar(&ctl->q_full, r & 1, p.err, abort_flag)) break;
+                // QK of the item's first two tiles; their S buffers were last
+                // read by PVs already issued.  This overlaps the previous
+                // item's epilogue.
+                for (int t = 0; t < 2 && t < nkv; ++t) {
+                    const uint32_t gk = kt + t, gs = gt + t;
+                    if (!wait_bar(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    issue_qk<D>(tS1 + bb * BN, q1a, kan);
-                    mma_commit(&ctl->s_full[0][bb]);
+                    const uint32_t ka = k0a + (gk % KS) * LY::KST_BYTES;
+                    issue_qk<D>(tS1 + (gs & 1) * BN, q1a, ka);
+                    mma_commit(&ctl->s_full[0][gs & 1]);
+                    issue_qk<D>(tS2 + (gs & 1) * BN, q2a, ka + LY::K_BYTES);
+                    mma_commit(&ctl->s_full[1][gs & 1]);
+                    mma_commit(&ctl->k_empty[gk % KS]);
                 }
-                // noise map: PV2(j), release V(j), then QK2(j+2) and release K(j+2)
-                if (!wait_bar(&ctl->p_full[1][bb], (j >> 1) & 1, p.err, abort_flag)) break;
-                tc_fence_after();
-                issue_pv<D>(tO2, tS2 + bb * BN, va, j > 0);
-                mma_commit(&ctl->o_done[1]);
-                mma_commit(&ctl->v_empty[j % VS]);
-                if (more) {
-                    issue_qk<D>(tS2 + bb * BN, q2a, kan + LY::K_BYTES);
-                    mma_commit(&ctl->s_full[1][bb]);
-                    mma_commit(&ctl->k_empty[jn % KS]);
+                if (!ok) break;
+                if (nkv <= 2) mma_commit(&ctl->q_empty);
+                // the accumulators are free once the previous item's epilogue has read them
+                if (r > 0 && !wait_bar(&ctl->o_free, (r - 1) & 1, p.err, abort_flag)) break;
+                for (int j = 0; j < nkv; ++j) {
+                    const uint32_t gs = gt + j, gv = vt + j;
+                    const int bb = gs & 1;
+                    const uint32_t va = v0a + (gv % VS) * LY::V_BYTES;
+                    const int jn = j + 2;                       // next tile for this S buffer
+                    const bool more = jn < nkv;
+                    const uint32_t gk = kt + jn;
+                    const uint32_t kan = k0a + (gk % KS) * LY::KST_BYTES;
+                    // signal map: PV1(j), then QK1(j+2) into the S1 buffer PV1(j) just read
+                    if (!wait_bar(&ctl->p_full[0][bb], (gs >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_bar(&ctl->v_full[gv % VS], (gv / VS) & 1, p.err, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv<D>(tO1, tS1 + bb * BN, va, j > 0);
+                    mma_commit(&ctl->o_done[0]);
+                    if (more) {
+                        if (!wait_bar(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_qk<D>(tS1 + bb * BN, q1a, kan);
+                        mma_commit(&ctl->s_full[0][bb]);
+                    }
+                    // noise map: PV2(j), release V(j), then QK2(j+2) and release K(j+2)
+                    if (!wait_bar(&ctl->p_full[1][bb], (gs >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv<D>(tO2, tS2 + bb * BN, va, j > 0);
+                    mma_commit(&ctl->o_done[1]);
+                    mma_commit(&ctl->v_empty[gv % VS]);
+                    if (more) {
+                        issue_qk<D>(tS2 + bb * BN, q2a, kan + LY::K_BYTES);
+                        mma_commit(&ctl->s_full[1][bb]);
+                        mma_commit(&ctl->k_empty[gk % KS]);
+                        if (jn == nkv - 1) mma_commit(&ctl->q_empty);
+                    }
                 }
-                if (j == nkv - 1) mma_commit(&ctl->o_final);
+                if (!ok) break;
+                mma_commit(&ctl->o_final);
+                kt += nkv;
+                vt += nkv;
+                gt += nkv;
             }
             // every issued MMA completes before TMEM is released
             mma_commit(&ctl->mma_idle);
             drain_wait(&ctl->mma_idle, 0, p.err);
         }
         __syncwarp();
-        if (p.nslices == 2) cluster_sync_all();
     } else {
         // ================================================= softmax groups
         const int m = (warp - 2) / 4;             // 0: signal map, 1: noise map
@@ -356,195 +463,215 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tSm = tmem + 256 + m * 2 * BN + lane_off;   // + buffer * BN
         const uint32_t tOm = tmem + m * 128 + lane_off;
-        const int qrow = q0 + row;
-        const int last_key = p.causal ? min(qrow, p.L - 1) : p.L - 1;
         const float sl2 = p.scale_log2;
-        float m_ref = -INFINITY;
-        float l = 0.f;
-        bool ok = true;
+        uint32_t gt = 0;
+        Item it;
+        for (int r = 0; item_of(p, r, G, cid, BN, it); ++r) {
+            const int nkv = it.nkv;
+            const int qrow = it.q0 + row;
+            const int last_key = p.causal ? min(qrow, p.L - 1) : p.L - 1;
+            float m_ref = -INFINITY;
+            float l = 0.f;
+            bool ok = true;
 
-        // r holds the current tile's S row; the next tile's row is requested
-        // into the same registers once the exponentials have consumed them, so
-        // its TMEM latency overlaps the P-store wait and the barrier arrive.
-        uint32_t r[BN];
-        if (warp_wait(&ctl->s_full[m][0], 0, p.err, abort_flag)) {
-            tc_fence_after();
-#pragma unroll
-            for (int cch = 0; cch < BN / 32; ++cch)
-                tmem_ld32(tSm + cch * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[cch * 32]));
-            tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-            reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-        } else {
-            ok = false;
-        }
-        for (int j = 0; ok && j < nkv; ++j) {
-            const uint32_t tS = tSm + (j & 1) * BN;
-            const int k0 = j * BN;
-            const bool need_mask = (p.causal && k0 + BN - 1 > q0) || (k0 + BN > p.L);
-            if (need_mask) {
-#pragma unroll
-                for (int e = 0; e < BN; ++e)
-                    if (k0 + e > last_key) r[e] = __float_as_uint(-INFINITY);
-            }
-            // row maximum: three-input max over 4 independent chains
-            float mx4[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) mx4[i] = __uint_as_float(r[i]);
-#pragma unroll
-            for (int e = 4; e + 8 <= BN; e += 8)
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    mx4[i] = max3f(mx4[i], __uint_as_float(r[e + 2 * i]), __uint_as_float(r[e + 2 * i + 1]));
-            float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
-#pragma unroll
-            for (int e = 4 + ((BN - 4) / 8) * 8; e < BN; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
-            const float mx_s = mx * sl2;
-            float alpha = 1.f;
-            bool rescale = false;
-            if (j == 0) {
-                m_ref = mx_s;
-            } else if (mx_s > m_ref + kRescaleThreshold) {
-                alpha = fast_exp2(m_ref - mx_s);
-                m_ref = mx_s;
-                rescale = true;
-            }
-            // P = 2^(s*scale - m_ref) (hidden keys hold -inf and give 0)
-            const float neg_m = -m_ref;
-            float sa = 0.f, sb = 0.f, sc = 0.f, sd = 0.f;
-#pragma unroll
-            for (int hh = 0; hh < BN / 32; ++hh) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    float x0 = __uint_as_float(r[hh * 32 + e]), x1 = __uint_as_float(r[hh * 32 + e + 1]);
-                    float x2 = __uint_as_float(r[hh * 32 + e + 2]), x3 = __uint_as_float(r[hh * 32 + e + 3]);
-                    ffma2(x0, x1, sl2, sl2, neg_m, neg_m);
-                    ffma2(x2, x3, sl2, sl2, neg_m, neg_m);
-                    x0 = fast_exp2(x0);
-                    x1 = fast_exp2(x1);
-                    x2 = fast_exp2(x2);
-                    x3 = fast_exp2(x3);
-                    fadd2(sa, sb, x0, x1);
-                    fadd2(sc, sd, x2, x3);
-                    pk[e / 2] = pack_hi16(round_bf16_bits(x0), round_bf16_bits(x1));
-                    pk[e / 2 + 1] = pack_hi16(round_bf16_bits(x2), round_bf16_bits(x3));
-                }
-                tmem_st16(tS + hh * 16, pk);
-            }
-            l = l * alpha + ((sa + sb) + (sc + sd));
-            // request the next S tile into r
-            const bool more = j + 1 < nkv;
-            if (more) {
-                if (!warp_wait(&ctl->s_full[m][(j + 1) & 1], ((j + 1) >> 1) & 1, p.err, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+            // r holds the current tile's S row; the next tile's row is requested
+            // into the same registers once the exponentials have consumed them,
+            // so its TMEM latency overlaps the P-store wait and the barrier arrive.
+            uint32_t rr[BN];
+            if (warp_wait(&ctl->s_full[m][gt & 1], (gt >> 1) & 1, p.err, abort_flag)) {
                 tc_fence_after();
-                const uint32_t tSn = tSm + ((j + 1) & 1) * BN;
 #pragma unroll
                 for (int cch = 0; cch < BN / 32; ++cch)
-                    tmem_ld32(tSn + cch * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[cch * 32]));
+                    tmem_ld32(tSm + (gt & 1) * BN + cch * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[cch * 32]));
+                tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
+                reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
+            } else {
+                ok = false;
             }
-            tmem_st_wait();
-            if (__any_sync(0xffffffffu, rescale)) {
-                // the accumulator may only be touched once PV(j-1) has completed
-                if (!warp_wait(&ctl->o_done[m], (j - 1) & 1, p.err, abort_flag)) {
-                    ok = false;
-                    break;
+            for (int j = 0; ok && j < nkv; ++j) {
+                const uint32_t gs = gt + j;
+                const uint32_t tS = tSm + (gs & 1) * BN;
+                const int k0 = j * BN;
+                const bool need_mask = (p.causal && k0 + BN - 1 > it.q0) || (k0 + BN > p.L);
+                if (need_mask) {
+#pragma unroll
+                    for (int e = 0; e < BN; ++e)
+                        if (k0 + e > last_key) rr[e] = __float_as_uint(-INFINITY);
                 }
-                tc_fence_after();
+                // row maximum: three-input max over 4 independent chains
+                float mx4[4];
 #pragma unroll
-                for (int cch = 0; cch < kDVS / 32; ++cch) {
-                    uint32_t o[32];
-                    tmem_ld32(tOm + cch * 32, o);
-                    tmem_ld_wait();
+                for (int i = 0; i < 4; ++i) mx4[i] = __uint_as_float(rr[i]);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(tOm + cch * 32, o);
+                for (int e = 4; e + 8 <= BN; e += 8)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        mx4[i] = max3f(mx4[i], __uint_as_float(rr[e + 2 * i]), __uint_as_float(rr[e + 2 * i + 1]));
+                float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+#pragma unroll
+                for (int e = 4 + ((BN - 4) / 8) * 8; e < BN; ++e) mx = fmaxf(mx, __uint_as_float(rr[e]));
+                const float mx_s = mx * sl2;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (j == 0) {
+                    m_ref = mx_s;
+                } else if (mx_s > m_ref + kRescaleThreshold) {
+                    alpha = fast_exp2(m_ref - mx_s);
+                    m_ref = mx_s;
+                    rescale = true;
+                }
+                // P = 2^(s*scale - m_ref) (hidden keys hold -inf and give 0)
+                const float neg_m = -m_ref;
+                float sa = 0.f, sb = 0.f, sc = 0.f, sd = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < BN / 32; ++hh) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        float x0 = __uint_as_float(rr[hh * 32 + e]), x1 = __uint_as_float(rr[hh * 32 + e + 1]);
+                        float x2 = __uint_as_float(rr[hh * 32 + e + 2]), x3 = __uint_as_float(rr[hh * 32 + e + 3]);
+                        ffma2(x0, x1, sl2, sl2, neg_m, neg_m);
+                        ffma2(x2, x3, sl2, sl2, neg_m, neg_m);
+                        x0 = fast_exp2(x0);
+                        x1 = fast_exp2(x1);
+                        x2 = fast_exp2(x2);
+                        x3 = fast_exp2(x3);
+                        fadd2(sa, sb, x0, x1);
+                        fadd2(sc, sd, x2, x3);
+                        pk[e / 2] = pack_hi16(round_bf16_bits(x0), round_bf16_bits(x1));
+                        pk[e / 2 + 1] = pack_hi16(round_bf16_bits(x2), round_bf16_bits(x3));
+                    }
+                    tmem_st16(tS + hh * 16, pk);
+                }
+                l = l * alpha + ((sa + sb) + (sc + sd));
+                // request the next S tile into rr
+                const bool more = j + 1 < nkv;
+                if (more) {
+                    if (!warp_wait(&ctl->s_full[m][(gs + 1) & 1], ((gs + 1) >> 1) & 1, p.err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tSn = tSm + ((gs + 1) & 1) * BN;
+#pragma unroll
+                    for (int cch = 0; cch < BN / 32; ++cch)
+                        tmem_ld32(tSn + cch * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[cch * 32]));
                 }
                 tmem_st_wait();
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // the accumulator may only be touched once PV(j-1) has completed
+                    if (!warp_wait(&ctl->o_done[m], (gs - 1) & 1, p.err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int cch = 0; cch < kDVS / 32; ++cch) {
+                        uint32_t o[32];
+                        tmem_ld32(tOm + cch * 32, o);
+                        tmem_ld_wait_regs(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(tOm + cch * 32, o);
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                mbar_arrive(&ctl->p_full[m][gs & 1]);
+                if (more) {
+                    tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
+                    reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
+                }
             }
-            tc_fence_before();
-            mbar_arrive(&ctl->p_full[m][j & 1]);
-            if (more) {
-                tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-            }
-        }
-        // drain any TMEM load still in flight after an early exit
-        tmem_ld_wait();
+            // drain any TMEM load still in flight after an early exit
+            tmem_ld_wait();
 
-        // ---------------------------------------------------- epilogue
-        ctl->l_row[m][row] = l;
-        named_bar_sync(1, 32 * kSoftmaxWarps);
-        const float l1 = ctl->l_row[0][row];
-        const float l2 = ctl->l_row[1][row];
-        ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
-        if (ok) ok = warp_wait(&ctl->o_final, 0, p.err, abort_flag);
-        tc_fence_after();
-        const float lam = p.lambda[h];
-        const float inv1 = 1.f / l1;
-        const float c2 = lam / l2;
-        const uint32_t tO1 = tmem + lane_off, tO2 = tmem + 128 + lane_off;
-        const int col0 = m * 64;                  // this warpgroup's 64 columns of the slice
-        float ss = 0.f;
-        if (ok) {
+            // ------------------------------------------------ epilogue of the item
+            ctl->l_row[m][row] = l;
+            named_bar_sync(1, 32 * kSoftmaxWarps);
+            const float l1 = ctl->l_row[0][row];
+            const float l2 = ctl->l_row[1][row];
+            ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
+            if (ok) ok = warp_wait(&ctl->o_final, r & 1, p.err, abort_flag);
+            tc_fence_after();
+            const float lam = p.lambda[it.h];
+            const float inv1 = 1.f / l1;
+            const float c2 = lam / l2;
+            const uint32_t tO1 = tmem + lane_off, tO2 = tmem + 128 + lane_off;
+            const int col0 = m * 64;                  // this warpgroup's 64 columns of the slice
+            float ss = 0.f;
+            if (ok) {
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t r1[32], r2[32];
-                tmem_ld32(tO1 + col0 + cc * 32, r1);
-                tmem_ld32(tO2 + col0 + cc * 32, r2);
-                tmem_ld_wait();
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t r1[32], r2[32];
+                    tmem_ld32(tO1 + col0 + cc * 32, r1);
+                    tmem_ld32(tO2 + col0 + cc * 32, r2);
+                    tmem_ld_wait_regs(r1);
+                    reg_fence(r2);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float o = __fmul_rn(__uint_as_float(r1[e]), inv1) - __fmul_rn(__uint_as_float(r2[e]), c2);
-                    ss = fmaf(o, o, ss);
+                    for (int e = 0; e < 32; ++e) {
+                        // both products rounded before the subtraction (no FMA
+                        // contraction), so equal maps with lambda = 1 cancel exactly
+                        const float o = __fmul_rn(__uint_as_float(r1[e]), inv1) - __fmul_rn(__uint_as_float(r2[e]), c2);
+                        ss = fmaf(o, o, ss);
+                    }
                 }
             }
-        }
-        ctl->ss_part[m][row] = ss;
-        named_bar_sync(1, 32 * kSoftmaxWarps);
-        float ss_tot = ctl->ss_part[0][row] + ctl->ss_part[1][row];
-        if (p.nslices == 2) {
-            if (m == 0) st_cluster_f32(&ctl->ss_peer[row], cluster_ctarank() ^ 1u, ss_tot);
-            cluster_sync_all();
-            ss_tot += ctl->ss_peer[row];
-        }
-        const float yscale =
-            p.no_norm ? 1.f : (1.f - p.lambda_init) * rsqrtf(ss_tot / static_cast<float>(p.dv) + p.eps);
-        if (ok) {
-            __nv_bfloat16 *orow =
-                p.out + ((static_cast<size_t>(b) * p.L + qrow) * p.hs + h) * p.dv + slice * kDVS + col0;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t r1[32], r2[32];
-                tmem_ld32(tO1 + col0 + cc * 32, r1);
-                tmem_ld32(tO2 + col0 + cc * 32, r2);
-                tmem_ld_wait();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    // both products rounded before the subtraction (no FMA
-                    // contraction), so equal maps with lambda = 1 cancel exactly
-                    const float y0 = (__fmul_rn(__uint_as_float(r1[e]), inv1) -
-                                      __fmul_rn(__uint_as_float(r2[e]), c2)) * yscale;
-                    const float y1 = (__fmul_rn(__uint_as_float(r1[e + 1]), inv1) -
-                                      __fmul_rn(__uint_as_float(r2[e + 1]), c2)) * yscale;
-                    pk[e / 2] = pack_bf16x2(y0, y1);
+            ctl->ss_part[m][row] = ss;
+            named_bar_sync(1, 32 * kSoftmaxWarps);
+            float ss_tot = ctl->ss_part[0][row] + ctl->ss_part[1][row];
+            if (p.nslices == 2) {
+                const int pb = r & 1;
+                if (m == 0) {
+                    st_cluster_f32(&ctl->ss_peer[pb][row], cluster_ctarank() ^ 1u, ss_tot);
+                    mbar_arrive_remote(&ctl->peer_bar[pb], cluster_ctarank() ^ 1u);
                 }
-                if (qrow < p.L) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+                if (!mbar_wait_cluster(&ctl->peer_bar[pb], (r >> 1) & 1, p.err, abort_flag)) ok = false;
+                ss_tot += ctl->ss_peer[pb][row];
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            const float yscale =
+                p.no_norm ? 1.f : (1.f - p.lambda_init) * rsqrtf(ss_tot / static_cast<float>(p.dv) + p.eps);
+            if (ok) {
+                __nv_bfloat16 *orow =
+                    p.out + ((static_cast<size_t>(it.b) * p.L + qrow) * p.hs + it.h) * p.dv + slice * kDVS + col0;
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t r1[32], r2[32];
+                    tmem_ld32(tO1 + col0 + cc * 32, r1);
+                    tmem_ld32(tO2 + col0 + cc * 32, r2);
+                    tmem_ld_wait_regs(r1);
+                    reg_fence(r2);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float y0 = (__fmul_rn(__uint_as_float(r1[e]), inv1) -
+                                          __fmul_rn(__uint_as_float(r2[e]), c2)) * yscale;
+                        const float y1 = (__fmul_rn(__uint_as_float(r1[e + 1]), inv1) -
+                                          __fmul_rn(__uint_as_float(r2[e + 1]), c2)) * yscale;
+                        pk[e / 2] = pack_bf16x2(y0, y1);
+                    }
+                    if (qrow < p.L) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    }
                 }
             }
+            // the accumulators may now be overwritten by the next item's first PV
+            tc_fence_before();
+            mbar_arrive(&ctl->o_free);
+            gt += nkv;
+            // every softmax thread agrees on whether to go on
+            if (bar_red_or(1, 32 * kSoftmaxWarps, !ok || *abort_flag)) break;
         }
     }
 
     // ---- teardown: all TMEM traffic of this CTA is complete past this barrier
     tc_fence_before();
     __syncthreads();
+    if (p.nslices == 2) cluster_sync_all();   // no DSMEM traffic into an exited peer
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -596,14 +723,22 @@ int launch_impl(const PrefillArgs &a, cudaStream_t stream) {
     p.nqt = (a.L + kBM - 1) / kBM;
     p.no_norm = (a.flags & GDA_FLAG_NO_NORM) ? 1 : 0;
 
-    auto kern = gda_prefill_tc_kernel<D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return record_cuda_error(e);
-    const long long grid = static_cast<long long>(p.nqt) * a.B * a.hs * p.nslices;
-    if (grid <= 0 || grid > 0x7fffffffLL) return GDA_ERR_UNSUPPORTED;
+    auto kern = gda_prefill_tc_kernel<D>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    const long long nitems = static_cast<long long>(p.nqt) * a.B * a.hs;
+    if (nitems <= 0 || nitems > 0x7fffffffLL) return GDA_ERR_UNSUPPORTED;
+    // one CTA (or CTA pair) per SM (pair of SMs), never more than there are items
+    long long groups = sms / p.nslices;
+    if (groups < 1) groups = 1;
+    if (groups > nitems) groups = nitems;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(groups * p.nslices), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = LY::TOTAL;
     cfg.stream = stream;
