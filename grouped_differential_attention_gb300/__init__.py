@@ -41,6 +41,7 @@ GDA_ERR_DEVICE_TIMEOUT = -6
 GDA_FLAG_NO_NORM = 0x1
 GDA_DEVERR_PREFILL_TIMEOUT = 0x1
 GDA_DEVERR_BAD_LENGTH = 0x2
+GDA_DEVERR_DECODE_TIMEOUT = 0x4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libgda.so")

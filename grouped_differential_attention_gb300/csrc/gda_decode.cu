@@ -10,23 +10,29 @@
 //
 // Memory-bound: per cached position a sequence reads its K1 row (h_s*d),
 // K2 row (h_n*d; each noise head read once for its whole group) and V row
-// (h_s*dv), all bf16.  One CTA handles one (sequence, split of `chunk`
-// positions) for ALL heads, so every position row is one contiguous,
-// fully coalesced sweep: thread t owns the t-th 16-byte chunk of the
-// concatenated [K1 | K2 | V] row and loads it with a 128-bit load for each
-// position (register double buffer: the next tile's loads are in flight
-// while the current tile is reduced).
+// (h_s*dv), all bf16.  The split kernel runs two CTAs per SM (one for very
+// wide rows); the batch's cache positions, concatenated sequence after
+// sequence, are cut into one equal contiguous range per CTA (stream-K), so
+// the load is even whatever the mix of lengths and no wave is left half
+// empty.  Each CTA streams its range through a ring of shared-memory stages
+// filled by 1-D bulk copies (TMA): the K1, K2 and V rows of consecutive
+// positions are contiguous in the cache, so a stage is three copies issued
+// by one thread, and up to 100 KB per CTA are in flight.  Every CTA handles
+// ALL heads of its positions; thread t owns the t-th 16-byte chunk of the
+// concatenated [K1 | K2 | V] position row and reads it from the stage:
 //   - K threads: partial dot product over 8 dims, warp-shuffle reduction over
 //     the d/8 threads of a head;
 //   - one thread per head (signal and noise): online softmax in exp2 units;
 //   - V threads: both accumulators O1, O2 for their 8 columns.
-// Partial (m, l) per head and (O1, O2) per signal head go to the workspace;
-// the combine kernel merges the splits and applies the difference and the
+// Each (CTA, sequence) segment leaves its partial (m, l) per head and
+// (O1, O2) per signal head in the workspace; the combine kernel merges a
+// sequence's segments and applies the difference and the
 // (1 - lambda_init) RMSNorm epilogue.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 #include <cmath>
+#include <algorithm>
 #include <mutex>
 
 #include "gda.h"
@@ -43,22 +49,17 @@ struct DecParams {
     const int *lens;
     const float *lambda;
     __nv_bfloat16 *out;
-    float *ws_o;       // [B][splits][hs][2][dv]
-    float *ws_ml;      // [B][splits][hs+hn][2]
+    float *ws_o;       // [slots][hs][2][dv]     slot = CTA + sequence
+    float *ws_ml;      // [slots][hs+hn][2]
+    int *ws_seg;       // [B][2]: first and last CTA holding a segment of the sequence
     unsigned *err;
     float lambda_init, eps, scale_log2;
-    int B, Lcap, hs, hn, d, dv, chunk, splits;
+    int B, Lcap, hs, hn, d, dv;
+    int min_per_cta;   // fewest positions a CTA takes
+    int ctas;          // CTAs of the split kernel
     int kc1, kc;       // chunk boundaries: K1 chunks [0,kc1), K2 [kc1,kc), V [kc, nchunks)
     int nchunks;
 };
-
-__device__ __forceinline__ uint4 ld_stream16(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 __device__ __forceinline__ int clamp_len(int len, int Lcap, unsigned *err) {
     if (len < 1 || len > Lcap) {
@@ -68,55 +69,229 @@ __device__ __forceinline__ int clamp_len(int len, int Lcap, unsigned *err) {
     return len;
 }
 
-// kTile positions per tile.  Narrow head sets (<= 384 chunks per row) run
-// 4-position tiles with two CTAs per SM; wide ones 2-position tiles with up
-// to 1024 threads, both without register spills.
-template <int D, int kTile, int kMaxThreads, int kMinBlocks>
-__global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
-gda_decode_split_kernel(const DecParams p) {
-    // scores, then weights; double-buffered by tile parity because the K
-    // threads write tile t+1's scores before the barrier that the V threads
-    // of tile t pass after reading tile t's weights
-    __shared__ float sc_buf[2][kMaxHeads][kTile];
-    __shared__ float alpha_s[kMaxHeads];
+constexpr int kMaxStages = 8;
 
-    const int split = blockIdx.x, b = blockIdx.y;
-    const int t = threadIdx.x;
-    const int len = clamp_len(p.lens[b], p.Lcap, p.err);
-    const int pos_begin = split * p.chunk;
-    if (pos_begin >= len) return;                 // uniform over the CTA
-    const int pos_end = min(len, pos_begin + p.chunk);
+// 1-D bulk copy (TMA) of `bytes` contiguous bytes into shared memory,
+// completing on `bar` as transaction bytes.  Both addresses 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ long long warp_incl_scan(long long x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+// Producer state (thread 0 of a CTA): a cursor over the CTA's range
+// [start, end) of the batch's concatenated cache positions.  b is the
+// current sequence, whose positions begin at `pre` in the concatenation;
+// pos is its next position and hi the end of its part of the range.
+struct Cursor {
+    long long pre, end, per;
+    int b, len, pos, hi, k;   // k: tiles issued so far
+    int cta;
+    bool done;
+};
+
+// What the consumers of a stage need to know about its tile.
+struct TileInfo {
+    int n;      // positions in the tile (1..P)
+    int b;      // sequence
+    int flags;  // kSegEnd: last tile of the CTA's segment of sequence b; kLast: last tile of the CTA
+};
+constexpr int kSegEnd = 1, kLast = 2;
+
+// A segment that starts at position 0 of sequence c.b records the first and
+// last CTA whose range meets the sequence (the combine kernel reads them).
+__device__ __forceinline__ void note_first_segment(const DecParams &p, const Cursor &c) {
+    if (c.pos != 0) return;
+    p.ws_seg[2 * c.b] = c.cta;
+    p.ws_seg[2 * c.b + 1] = static_cast<int>((c.pre + c.len - 1) / c.per);
+}
+
+// Issues the next tile of cursor c (if any) into stage c.k % stages: its
+// TileInfo, then the three bulk copies on the stage's barrier.
+template <int P>
+__device__ __forceinline__ void issue_tile(const DecParams &p, Cursor &c, int stages, uint8_t *ring,
+                                           uint64_t *full, TileInfo *info) {
+    if (c.done) return;
+    const uint32_t rk1 = p.hs * p.d * 2, rk2 = p.hn * p.d * 2, rv = p.hs * p.dv * 2;
+    const int n = min(P, c.hi - c.pos);
+    const int st = c.k % stages;
+    uint8_t *sb = ring + static_cast<size_t>(st) * P * (rk1 + rk2 + rv);
+    const size_t row0 = static_cast<size_t>(c.b) * p.Lcap + c.pos;
+    const int b = c.b;
+
+    // advance the cursor
+    int flags = 0;
+    c.pos += n;
+    if (c.pos >= c.hi) {
+        flags = kSegEnd;
+        if (c.pre + c.hi >= c.end) {
+            c.done = true;
+            flags |= kLast;
+        } else {
+            c.pre += c.len;
+            ++c.b;
+            c.len = clamp_len(p.lens[c.b], p.Lcap, p.err);
+            c.pos = 0;
+            c.hi = static_cast<int>(min(static_cast<long long>(c.len), c.end - c.pre));
+            note_first_segment(p, c);
+        }
+    }
+    info[st] = TileInfo{n, b, flags};
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // prior generic reads of the stage
+    mbar_arrive_expect_tx(&full[st], n * (rk1 + rk2 + rv));          // releases info[st]
+    bulk_copy_g2s(sb, p.k1c + row0 * (rk1 / 2), n * rk1, &full[st]);
+    bulk_copy_g2s(sb + P * rk1, p.k2c + row0 * (rk2 / 2), n * rk2, &full[st]);
+    bulk_copy_g2s(sb + P * (rk1 + rk2), p.vc + row0 * (rv / 2), n * rv, &full[st]);
+    ++c.k;
+}
+
+// Stream-K split of the cache: the batch's cache positions, concatenated
+// sequence after sequence, are cut into gridDim.x equal contiguous ranges,
+// one per CTA, so every CTA streams the same number of bytes whatever the
+// mix of lengths.  A range may span several sequences; the part of it in
+// one sequence is a segment, and each segment leaves one partial softmax
+// state in workspace slot (CTA + sequence) (unique: along the position axis
+// neither index decreases and at least one grows at each segment change).
+//
+// The positions stream through a ring of `stages` shared-memory stages of
+// P positions, filled by thread 0 with three bulk copies per stage (the K1,
+// K2 and V rows of P consecutive positions of one sequence, contiguous in
+// the cache); positions outside the range are never copied.  Thread t owns
+// the t-th 16-byte chunk of the concatenated [K1 | K2 | V] position row
+// and reads it from the stage.
+template <int D, int P, int kMaxThreads, int kMinBlocks>
+__global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
+gda_decode_split_kernel(const DecParams p, int stages) {
+    // scores, then weights; double-buffered by tile parity because the K
+    // threads write tile i+1's scores before the barrier that the V threads
+    // of tile i pass after reading tile i's weights
+    __shared__ float sc_buf[2][kMaxHeads][P];
+    __shared__ float alpha_s[kMaxHeads];
+    __shared__ uint64_t full[kMaxStages];
+    __shared__ TileInfo info[kMaxStages];
+    __shared__ long long red_s[32];
+    __shared__ long long found_pre;
+    __shared__ int found_b;
+    __shared__ int abort_flag;
+    __shared__ Cursor prod;
+    extern __shared__ __align__(128) uint8_t ring[];
+
+    const int cta = blockIdx.x;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = blockDim.x >> 5;
+
+    // ---- total positions of the batch, and this CTA's range
+    long long part = 0;
+    for (int b = t; b < p.B; b += blockDim.x) part += clamp_len(p.lens[b], p.Lcap, p.err);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) red_s[warp] = part;
+    if (t == 0) found_b = -1;
+    __syncthreads();
+    long long total = 0;
+    for (int w = 0; w < nwarps; ++w) total += red_s[w];
+    long long per = (total + gridDim.x - 1) / gridDim.x;
+    if (per < p.min_per_cta) per = p.min_per_cta;
+    const long long start = static_cast<long long>(cta) * per;
+    if (start >= total) return;                   // uniform over the CTA
+
+    // ---- the sequence holding position `start`: block-wide scan of the lengths
+    long long carry = 0;
+    for (int base = 0; base < p.B; base += blockDim.x) {
+        __syncthreads();                           // red_s reads of the previous pass are done
+        const int b = base + t;
+        const long long len = b < p.B ? clamp_len(p.lens[b], p.Lcap, p.err) : 0;
+        const long long incl = warp_incl_scan(len);
+        if (lane == 31) red_s[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            long long w = lane < nwarps ? red_s[lane] : 0;
+            w = warp_incl_scan(w);
+            if (lane < nwarps) red_s[lane] = w;
+        }
+        __syncthreads();
+        const long long before = carry + (warp > 0 ? red_s[warp - 1] : 0) + incl - len;
+        if (b < p.B && before <= start && start < before + len) {
+            found_b = b;
+            found_pre = before;
+        }
+        carry += red_s[nwarps - 1];
+        __syncthreads();
+        if (found_b >= 0) break;                   // uniform
+    }
+    if (found_b < 0) return;                       // unreachable while every length is >= 1
+
     const int nheads = p.hs + p.hn;
     constexpr int CPH = D / 8;                    // 16-byte chunks per head row of K
+    const uint32_t rk1 = p.hs * D * 2, rk2 = p.hn * D * 2, rv = p.hs * p.dv * 2;   // row bytes
+    const uint32_t stage_bytes = P * (rk1 + rk2 + rv);
+
+    // ---- producer (thread 0), stages-1 tiles ahead of the consumers
+    if (t == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        Cursor c;
+        c.pre = found_pre;
+        c.end = min(total, start + per);
+        c.per = per;
+        c.b = found_b;
+        c.len = clamp_len(p.lens[c.b], p.Lcap, p.err);
+        c.pos = static_cast<int>(start - c.pre);
+        c.hi = static_cast<int>(min(static_cast<long long>(c.len), c.end - c.pre));
+        c.k = 0;
+        c.cta = cta;
+        c.done = false;
+        note_first_segment(p, c);
+        for (int i = 0; i < stages - 1; ++i) issue_tile<P>(p, c, stages, ring, full, info);
+        prod = c;
+    }
+    const int b_first = found_b;
+    __syncthreads();
 
     // ---- role of this thread
     const bool is_k = t < p.kc;
     const bool is_v = t >= p.kc && t < p.nchunks;
-    const size_t row_k1 = static_cast<size_t>(p.hs) * D;
-    const size_t row_k2 = static_cast<size_t>(p.hn) * D;
-    const size_t row_v = static_cast<size_t>(p.hs) * p.dv;
-    const __nv_bfloat16 *base = nullptr;          // element address of this chunk at position 0
-    size_t stride = 0;                            // elements between positions
+    uint32_t off = 0, stride = 0;                 // byte offset of the chunk in a stage, row stride
     int sh = 0;                                   // score head of a K thread
     if (t < p.kc1) {
-        base = p.k1c + static_cast<size_t>(b) * p.Lcap * row_k1 + static_cast<size_t>(t) * 8;
-        stride = row_k1;
+        off = t * 16;
+        stride = rk1;
         sh = t / CPH;
     } else if (t < p.kc) {
-        base = p.k2c + static_cast<size_t>(b) * p.Lcap * row_k2 + static_cast<size_t>(t - p.kc1) * 8;
-        stride = row_k2;
+        off = P * rk1 + (t - p.kc1) * 16;
+        stride = rk2;
         sh = p.hs + (t - p.kc1) / CPH;
     } else if (is_v) {
-        base = p.vc + static_cast<size_t>(b) * p.Lcap * row_v + static_cast<size_t>(t - p.kc) * 8;
-        stride = row_v;
+        off = P * (rk1 + rk2) + (t - p.kc) * 16;
+        stride = rv;
     }
+    // V thread: signal head, its noise head and its 8 columns
+    const int vh = is_v ? (t - p.kc) / (p.dv / 8) : 0;
+    const int vg = vh / (p.hs / p.hn);
+    const int vcol = is_v ? (t - p.kc) % (p.dv / 8) * 8 : 0;
 
-    // query chunk of a K thread, pre-scaled into exp2 units
+    // query chunk of a K thread for sequence b, pre-scaled into exp2 units
     float q[8];
-    if (is_k) {
+    auto load_q = [&](int b) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = 0.f;
+        if (!is_k) return;
         const __nv_bfloat16 *qp = (t < p.kc1)
-            ? p.q1 + static_cast<size_t>(b) * row_k1 + static_cast<size_t>(t) * 8
-            : p.q2 + static_cast<size_t>(b) * row_k2 + static_cast<size_t>(t - p.kc1) * 8;
+            ? p.q1 + static_cast<size_t>(b) * p.hs * D + static_cast<size_t>(t) * 8
+            : p.q2 + static_cast<size_t>(b) * p.hn * D + static_cast<size_t>(t - p.kc1) * 8;
         const uint4 qv = *reinterpret_cast<const uint4 *>(qp);
         const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
@@ -124,37 +299,34 @@ gda_decode_split_kernel(const DecParams p) {
             q[2 * i] = bf16_lo(w[i]) * p.scale_log2;
             q[2 * i + 1] = bf16_hi(w[i]) * p.scale_log2;
         }
-    }
+    };
+    load_q(b_first);
 
-    // V thread: signal head and its noise head
-    const int vh = is_v ? (t - p.kc) / (p.dv / 8) : 0;
-    const int vg = vh / (p.hs / p.hn);
     float o1[8], o2[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o1[i] = o2[i] = 0.f;
     // softmax state of head t (threads t < nheads)
     float m_run = -INFINITY, l_run = 0.f;
 
-    auto load_tile = [&](uint4 (&buf)[kTile], int pos0) {
-        if (is_k || is_v) {
-#pragma unroll
-            for (int i = 0; i < kTile; ++i) {
-                const int pos = min(pos0 + i, pos_end - 1);   // stay inside the sequence
-                buf[i] = ld_stream16(base + static_cast<size_t>(pos) * stride);
-            }
-        }
-    };
-
-    auto process_tile = [&](const uint4 (&buf)[kTile], int pos0, int par) {
-        float (*sc)[kTile] = sc_buf[par];
+    for (int it = 0;; ++it) {
+        const int st = it % stages;
+        const uint8_t *sb = ring + static_cast<size_t>(st) * stage_bytes + off;
+        float (*sc)[P] = sc_buf[it & 1];
+        // a wait that runs out leaves this CTA's result undefined, but every
+        // thread still takes every barrier below (and the tile's info,
+        // written before the barrier's arrive, is valid either way)
+        mbar_wait(&full[st], (it / stages) & 1, p.err, GDA_DEVERR_DECODE_TIMEOUT, &abort_flag);
+        const TileInfo ti = info[st];
+        const int n = ti.n;
         // Every lane of the warp takes part in the shuffles (a warp may hold
         // both K and V chunks); head groups of CPH lanes are CPH-aligned and
         // the K/V boundary is a multiple of CPH, so sums never mix roles.
 #pragma unroll
-        for (int i = 0; i < kTile; ++i) {
+        for (int i = 0; i < P; ++i) {
             float s = 0.f;
-            if (is_k) {
-                const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+            if (is_k && i < n) {
+                const uint4 kv = *reinterpret_cast<const uint4 *>(sb + i * stride);
+                const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     s = fmaf(q[2 * e], bf16_lo(w[e]), s);
@@ -163,18 +335,20 @@ gda_decode_split_kernel(const DecParams p) {
             }
 #pragma unroll
             for (int o = CPH / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (is_k && (t % CPH) == 0) sc[sh][i] = (pos0 + i < pos_end) ? s : -INFINITY;
+            if (is_k && (t % CPH) == 0) sc[sh][i] = (i < n) ? s : -INFINITY;
         }
         __syncthreads();
+        // the stage read in the previous tile is free: refill it
+        if (t == 0) issue_tile<P>(p, prod, stages, ring, full, info);
         if (t < nheads) {
             float mt = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) mt = fmaxf(mt, sc[t][i]);
-            const float mn = fmaxf(m_run, mt);          // finite: position pos0 is valid
+            for (int i = 0; i < P; ++i) mt = fmaxf(mt, sc[t][i]);
+            const float mn = fmaxf(m_run, mt);          // finite: the tile holds >= 1 position
             const float a = fast_exp2(m_run - mn);      // m_run = -inf gives 0
             float sum = 0.f;
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) {
+            for (int i = 0; i < P; ++i) {
                 const float w = fast_exp2(sc[t][i] - mn);
                 sc[t][i] = w;
                 sum += w;
@@ -192,9 +366,11 @@ gda_decode_split_kernel(const DecParams p) {
                 o2[e] *= a2;
             }
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) {
+            for (int i = 0; i < P; ++i) {
+                if (i >= n) break;                      // rows outside the range were never copied
                 const float w1 = sc[vh][i], w2 = sc[p.hs + vg][i];
-                const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+                const uint4 vv = *reinterpret_cast<const uint4 *>(sb + i * stride);
+                const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float v0 = bf16_lo(w[e]), v1 = bf16_hi(w[e]);
@@ -205,63 +381,60 @@ gda_decode_split_kernel(const DecParams p) {
                 }
             }
         }
-        // alpha_s is rewritten only after the next tile's first barrier, which
-        // every V thread reaches after its reads above
-    };
+        // alpha_s, info[st] and this stage are rewritten only after the next
+        // tile's first barrier, which every V thread reaches after its reads
 
-    const int ntiles = (pos_end - pos_begin + kTile - 1) / kTile;
-    uint4 bufA[kTile], bufB[kTile];
-    load_tile(bufA, pos_begin);
-    for (int tile = 0; tile < ntiles; tile += 2) {
-        const int pa = pos_begin + tile * kTile;
-        if (tile + 1 < ntiles) load_tile(bufB, pa + kTile);
-        process_tile(bufA, pa, 0);
-        if (tile + 1 >= ntiles) break;
-        if (tile + 2 < ntiles) load_tile(bufA, pa + 2 * kTile);
-        process_tile(bufB, pa + kTile, 1);
-    }
-
-    // ---- partial state of this split
-    const size_t bs = static_cast<size_t>(b) * p.splits + split;
-    if (t < nheads) {
-        p.ws_ml[(bs * nheads + t) * 2 + 0] = m_run;
-        p.ws_ml[(bs * nheads + t) * 2 + 1] = l_run;
-    }
-    if (is_v) {
-        const int col = (t - p.kc) % (p.dv / 8) * 8;
-        float *dst = p.ws_o + ((bs * p.hs + vh) * 2) * p.dv + col;
-        reinterpret_cast<float4 *>(dst)[0] = make_float4(o1[0], o1[1], o1[2], o1[3]);
-        reinterpret_cast<float4 *>(dst)[1] = make_float4(o1[4], o1[5], o1[6], o1[7]);
-        reinterpret_cast<float4 *>(dst + p.dv)[0] = make_float4(o2[0], o2[1], o2[2], o2[3]);
-        reinterpret_cast<float4 *>(dst + p.dv)[1] = make_float4(o2[4], o2[5], o2[6], o2[7]);
+        if (ti.flags & kSegEnd) {
+            // end of a segment: its partial state goes to slot (CTA + sequence)
+            const size_t slot = static_cast<size_t>(cta) + ti.b;
+            if (t < nheads) {
+                p.ws_ml[(slot * nheads + t) * 2 + 0] = m_run;
+                p.ws_ml[(slot * nheads + t) * 2 + 1] = l_run;
+            }
+            if (is_v) {
+                float *dst = p.ws_o + ((slot * p.hs + vh) * 2) * p.dv + vcol;
+                reinterpret_cast<float4 *>(dst)[0] = make_float4(o1[0], o1[1], o1[2], o1[3]);
+                reinterpret_cast<float4 *>(dst)[1] = make_float4(o1[4], o1[5], o1[6], o1[7]);
+                reinterpret_cast<float4 *>(dst + p.dv)[0] = make_float4(o2[0], o2[1], o2[2], o2[3]);
+                reinterpret_cast<float4 *>(dst + p.dv)[1] = make_float4(o2[4], o2[5], o2[6], o2[7]);
+            }
+            if (ti.flags & kLast) break;
+            m_run = -INFINITY;
+            l_run = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o1[i] = o2[i] = 0.f;
+            load_q(ti.b + 1);                           // segments follow the sequences in order
+        }
     }
 }
 
-// grid (h_s, B), block dv threads: merge the splits of one (sequence, head).
+// grid (h_s, B), block dv threads: merge the segments of one (sequence, head).
 __global__ void __launch_bounds__(256)
 gda_decode_combine_kernel(const DecParams p) {
     __shared__ float red[8];
     const int h = blockIdx.x, b = blockIdx.y, col = threadIdx.x;
     const int g = h / (p.hs / p.hn);
     const int nheads = p.hs + p.hn;
-    int len = p.lens[b];
-    len = len < 1 ? 1 : (len > p.Lcap ? p.Lcap : len);
-    const int ns = (len + p.chunk - 1) / p.chunk;
-    const size_t b0 = static_cast<size_t>(b) * p.splits;
+    // CTAs c0..c1 left a segment of this sequence in slots c + b (clamped so
+    // that a damaged workspace cannot send the reads out of bounds)
+    const int c0 = min(max(p.ws_seg[2 * b], 0), p.ctas - 1);
+    const int c1 = min(max(p.ws_seg[2 * b + 1], c0), p.ctas - 1);
 
     float M1 = -INFINITY, M2 = -INFINITY;
-    for (int s = 0; s < ns; ++s) {
-        M1 = fmaxf(M1, p.ws_ml[((b0 + s) * nheads + h) * 2]);
-        M2 = fmaxf(M2, p.ws_ml[((b0 + s) * nheads + p.hs + g) * 2]);
+    for (int c = c0; c <= c1; ++c) {
+        const size_t slot = static_cast<size_t>(c) + b;
+        M1 = fmaxf(M1, p.ws_ml[(slot * nheads + h) * 2]);
+        M2 = fmaxf(M2, p.ws_ml[(slot * nheads + p.hs + g) * 2]);
     }
     float L1 = 0.f, L2 = 0.f, O1 = 0.f, O2 = 0.f;
-    for (int s = 0; s < ns; ++s) {
-        const float *ml1 = p.ws_ml + ((b0 + s) * nheads + h) * 2;
-        const float *ml2 = p.ws_ml + ((b0 + s) * nheads + p.hs + g) * 2;
+    for (int c = c0; c <= c1; ++c) {
+        const size_t slot = static_cast<size_t>(c) + b;
+        const float *ml1 = p.ws_ml + (slot * nheads + h) * 2;
+        const float *ml2 = p.ws_ml + (slot * nheads + p.hs + g) * 2;
         const float f1 = fast_exp2(ml1[0] - M1), f2 = fast_exp2(ml2[0] - M2);
         L1 = fmaf(ml1[1], f1, L1);
         L2 = fmaf(ml2[1], f2, L2);
-        const float *os = p.ws_o + (((b0 + s) * p.hs + h) * 2) * p.dv;
+        const float *os = p.ws_o + ((slot * p.hs + h) * 2) * p.dv;
         O1 = fmaf(os[col], f1, O1);
         O2 = fmaf(os[p.dv + col], f2, O2);
     }
@@ -277,21 +450,30 @@ gda_decode_combine_kernel(const DecParams p) {
     p.out[(static_cast<size_t>(b) * p.hs + h) * p.dv + col] = __float2bfloat16_rn(y);
 }
 
+template <int D, int P>
+cudaError_t launch_split(dim3 grid, int threads, size_t smem, cudaStream_t stream, const DecParams &p, int stages) {
+    // up to 384 threads: two CTAs per SM with up to 80 registers a thread;
+    // else at most 64 registers (two CTAs of up to 512 threads, or one)
+    auto kern = threads <= 384 ? gda_decode_split_kernel<D, P, 384, 2> : gda_decode_split_kernel<D, P, 1024, 1>;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, threads, smem, stream>>>(p, stages);
+    return cudaSuccess;
+}
+
 }  // namespace
 
+// Upper bound on the split kernel's CTAs (two per SM on a 152-SM part); the
+// workspace holds one partial state per (CTA + sequence) slot.
+constexpr int kDecodeMaxCtas = 304;
+
 DecodePlan decode_plan(int B, int Lcap, int hs, int hn, int dv) {
+    (void)Lcap;
     DecodePlan pl;
-    // 256 positions per CTA keeps >= a few waves of CTAs at serving batch
-    // sizes; short caches get smaller chunks so every SM has work.
-    int chunk = 256;
-    while (chunk > 32 && static_cast<long long>(B) * ((Lcap + chunk - 1) / chunk) < 4 * 152) chunk /= 2;
-    pl.chunk = chunk;
-    pl.splits = (Lcap + chunk - 1) / chunk;
-    const size_t nb = static_cast<size_t>(B) * pl.splits;
-    size_t o_bytes = nb * hs * 2 * static_cast<size_t>(dv) * sizeof(float);
-    o_bytes = (o_bytes + 255) / 256 * 256;
-    const size_t ml_bytes = nb * (hs + hn) * 2 * sizeof(float);
-    pl.bytes = o_bytes + ml_bytes;
+    pl.slots = kDecodeMaxCtas + B;
+    pl.o_bytes = (static_cast<size_t>(pl.slots) * hs * 2 * dv * sizeof(float) + 255) / 256 * 256;
+    pl.ml_bytes = (static_cast<size_t>(pl.slots) * (hs + hn) * 2 * sizeof(float) + 255) / 256 * 256;
+    pl.bytes = pl.o_bytes + pl.ml_bytes + static_cast<size_t>(B) * 2 * sizeof(int);
     return pl;
 }
 
@@ -307,10 +489,9 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     p.lens = a.lens;
     p.lambda = a.lambda;
     p.out = static_cast<__nv_bfloat16 *>(a.out);
-    size_t o_bytes = static_cast<size_t>(a.B) * pl.splits * a.hs * 2 * static_cast<size_t>(a.dv) * sizeof(float);
-    o_bytes = (o_bytes + 255) / 256 * 256;
     p.ws_o = static_cast<float *>(a.workspace);
-    p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(a.workspace) + o_bytes);
+    p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(a.workspace) + pl.o_bytes);
+    p.ws_seg = reinterpret_cast<int *>(static_cast<char *>(a.workspace) + pl.o_bytes + pl.ml_bytes);
     p.err = a.dev_err;
     p.lambda_init = a.lambda_init;
     p.eps = a.eps;
@@ -321,8 +502,6 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     p.hn = a.hn;
     p.d = a.d;
     p.dv = a.dv;
-    p.chunk = pl.chunk;
-    p.splits = pl.splits;
     p.kc1 = a.hs * a.d / 8;
     p.kc = (a.hs + a.hn) * a.d / 8;
     p.nchunks = p.kc + a.hs * a.dv / 8;
@@ -330,18 +509,38 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     if (threads > 1024 || a.hs + a.hn > kMaxHeads) return GDA_ERR_UNSUPPORTED;
     if (a.B > 65535) return GDA_ERR_UNSUPPORTED;
 
-    dim3 grid(pl.splits, a.B);
-    const bool narrow = threads <= 384;
-    if (a.d == 64 && narrow)
-        gda_decode_split_kernel<64, 4, 384, 2><<<grid, threads, 0, stream>>>(p);
-    else if (a.d == 64)
-        gda_decode_split_kernel<64, 2, 1024, 1><<<grid, threads, 0, stream>>>(p);
-    else if (a.d == 128 && narrow)
-        gda_decode_split_kernel<128, 4, 384, 2><<<grid, threads, 0, stream>>>(p);
-    else if (a.d == 128)
-        gda_decode_split_kernel<128, 2, 1024, 1><<<grid, threads, 0, stream>>>(p);
-    else
-        return GDA_ERR_UNSUPPORTED;
+    // every copy in flight completes within the CTA's range (no position
+    // outside it is copied), so the CTA can exit after its last tile
+    const size_t row_bytes = 2 * (static_cast<size_t>(a.hs) * a.d + static_cast<size_t>(a.hn) * a.d +
+                                  static_cast<size_t>(a.hs) * a.dv);
+    // ring budget: two CTAs per SM (with their static arrays) fit in 228 KB
+    // when a CTA has at most 512 threads, else one; the largest stage of
+    // 8, 4 or 2 positions of which at least four fit
+    const size_t budget = threads <= 512 ? 100 * 1024 : 200 * 1024;
+    int P = 8;
+    while (P > 2 && row_bytes * P * 4 > budget) P /= 2;
+    int stages = static_cast<int>(budget / (row_bytes * P));
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) return GDA_ERR_UNSUPPORTED;
+    const size_t smem = static_cast<size_t>(stages) * P * row_bytes;
+    int dev = 0, sms = 0;
+    cudaError_t e1 = cudaGetDevice(&dev);
+    if (e1 == cudaSuccess) e1 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e1 != cudaSuccess) return record_cuda_error(e1);
+    p.ctas = std::min(kDecodeMaxCtas, (threads <= 512 ? 2 : 1) * sms);
+    p.min_per_cta = 64;
+    const dim3 grid(p.ctas);
+    cudaError_t e0;
+    switch (a.d * 16 + P) {
+        case 64 * 16 + 8: e0 = launch_split<64, 8>(grid, threads, smem, stream, p, stages); break;
+        case 64 * 16 + 4: e0 = launch_split<64, 4>(grid, threads, smem, stream, p, stages); break;
+        case 64 * 16 + 2: e0 = launch_split<64, 2>(grid, threads, smem, stream, p, stages); break;
+        case 128 * 16 + 8: e0 = launch_split<128, 8>(grid, threads, smem, stream, p, stages); break;
+        case 128 * 16 + 4: e0 = launch_split<128, 4>(grid, threads, smem, stream, p, stages); break;
+        case 128 * 16 + 2: e0 = launch_split<128, 2>(grid, threads, smem, stream, p, stages); break;
+        default: return GDA_ERR_UNSUPPORTED;
+    }
+    if (e0 != cudaSuccess) return record_cuda_error(e0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return record_cuda_error(e);
     gda_decode_combine_kernel<<<dim3(a.hs, a.B), a.dv, 0, stream>>>(p);

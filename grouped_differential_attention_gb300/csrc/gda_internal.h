@@ -50,8 +50,9 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream);
 
 // Split plan of the decode kernel (positions per split and split count).
 struct DecodePlan {
-    int chunk;        // cache positions handled by one CTA
-    int splits;       // ceil(Lcap / chunk)
+    int slots;        // partial-state slots (split CTAs + sequences)
+    size_t o_bytes;   // accumulator partials
+    size_t ml_bytes;  // (max, sum) partials
     size_t bytes;     // workspace bytes
 };
 DecodePlan decode_plan(int B, int Lcap, int hs, int hn, int dv);

@@ -112,7 +112,9 @@ int gda_attn_fwd_f32_ex(const float *q_sig, const float *k_sig, const float *q_n
 
 /*
  * Bytes of device workspace gda_attn_decode needs for these sizes (it holds
- * the per-split partial softmax states).  Returns 0 for invalid sizes.
+ * the partial softmax states of the cache segments that the split kernel's
+ * CTAs produce; the size does not depend on Lcap).  Returns 0 for invalid
+ * sizes.
  */
 size_t gda_attn_decode_workspace_size(int B, int Lcap, int h_s, int h_n, int dv);
 
@@ -134,7 +136,9 @@ size_t gda_attn_decode_workspace_size(int B, int Lcap, int h_s, int h_n, int dv)
  *   reported through gda_device_error (GDA_DEVERR_BAD_LENGTH).
  *   Supported: d in {64, 128}; dv in {64, 128, 256};
  *   (h_s*d + h_n*d + h_s*dv) / 8 <= 1024.
- * Split-KV kernel with 16-byte coalesced cache loads plus a combine kernel.
+ * Split kernel (the batch's cache positions cut into equal contiguous ranges,
+ * one per CTA, streamed through shared memory by bulk copies) plus a
+ * combine kernel.
  */
 int gda_attn_decode(const void *q_sig, const void *q_noise, const void *k_sig_cache,
                     const void *k_noise_cache, const void *v_cache, const int *cache_lens,
@@ -153,8 +157,9 @@ int gda_attn_decode(const void *q_sig, const void *q_noise, const void *k_sig_ca
  *   GDA_DECODE_SCRATCH_BYTES (32 MiB) per device, held by every device that
  *   loads the library until the process exits.
  *   Returns GDA_ERR_WORKSPACE if gda_attn_decode_workspace_size(B, Lcap, h_s,
- *   h_n, dv) exceeds GDA_DECODE_SCRATCH_BYTES (e.g. 64 sequences of up to
- *   8192 cached positions with 12 + 4 heads and dv = 128 need about 25 MB).
+ *   h_n, dv) exceeds GDA_DECODE_SCRATCH_BYTES (e.g. 64 sequences with
+ *   12 + 4 heads and dv = 128 need about 4.6 MB whatever their lengths;
+ *   more than about 2400 such sequences do not fit).
  *   The first call on a device looks up the scratch array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
  *   before any stream capture.
@@ -181,6 +186,7 @@ int gda_last_cuda_error(void);
 /* Bits of the device error word. */
 #define GDA_DEVERR_PREFILL_TIMEOUT 0x1u  /* a prefill pipeline wait ran out */
 #define GDA_DEVERR_BAD_LENGTH      0x2u  /* a decode cache length was outside [1, Lcap] */
+#define GDA_DEVERR_DECODE_TIMEOUT  0x4u  /* a decode cache-streaming wait ran out */
 
 /*
  * Reads the error word of the current device (synchronises the device

@@ -109,8 +109,11 @@ def decode(lib, ws_bytes=None, ws=A, B=4, Lcap=256, hs=6, hn=2, d=64, dv=128, pt
 
 def test_decode_workspace_size(lib):
     n = lib.gda_attn_decode_workspace_size(64, 8192, 12, 4, 128)
-    # per split: 12 heads x 2 accumulators x 128 floats, plus (m, l) for 16 heads
+    # one slot per sequence at least: 12 heads x 2 accumulators x 128 floats,
+    # plus (m, l) for 16 heads
     assert n >= 64 * (12 * 2 * 128 + 16 * 2) * 4
+    # the slots do not depend on the cache length
+    assert lib.gda_attn_decode_workspace_size(64, 128, 12, 4, 128) == n
     assert n % 16 == 0
     assert lib.gda_attn_decode_workspace_size(0, 8192, 12, 4, 128) == 0
     assert lib.gda_attn_decode_workspace_size(64, 8192, 12, 5, 128) == 0

@@ -52,7 +52,7 @@ def test_no_alloc_decode_matches_workspace_decode():
 
 def test_no_alloc_decode_refuses_sizes_beyond_its_scratch():
     lib = gda._load()
-    B, Lcap, hs, hn, dv = 256, 16384, 12, 4, 128
+    B, Lcap, hs, hn, dv = 4096, 16384, 12, 4, 128   # partials of ~4400 segment slots
     assert gda.gda_attn_decode_workspace_size(B, Lcap, hs, hn, dv) > SCRATCH_BYTES
     A = ctypes.c_void_p(0x10000)   # never dereferenced: the size check comes first
     rc = lib.gda_attn_decode_noalloc(A, A, A, A, A, A, A, ctypes.c_float(0.8), A, B, Lcap, hs, hn,
