@@ -158,6 +158,28 @@ __device__ __forceinline__ void issue_tile(const DecParams &p, Cursor &c, int st
     ++c.k;
 }
 
+// P consecutive floats from shared memory (16-byte aligned for P >= 4, 8-byte for P = 2).
+template <int P>
+__device__ __forceinline__ void load_weights(float (&w)[P], const float *src) {
+    if constexpr (P % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < P; i += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(src + i);
+            w[i] = x.x;
+            w[i + 1] = x.y;
+            w[i + 2] = x.z;
+            w[i + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < P; i += 2) {
+            const float2 x = *reinterpret_cast<const float2 *>(src + i);
+            w[i] = x.x;
+            w[i + 1] = x.y;
+        }
+    }
+}
+
 // Stream-K split of the cache: the batch's cache positions, concatenated
 // sequence after sequence, are cut into gridDim.x equal contiguous ranges,
 // one per CTA, so every CTA streams the same number of bytes whatever the
@@ -166,27 +188,33 @@ __device__ __forceinline__ void issue_tile(const DecParams &p, Cursor &c, int st
 // state in workspace slot (CTA + sequence) (unique: along the position axis
 // neither index decreases and at least one grows at each segment change).
 //
-// The positions stream through a ring of `stages` shared-memory stages of
-// P positions, filled by thread 0 with three bulk copies per stage (the K1,
-// K2 and V rows of P consecutive positions of one sequence, contiguous in
-// the cache); positions outside the range are never copied.  Thread t owns
-// the t-th 16-byte chunk of the concatenated [K1 | K2 | V] position row
-// and reads it from the stage.
+// Warp roles, decoupled by mbarriers (no CTA-wide barrier per tile):
+//   - warp 0, one thread: producer.  Streams the range through a ring of
+//     `stages` shared-memory stages of P positions: per stage its TileInfo
+//     and three bulk copies (the K1, K2 and V rows of P consecutive
+//     positions of one sequence, contiguous in the cache).  Positions
+//     outside the range are never copied.
+//   - K warps: thread (32 + c) owns the c-th 16-byte chunk of the
+//     concatenated [K1 | K2] row: 8-dim partial dot products, reduced over
+//     the head's d/8 lanes by shuffles, after which every lane of the head
+//     holds the head's P scores and runs the head's online softmax
+//     (exp2 units) redundantly; the head's weights and rescale factor go to
+//     the stage's weight slot, then the warp arrives on wready[stage].
+//   - V warps (from the next warp boundary): one 16-byte chunk of the V row
+//     each; wait for wready, rescale and accumulate O1 (signal weights) and
+//     O2 (weights of the head's noise head) for 8 columns, arrive on
+//     empty[stage], which hands the stage back to the producer.
+// Shared memory (dynamic): ring [stages][P rows of K1 | P rows of K2 |
+// P rows of V], weights [stages][h_s + h_n][P], rescale [stages][h_s + h_n].
 template <int D, int P, int kMaxThreads, int kMinBlocks>
 __global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
 gda_decode_split_kernel(const DecParams p, int stages) {
-    // scores, then weights; double-buffered by tile parity because the K
-    // threads write tile i+1's scores before the barrier that the V threads
-    // of tile i pass after reading tile i's weights
-    __shared__ float sc_buf[2][kMaxHeads][P];
-    __shared__ float alpha_s[kMaxHeads];
-    __shared__ uint64_t full[kMaxStages];
+    __shared__ uint64_t full[kMaxStages], wready[kMaxStages], empty[kMaxStages];
     __shared__ TileInfo info[kMaxStages];
     __shared__ long long red_s[32];
     __shared__ long long found_pre;
     __shared__ int found_b;
     __shared__ int abort_flag;
-    __shared__ Cursor prod;
     extern __shared__ __align__(128) uint8_t ring[];
 
     const int cta = blockIdx.x;
@@ -234,20 +262,34 @@ gda_decode_split_kernel(const DecParams p, int stages) {
     if (found_b < 0) return;                       // unreachable while every length is >= 1
 
     const int nheads = p.hs + p.hn;
-    constexpr int CPH = D / 8;                    // 16-byte chunks per head row of K
+    const int n_kwarps = (p.kc + 31) / 32;
+    const int vbase = 32 + n_kwarps * 32;          // first V thread
+    const int n_vwarps = (p.nchunks - p.kc + 31) / 32;
     const uint32_t rk1 = p.hs * D * 2, rk2 = p.hn * D * 2, rv = p.hs * p.dv * 2;   // row bytes
     const uint32_t stage_bytes = P * (rk1 + rk2 + rv);
+    float *wts = reinterpret_cast<float *>(ring + static_cast<size_t>(stages) * stage_bytes);  // [stages][nheads][P]
+    float *alph = wts + stages * nheads * P;                                                    // [stages][nheads]
 
-    // ---- producer (thread 0), stages-1 tiles ahead of the consumers
     if (t == 0) {
-        for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&wready[s], n_kwarps);
+            mbar_init(&empty[s], n_vwarps);
+        }
         abort_flag = 0;
         fence_mbar_init();
+    }
+    const int b_first = found_b;
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer
+        if (lane != 0) return;
         Cursor c;
         c.pre = found_pre;
         c.end = min(total, start + per);
         c.per = per;
-        c.b = found_b;
+        c.b = b_first;
         c.len = clamp_len(p.lens[c.b], p.Lcap, p.err);
         c.pos = static_cast<int>(start - c.pre);
         c.hi = static_cast<int>(min(static_cast<long long>(c.len), c.end - c.pre));
@@ -255,155 +297,177 @@ gda_decode_split_kernel(const DecParams p, int stages) {
         c.cta = cta;
         c.done = false;
         note_first_segment(p, c);
-        for (int i = 0; i < stages - 1; ++i) issue_tile<P>(p, c, stages, ring, full, info);
-        prod = c;
-    }
-    const int b_first = found_b;
-    __syncthreads();
-
-    // ---- role of this thread
-    const bool is_k = t < p.kc;
-    const bool is_v = t >= p.kc && t < p.nchunks;
-    uint32_t off = 0, stride = 0;                 // byte offset of the chunk in a stage, row stride
-    int sh = 0;                                   // score head of a K thread
-    if (t < p.kc1) {
-        off = t * 16;
-        stride = rk1;
-        sh = t / CPH;
-    } else if (t < p.kc) {
-        off = P * rk1 + (t - p.kc1) * 16;
-        stride = rk2;
-        sh = p.hs + (t - p.kc1) / CPH;
-    } else if (is_v) {
-        off = P * (rk1 + rk2) + (t - p.kc) * 16;
-        stride = rv;
-    }
-    // V thread: signal head, its noise head and its 8 columns
-    const int vh = is_v ? (t - p.kc) / (p.dv / 8) : 0;
-    const int vg = vh / (p.hs / p.hn);
-    const int vcol = is_v ? (t - p.kc) % (p.dv / 8) * 8 : 0;
-
-    // query chunk of a K thread for sequence b, pre-scaled into exp2 units
-    float q[8];
-    auto load_q = [&](int b) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = 0.f;
-        if (!is_k) return;
-        const __nv_bfloat16 *qp = (t < p.kc1)
-            ? p.q1 + static_cast<size_t>(b) * p.hs * D + static_cast<size_t>(t) * 8
-            : p.q2 + static_cast<size_t>(b) * p.hn * D + static_cast<size_t>(t - p.kc1) * 8;
-        const uint4 qv = *reinterpret_cast<const uint4 *>(qp);
-        const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            q[2 * i] = bf16_lo(w[i]) * p.scale_log2;
-            q[2 * i + 1] = bf16_hi(w[i]) * p.scale_log2;
+        while (!c.done) {
+            if (c.k >= stages &&
+                !mbar_wait(&empty[c.k % stages], ((c.k / stages) - 1) & 1, p.err, GDA_DEVERR_DECODE_TIMEOUT,
+                           &abort_flag))
+                return;
+            issue_tile<P>(p, c, stages, ring, full, info);
         }
-    };
-    load_q(b_first);
+        return;
+    }
 
-    float o1[8], o2[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o1[i] = o2[i] = 0.f;
-    // softmax state of head t (threads t < nheads)
-    float m_run = -INFINITY, l_run = 0.f;
+    if (t < vbase) {
+        // ------------------------------------------------------ K warps
+        constexpr int CPH = D / 8;                 // lanes (16-byte chunks) per head row of K
+        const int kk = t - 32;                     // chunk index in [K1 | K2]
+        const bool is_k = kk < p.kc;
+        uint32_t off = 0, stride = 0;
+        int sh = 0;                                // score head
+        if (kk < p.kc1) {
+            off = kk * 16;
+            stride = rk1;
+            sh = kk / CPH;
+        } else if (is_k) {
+            off = P * rk1 + (kk - p.kc1) * 16;
+            stride = rk2;
+            sh = p.hs + (kk - p.kc1) / CPH;
+        }
+        const int gl = kk % CPH;                   // lane within the head's group
 
-    for (int it = 0;; ++it) {
-        const int st = it % stages;
-        const uint8_t *sb = ring + static_cast<size_t>(st) * stage_bytes + off;
-        float (*sc)[P] = sc_buf[it & 1];
-        // a wait that runs out leaves this CTA's result undefined, but every
-        // thread still takes every barrier below (and the tile's info,
-        // written before the barrier's arrive, is valid either way)
-        mbar_wait(&full[st], (it / stages) & 1, p.err, GDA_DEVERR_DECODE_TIMEOUT, &abort_flag);
-        const TileInfo ti = info[st];
-        const int n = ti.n;
-        // Every lane of the warp takes part in the shuffles (a warp may hold
-        // both K and V chunks); head groups of CPH lanes are CPH-aligned and
-        // the K/V boundary is a multiple of CPH, so sums never mix roles.
+        float q[8];
+        auto load_q = [&](int b) {
 #pragma unroll
-        for (int i = 0; i < P; ++i) {
-            float s = 0.f;
-            if (is_k && i < n) {
-                const uint4 kv = *reinterpret_cast<const uint4 *>(sb + i * stride);
-                const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+            for (int i = 0; i < 8; ++i) q[i] = 0.f;
+            if (!is_k) return;
+            const __nv_bfloat16 *qp = (kk < p.kc1)
+                ? p.q1 + static_cast<size_t>(b) * p.hs * D + static_cast<size_t>(kk) * 8
+                : p.q2 + static_cast<size_t>(b) * p.hn * D + static_cast<size_t>(kk - p.kc1) * 8;
+            const uint4 qv = *reinterpret_cast<const uint4 *>(qp);
+            const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    s = fmaf(q[2 * e], bf16_lo(w[e]), s);
-                    s = fmaf(q[2 * e + 1], bf16_hi(w[e]), s);
-                }
+            for (int i = 0; i < 4; ++i) {
+                q[2 * i] = bf16_lo(w[i]) * p.scale_log2;
+                q[2 * i + 1] = bf16_hi(w[i]) * p.scale_log2;
             }
+        };
+        load_q(b_first);
+        float m_run = -INFINITY, l_run = 0.f;     // softmax state of head sh
+
+        for (int it = 0;; ++it) {
+            const int st = it % stages;
+            // warp-uniform outcome: the shuffles below need every lane
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&full[st], (it / stages) & 1, p.err, GDA_DEVERR_DECODE_TIMEOUT, &abort_flag)))
+                return;
+            const TileInfo ti = info[st];
+            const uint8_t *sb = ring + static_cast<size_t>(st) * stage_bytes + off;
+            float s[P];
 #pragma unroll
-            for (int o = CPH / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (is_k && (t % CPH) == 0) sc[sh][i] = (i < n) ? s : -INFINITY;
-        }
-        __syncthreads();
-        // the stage read in the previous tile is free: refill it
-        if (t == 0) issue_tile<P>(p, prod, stages, ring, full, info);
-        if (t < nheads) {
-            float mt = -INFINITY;
+            for (int i = 0; i < P; ++i) {
+                float a0 = 0.f, a1 = 0.f;
+                if (is_k && i < ti.n) {
+                    const uint4 kv = *reinterpret_cast<const uint4 *>(sb + i * stride);
+                    const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-            for (int i = 0; i < P; ++i) mt = fmaxf(mt, sc[t][i]);
-            const float mn = fmaxf(m_run, mt);          // finite: the tile holds >= 1 position
-            const float a = fast_exp2(m_run - mn);      // m_run = -inf gives 0
+                    for (int e = 0; e < 4; ++e)
+                        ffma2_acc(a0, a1, q[2 * e], q[2 * e + 1], bf16_lo(w[e]), bf16_hi(w[e]));
+                }
+                s[i] = a0 + a1;
+            }
+            // head sums over the CPH lanes of each head (CPH-aligned groups;
+            // lanes past the K chunks hold zeros and form their own groups)
+#pragma unroll
+            for (int o = CPH / 2; o > 0; o >>= 1)
+#pragma unroll
+                for (int i = 0; i < P; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], o);
+            // online softmax of head sh, identical on every lane of the group
+            float mt = m_run;
+#pragma unroll
+            for (int i = 0; i < P; ++i) {
+                if (i >= ti.n) s[i] = -INFINITY;
+                mt = fmaxf(mt, s[i]);
+            }
+            const float a = fast_exp2(m_run - mt);    // m_run = -inf gives 0
             float sum = 0.f;
 #pragma unroll
             for (int i = 0; i < P; ++i) {
-                const float w = fast_exp2(sc[t][i] - mn);
-                sc[t][i] = w;
-                sum += w;
+                s[i] = fast_exp2(s[i] - mt);
+                sum += s[i];
             }
             l_run = l_run * a + sum;
-            m_run = mn;
-            alpha_s[t] = a;
+            m_run = mt;
+            if (is_k) {
+                float *wrow = wts + (st * nheads + sh) * P;
+#pragma unroll
+                for (int i = 0; i < P; ++i)
+                    if (gl == i) wrow[i] = s[i];
+                if (gl == 0) alph[st * nheads + sh] = a;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wready[st]);
+
+            if (ti.flags & kSegEnd) {
+                if (is_k && gl == 0) {
+                    const size_t slot = static_cast<size_t>(cta) + ti.b;
+                    p.ws_ml[(slot * nheads + sh) * 2 + 0] = m_run;
+                    p.ws_ml[(slot * nheads + sh) * 2 + 1] = l_run;
+                }
+                if (ti.flags & kLast) return;
+                m_run = -INFINITY;
+                l_run = 0.f;
+                load_q(ti.b + 1);                      // segments follow the sequences in order
+            }
         }
-        __syncthreads();
+    }
+
+    // ---------------------------------------------------------- V warps
+    const int vv = t - vbase;                      // chunk index in the V row
+    const bool is_v = vv < p.hs * p.dv / 8;
+    const int vh = is_v ? vv / (p.dv / 8) : 0;     // signal head
+    const int vg = p.hs + vh / (p.hs / p.hn);      // its noise head's score index
+    const int vcol = is_v ? vv % (p.dv / 8) * 8 : 0;
+    const uint32_t off = P * (rk1 + rk2) + (is_v ? vv : 0) * 16;
+    float o1[8], o2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o1[i] = o2[i] = 0.f;
+
+    for (int it = 0;; ++it) {
+        const int st = it % stages;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&wready[st], (it / stages) & 1, p.err, GDA_DEVERR_DECODE_TIMEOUT, &abort_flag)))
+            return;
+        const TileInfo ti = info[st];
         if (is_v) {
-            const float a1 = alpha_s[vh], a2 = alpha_s[p.hs + vg];
+            const float a1 = alph[st * nheads + vh], a2 = alph[st * nheads + vg];
+            float w1[P], w2[P];
+            load_weights<P>(w1, wts + (st * nheads + vh) * P);
+            load_weights<P>(w2, wts + (st * nheads + vg) * P);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 o1[e] *= a1;
                 o2[e] *= a2;
             }
+            const uint8_t *sb = ring + static_cast<size_t>(st) * stage_bytes + off;
 #pragma unroll
             for (int i = 0; i < P; ++i) {
-                if (i >= n) break;                      // rows outside the range were never copied
-                const float w1 = sc[vh][i], w2 = sc[p.hs + vg][i];
-                const uint4 vv = *reinterpret_cast<const uint4 *>(sb + i * stride);
-                const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+                if (i >= ti.n) break;                  // rows outside the range were never copied
+                const uint4 vq = *reinterpret_cast<const uint4 *>(sb + i * rv);
+                const uint32_t w[4] = {vq.x, vq.y, vq.z, vq.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float v0 = bf16_lo(w[e]), v1 = bf16_hi(w[e]);
-                    o1[2 * e] = fmaf(w1, v0, o1[2 * e]);
-                    o1[2 * e + 1] = fmaf(w1, v1, o1[2 * e + 1]);
-                    o2[2 * e] = fmaf(w2, v0, o2[2 * e]);
-                    o2[2 * e + 1] = fmaf(w2, v1, o2[2 * e + 1]);
+                    ffma2_acc(o1[2 * e], o1[2 * e + 1], w1[i], w1[i], v0, v1);
+                    ffma2_acc(o2[2 * e], o2[2 * e + 1], w2[i], w2[i], v0, v1);
                 }
             }
         }
-        // alpha_s, info[st] and this stage are rewritten only after the next
-        // tile's first barrier, which every V thread reaches after its reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
 
         if (ti.flags & kSegEnd) {
             // end of a segment: its partial state goes to slot (CTA + sequence)
-            const size_t slot = static_cast<size_t>(cta) + ti.b;
-            if (t < nheads) {
-                p.ws_ml[(slot * nheads + t) * 2 + 0] = m_run;
-                p.ws_ml[(slot * nheads + t) * 2 + 1] = l_run;
-            }
             if (is_v) {
+                const size_t slot = static_cast<size_t>(cta) + ti.b;
                 float *dst = p.ws_o + ((slot * p.hs + vh) * 2) * p.dv + vcol;
                 reinterpret_cast<float4 *>(dst)[0] = make_float4(o1[0], o1[1], o1[2], o1[3]);
                 reinterpret_cast<float4 *>(dst)[1] = make_float4(o1[4], o1[5], o1[6], o1[7]);
                 reinterpret_cast<float4 *>(dst + p.dv)[0] = make_float4(o2[0], o2[1], o2[2], o2[3]);
                 reinterpret_cast<float4 *>(dst + p.dv)[1] = make_float4(o2[4], o2[5], o2[6], o2[7]);
             }
-            if (ti.flags & kLast) break;
-            m_run = -INFINITY;
-            l_run = 0.f;
+            if (ti.flags & kLast) return;
 #pragma unroll
             for (int i = 0; i < 8; ++i) o1[i] = o2[i] = 0.f;
-            load_q(ti.b + 1);                           // segments follow the sequences in order
         }
     }
 }
@@ -505,7 +569,8 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     p.kc1 = a.hs * a.d / 8;
     p.kc = (a.hs + a.hn) * a.d / 8;
     p.nchunks = p.kc + a.hs * a.dv / 8;
-    const int threads = (p.nchunks + 31) / 32 * 32;
+    // producer warp, K warps, V warps (each role starts on a warp boundary)
+    const int threads = 32 + (p.kc + 31) / 32 * 32 + (p.nchunks - p.kc + 31) / 32 * 32;
     if (threads > 1024 || a.hs + a.hn > kMaxHeads) return GDA_ERR_UNSUPPORTED;
     if (a.B > 65535) return GDA_ERR_UNSUPPORTED;
 
@@ -513,16 +578,19 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     // outside it is copied), so the CTA can exit after its last tile
     const size_t row_bytes = 2 * (static_cast<size_t>(a.hs) * a.d + static_cast<size_t>(a.hn) * a.d +
                                   static_cast<size_t>(a.hs) * a.dv);
-    // ring budget: two CTAs per SM (with their static arrays) fit in 228 KB
-    // when a CTA has at most 512 threads, else one; the largest stage of
-    // 8, 4 or 2 positions of which at least four fit
+    const int nheads = a.hs + a.hn;
+    // ring budget: two CTAs per SM fit in 228 KB when a CTA has at most 512
+    // threads, else one; the largest stage of 8, 4 or 2 positions of which
+    // at least four fit (a stage also holds its P weights and rescale factor
+    // per head)
     const size_t budget = threads <= 512 ? 100 * 1024 : 200 * 1024;
     int P = 8;
-    while (P > 2 && row_bytes * P * 4 > budget) P /= 2;
-    int stages = static_cast<int>(budget / (row_bytes * P));
+    while (P > 2 && (row_bytes * P + nheads * (P + 1) * 4) * 4 > budget) P /= 2;
+    const size_t per_stage = row_bytes * P + static_cast<size_t>(nheads) * (P + 1) * 4;
+    int stages = static_cast<int>(budget / per_stage);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return GDA_ERR_UNSUPPORTED;
-    const size_t smem = static_cast<size_t>(stages) * P * row_bytes;
+    const size_t smem = static_cast<size_t>(stages) * per_stage;
     int dev = 0, sms = 0;
     cudaError_t e1 = cudaGetDevice(&dev);
     if (e1 == cudaSuccess) e1 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -296,6 +296,18 @@ __device__ __forceinline__ void ffma2(float &a0, float &a1, float b0, float b1, 
         : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
+// (d0, d1) += (a0 * b0, a1 * b1) as one packed fma.rn.f32x2.
+__device__ __forceinline__ void ffma2_acc(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 y, {%4, %5};\n\t"
+        "mov.b64 z, {%0, %1};\n\t"
+        "fma.rn.f32x2 z, x, y, z;\n\t"
+        "mov.b64 {%0, %1}, z;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // (a0, a1) += (b0, b1) as one packed add.f32x2.
 __device__ __forceinline__ void fadd2(float &a0, float &a1, float b0, float b1) {
     asm("{\n\t.reg .b64 x, y;\n\t"

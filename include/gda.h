@@ -134,8 +134,10 @@ size_t gda_attn_decode_workspace_size(int B, int Lcap, int h_s, int h_n, int dv)
  *   Two decode calls that are in flight at the same time need two
  *   workspaces.  A length outside [1, Lcap] is clamped on the device and
  *   reported through gda_device_error (GDA_DEVERR_BAD_LENGTH).
- *   Supported: d in {64, 128}; dv in {64, 128, 256};
- *   (h_s*d + h_n*d + h_s*dv) / 8 <= 1024.
+ *   Supported: d in {64, 128}; dv in {64, 128, 256}; h_s + h_n <= 128;
+ *   32 + up32((h_s + h_n)*d/8) + up32(h_s*dv/8) <= 1024, up32 rounding up
+ *   to a multiple of 32 (one thread per 16 bytes of a cache row, plus a
+ *   producer warp).
  * Split kernel (the batch's cache positions cut into equal contiguous ranges,
  * one per CTA, streamed through shared memory by bulk copies) plus a
  * combine kernel.
