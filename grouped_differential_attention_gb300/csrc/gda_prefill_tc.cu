@@ -31,11 +31,11 @@
 // is double-buffered, so QK(j+2) runs on the tensor core while the softmax
 // of tile j+1 runs, and the softmax warps never wait on their own map's PV.
 // P overwrites the first 32 columns of its S tile and feeds the PV MMA
-// straight from TMEM.  P is rounded to bf16 with an integer add and a byte
-// permute, leaving the special-function unit (which also executes the bf16
-// conversion instruction) to the exponentials.  A row's running max only
-// moves when it grows by more than 2^8 (exp2 units); only then is its
-// accumulator rescaled.
+// straight from TMEM.  A row's reference maximum is taken exactly on its
+// first key tile only; later tiles exponentiate against it directly (no
+// per-tile maximum on the critical path) and only a tile whose sum of P
+// grows past 2^16 is redone with its exact maximum, rescaling the row's sum
+// and accumulator.
 // dv = 256 is split over a 2-CTA cluster; the two CTAs exchange the per-row
 // sum of squares through distributed shared memory (remote store plus remote
 // mbarrier arrive) for the RMSNorm.
@@ -56,7 +56,7 @@ constexpr int kBM = 128;          // query rows per CTA (= TMEM lanes)
 constexpr int kDVS = 128;         // dv columns per CTA
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = 32 * (2 + kSoftmaxWarps);
-constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr float kSumLimit = 65536.0f;       // per-tile P sum that triggers a new reference
 
 template <int D> struct TcCfg;
 template <> struct TcCfg<64> { static constexpr int BN = 64, KS = 4, VS = 4; };
@@ -498,52 +498,72 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                     for (int e = 0; e < BN; ++e)
                         if (k0 + e > last_key) rr[e] = __float_as_uint(-INFINITY);
                 }
-                // row maximum: three-input max over 4 independent chains
-                float mx4[4];
+                // exact row maximum of the tile (exp2 units)
+                auto row_max = [&]() -> float {
+                    float mx4[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) mx4[i] = __uint_as_float(rr[i]);
+                    for (int i = 0; i < 4; ++i) mx4[i] = __uint_as_float(rr[i]);
 #pragma unroll
-                for (int e = 4; e + 8 <= BN; e += 8)
+                    for (int e = 4; e + 8 <= BN; e += 8)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        mx4[i] = max3f(mx4[i], __uint_as_float(rr[e + 2 * i]), __uint_as_float(rr[e + 2 * i + 1]));
-                float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+                        for (int i = 0; i < 4; ++i)
+                            mx4[i] = max3f(mx4[i], __uint_as_float(rr[e + 2 * i]), __uint_as_float(rr[e + 2 * i + 1]));
+                    float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
 #pragma unroll
-                for (int e = 4 + ((BN - 4) / 8) * 8; e < BN; ++e) mx = fmaxf(mx, __uint_as_float(rr[e]));
-                const float mx_s = mx * sl2;
+                    for (int e = 4 + ((BN - 4) / 8) * 8; e < BN; ++e) mx = fmaxf(mx, __uint_as_float(rr[e]));
+                    return mx * sl2;
+                };
+                // P = 2^(s*scale - m) stored packed over S (hidden keys hold
+                // -inf and give 0); returns the tile's sum of P
+                auto exp_store = [&](float m) -> float {
+                    const float neg_m = -m;
+                    float sa = 0.f, sb = 0.f, sc = 0.f, sd = 0.f;
+#pragma unroll
+                    for (int hh = 0; hh < BN / 32; ++hh) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            float x0 = __uint_as_float(rr[hh * 32 + e]), x1 = __uint_as_float(rr[hh * 32 + e + 1]);
+                            float x2 = __uint_as_float(rr[hh * 32 + e + 2]), x3 = __uint_as_float(rr[hh * 32 + e + 3]);
+                            ffma2(x0, x1, sl2, sl2, neg_m, neg_m);
+                            ffma2(x2, x3, sl2, sl2, neg_m, neg_m);
+                            x0 = fast_exp2(x0);
+                            x1 = fast_exp2(x1);
+                            x2 = fast_exp2(x2);
+                            x3 = fast_exp2(x3);
+                            fadd2(sa, sb, x0, x1);
+                            fadd2(sc, sd, x2, x3);
+                            pk[e / 2] = pack_bf16x2(x0, x1);
+                            pk[e / 2 + 1] = pack_bf16x2(x2, x3);
+                        }
+                        tmem_st16(tS + hh * 16, pk);
+                    }
+                    return (sa + sb) + (sc + sd);
+                };
+                // The reference m_ref is the exact maximum of the first tile.
+                // Later tiles reuse it: floating point keeps P's relative
+                // precision at any scale, so m_ref only has to keep P and the
+                // sums far from overflow.  A tile whose P sum exceeds
+                // kSumLimit (some P > kSumLimit / BN, or inf) is redone with
+                // its exact maximum as the new reference, and the row's sum
+                // and accumulator are rescaled.
+                if (j == 0) m_ref = row_max();
                 float alpha = 1.f;
                 bool rescale = false;
-                if (j == 0) {
-                    m_ref = mx_s;
-                } else if (mx_s > m_ref + kRescaleThreshold) {
-                    alpha = fast_exp2(m_ref - mx_s);
-                    m_ref = mx_s;
-                    rescale = true;
-                }
-                // P = 2^(s*scale - m_ref) (hidden keys hold -inf and give 0)
-                const float neg_m = -m_ref;
-                float sa = 0.f, sb = 0.f, sc = 0.f, sd = 0.f;
-#pragma unroll
-                for (int hh = 0; hh < BN / 32; ++hh) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        float x0 = __uint_as_float(rr[hh * 32 + e]), x1 = __uint_as_float(rr[hh * 32 + e + 1]);
-                        float x2 = __uint_as_float(rr[hh * 32 + e + 2]), x3 = __uint_as_float(rr[hh * 32 + e + 3]);
-                        ffma2(x0, x1, sl2, sl2, neg_m, neg_m);
-                        ffma2(x2, x3, sl2, sl2, neg_m, neg_m);
-                        x0 = fast_exp2(x0);
-                        x1 = fast_exp2(x1);
-                        x2 = fast_exp2(x2);
-                        x3 = fast_exp2(x3);
-                        fadd2(sa, sb, x0, x1);
-                        fadd2(sc, sd, x2, x3);
-                        pk[e / 2] = pack_hi16(round_bf16_bits(x0), round_bf16_bits(x1));
-                        pk[e / 2 + 1] = pack_hi16(round_bf16_bits(x2), round_bf16_bits(x3));
+                float tsum = exp_store(m_ref);
+                if (__any_sync(0xffffffffu, !(tsum <= kSumLimit))) {
+                    if (!(tsum <= kSumLimit)) {
+                        const float mt = row_max();
+                        if (mt > m_ref) {
+                            alpha = fast_exp2(m_ref - mt);
+                            m_ref = mt;
+                            rescale = true;
+                        }
                     }
-                    tmem_st16(tS + hh * 16, pk);
+                    tmem_st_wait();            // the first P store lands before it is overwritten
+                    tsum = exp_store(m_ref);   // every lane again: the TMEM store is warp-wide
                 }
-                l = l * alpha + ((sa + sb) + (sc + sd));
+                l = l * alpha + tsum;
                 // request the next S tile into rr
                 const bool more = j + 1 < nkv;
                 if (more) {

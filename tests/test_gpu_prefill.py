@@ -163,3 +163,25 @@ def test_prefill_f32_equal_maps_cancel():
     q1, k1, _, _, v, lam = W.make_prefill_inputs(W.DIFF_F32_L128, B=1, L=77, h_s=2, h_n=2, seed=3)
     got = run_f32((q1, k1, q1, k1, v, torch.ones_like(lam)), 0.8, flags=gda.GDA_FLAG_NO_NORM)
     assert torch.count_nonzero(got) == 0
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_bf16_rising_and_falling_scores(oracle_mod, causal):
+    """Scores that climb ~230 log2 units along the keys (2^230 overflows float32
+    unless the kernel moves its reference maximum as the row goes on) for the
+    signal map, and fall as steeply for the noise map (later keys underflow)."""
+    B, L, hs, hn, d, dv = 1, 600, 3, 1, 64, 128
+    g = torch.Generator().manual_seed(23)
+    t = torch.linspace(-1.0, 20.0, L)
+    q1 = torch.ones(B, L, hs, d) + 0.05 * torch.randn(B, L, hs, d, generator=g)
+    k1 = t[None, :, None, None] * torch.ones(B, L, hs, d)
+    q2 = torch.ones(B, L, hn, d) + 0.05 * torch.randn(B, L, hn, d, generator=g)
+    k2 = -t[None, :, None, None] * torch.ones(B, L, hn, d)
+    v = torch.randn(B, L, hs, dv, generator=g)
+    lam = torch.tensor([0.3, 0.5, 0.7])
+    bf = torch.bfloat16
+    inp = (q1.to(bf), k1.to(bf), q2.to(bf), k2.to(bf), v.to(bf), lam)
+    got = run_bf16(inp, 0.8, causal)
+    assert torch.isfinite(got.float()).all()
+    ref = oracle_mod.prefill(*inp, 0.8, causal=causal)
+    assert_bf16_close(got, ref, "rising/falling scores")
