@@ -92,7 +92,12 @@ template <int D> struct Layout {
     static constexpr int OFF_Q2 = Q_BYTES;
     static constexpr int OFF_K = 2 * Q_BYTES;
     static constexpr int OFF_V = OFF_K + KS * KST_BYTES;
-    static constexpr int TILES = OFF_V + VS * V_BYTES;
+    static constexpr int OFF_OUT = OFF_V + VS * V_BYTES;
+    // output staging for TMA stores: 32 rows x 64 columns (128-byte
+    // swizzle) per softmax warp, where shared memory allows (d = 64)
+    static constexpr bool TMA_OUT = D == 64;
+    static constexpr int OUT_BYTES = TMA_OUT ? kSoftmaxWarps * 32 * 128 : 0;
+    static constexpr int TILES = OFF_OUT + OUT_BYTES;
     static constexpr int TOTAL = TILES + (int)((sizeof(Ctrl) + 1023) / 1024) * 1024 + 1024;
     static_assert(TOTAL <= 232448, "shared memory budget");
     static_assert(256 + 4 * BN <= 512, "TMEM budget");
@@ -248,7 +253,8 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                       const __grid_constant__ CUtensorMap tmK1,
                       const __grid_constant__ CUtensorMap tmQ2,
                       const __grid_constant__ CUtensorMap tmK2,
-                      const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+                      const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmO, const TcParams p) {
     using LY = Layout<D>;
     constexpr int BN = LY::BN;
     constexpr int KS = LY::KS;
@@ -470,6 +476,7 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
             const int nkv = it.nkv;
             const int qrow = it.q0 + row;
             const int last_key = p.causal ? min(qrow, p.L - 1) : p.L - 1;
+            const float lam = p.lambda[it.h];     // loaded now, used by the epilogue
             float m_ref = -INFINITY;
             float l = 0.f;
             bool ok = true;
@@ -614,7 +621,6 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
             ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
             if (ok) ok = warp_wait(&ctl->o_final, r & 1, p.err, abort_flag);
             tc_fence_after();
-            const float lam = p.lambda[it.h];
             const float inv1 = 1.f / l1;
             const float c2 = lam / l2;
             const uint32_t tO1 = tmem + lane_off, tO2 = tmem + 128 + lane_off;
@@ -653,29 +659,67 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
             const float yscale =
                 p.no_norm ? 1.f : (1.f - p.lambda_init) * rsqrtf(ss_tot / static_cast<float>(p.dv) + p.eps);
             if (ok) {
-                __nv_bfloat16 *orow =
-                    p.out + ((static_cast<size_t>(it.b) * p.L + qrow) * p.hs + it.h) * p.dv + slice * kDVS + col0;
+                if constexpr (LY::TMA_OUT) {
+                    // stage this warp's 32 rows x 64 columns (128-byte swizzle:
+                    // 16-byte chunk c of row t sits at chunk c ^ (t % 8)) and
+                    // write them with one TMA store; rows past L are clipped
+                    uint8_t *obuf = smem + LY::OFF_OUT + (warp - 2) * (32 * 128);
+                    if (lane == 0) bulk_wait_group_read0();   // the previous item's store has read it
+                    __syncwarp();
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t r1[32], r2[32];
-                    tmem_ld32(tO1 + col0 + cc * 32, r1);
-                    tmem_ld32(tO2 + col0 + cc * 32, r2);
-                    tmem_ld_wait_regs(r1);
-                    reg_fence(r2);
-                    uint32_t pk[16];
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t r1[32], r2[32];
+                        tmem_ld32(tO1 + col0 + cc * 32, r1);
+                        tmem_ld32(tO2 + col0 + cc * 32, r2);
+                        tmem_ld_wait_regs(r1);
+                        reg_fence(r2);
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float y0 = (__fmul_rn(__uint_as_float(r1[e]), inv1) -
-                                          __fmul_rn(__uint_as_float(r2[e]), c2)) * yscale;
-                        const float y1 = (__fmul_rn(__uint_as_float(r1[e + 1]), inv1) -
-                                          __fmul_rn(__uint_as_float(r2[e + 1]), c2)) * yscale;
-                        pk[e / 2] = pack_bf16x2(y0, y1);
+                        for (int e = 0; e < 32; e += 2) {
+                            const float y0 = (__fmul_rn(__uint_as_float(r1[e]), inv1) -
+                                              __fmul_rn(__uint_as_float(r2[e]), c2)) * yscale;
+                            const float y1 = (__fmul_rn(__uint_as_float(r1[e + 1]), inv1) -
+                                              __fmul_rn(__uint_as_float(r2[e + 1]), c2)) * yscale;
+                            pk[e / 2] = pack_bf16x2(y0, y1);
+                        }
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            const int ch = cc * 4 + v4;
+                            *reinterpret_cast<uint4 *>(obuf + lane * 128 + ((ch ^ (lane & 7)) * 16)) =
+                                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                        }
                     }
-                    if (qrow < p.L) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_4d(&tmO, obuf, slice * kDVS + col0, it.h, it.q0 + quarter * 32, it.b);
+                        bulk_commit_group();
+                    }
+                } else {
+                    __nv_bfloat16 *orow =
+                        p.out + ((static_cast<size_t>(it.b) * p.L + qrow) * p.hs + it.h) * p.dv + slice * kDVS + col0;
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t r1[32], r2[32];
+                        tmem_ld32(tO1 + col0 + cc * 32, r1);
+                        tmem_ld32(tO2 + col0 + cc * 32, r2);
+                        tmem_ld_wait_regs(r1);
+                        reg_fence(r2);
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float y0 = (__fmul_rn(__uint_as_float(r1[e]), inv1) -
+                                              __fmul_rn(__uint_as_float(r2[e]), c2)) * yscale;
+                            const float y1 = (__fmul_rn(__uint_as_float(r1[e + 1]), inv1) -
+                                              __fmul_rn(__uint_as_float(r2[e + 1]), c2)) * yscale;
+                            pk[e / 2] = pack_bf16x2(y0, y1);
+                        }
+                        if (qrow < p.L) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+#pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4)
+                                dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                        }
                     }
                 }
             }
@@ -688,7 +732,9 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
         }
     }
 
-    // ---- teardown: all TMEM traffic of this CTA is complete past this barrier
+    // ---- teardown: our TMA stores have read their staging buffers, and all
+    // TMEM traffic of this CTA is complete past this barrier
+    if (LY::TMA_OUT && warp >= 2 && lane == 0) bulk_wait_group0();
     tc_fence_before();
     __syncthreads();
     if (p.nslices == 2) cluster_sync_all();   // no DSMEM traffic into an exited peer
@@ -702,7 +748,7 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
 template <int D>
 int launch_impl(const PrefillArgs &a, cudaStream_t stream) {
     using LY = Layout<D>;
-    CUtensorMap mQ1, mK1, mQ2, mK2, mV;
+    CUtensorMap mQ1, mK1, mQ2, mK2, mV, mO;
     const uint64_t B = a.B, L = a.L, hs = a.hs, hn = a.hn, d = a.d, dv = a.dv;
     {
         const uint64_t dims[4] = {d, hs, L, B};
@@ -725,6 +771,9 @@ int launch_impl(const PrefillArgs &a, cudaStream_t stream) {
         const uint64_t str[3] = {dv * 2, hs * dv * 2, L * hs * dv * 2};
         const uint32_t box[4] = {64, 1, (uint32_t)LY::BN, 1};
         if (!encode_tmap_4d_bf16(&mV, a.v, dims, str, box)) return GDA_ERR_CUDA;
+        // output: 32 query rows x 64 columns of one head per store
+        const uint32_t boxo[4] = {64, 1, 32, 1};
+        if (!encode_tmap_4d_bf16(&mO, a.out, dims, str, boxo)) return GDA_ERR_CUDA;
     }
     TcParams p;
     p.lambda = a.lambda;
@@ -769,7 +818,7 @@ int launch_impl(const PrefillArgs &a, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mQ1, mK1, mQ2, mK2, mV, p);
+    e = cudaLaunchKernelEx(&cfg, kern, mQ1, mK1, mQ2, mK2, mV, mO, p);
     return e == cudaSuccess ? GDA_OK : record_cuda_error(e);
 }
 
