@@ -36,9 +36,16 @@ import torch  # noqa: E402
 
 METRIC = "GDA causal prefill TFLOP/s (bf16) and decode HBM GB/s, % of GB300 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-PROFILE_FILE = os.path.join(ROOT, "profiles", "prefill_tc_counters.json")
-KERNEL_SOURCES = ["grouped_differential_attention_gb300/csrc/gda_prefill_tc.cu",
-                  "grouped_differential_attention_gb300/csrc/gda_device.cuh"]
+# DRAM counters of one ncu capture per kernel, valid while the kernel's
+# sources hash to the recorded value
+PROFILES = {
+    "prefill": (os.path.join(ROOT, "profiles", "prefill_tc_counters.json"),
+                ["grouped_differential_attention_gb300/csrc/gda_prefill_tc.cu",
+                 "grouped_differential_attention_gb300/csrc/gda_device.cuh"]),
+    "decode": (os.path.join(ROOT, "profiles", "decode_split_counters.json"),
+               ["grouped_differential_attention_gb300/csrc/gda_decode.cu",
+                "grouped_differential_attention_gb300/csrc/gda_device.cuh"]),
+}
 N_INPUT_SETS = 4          # rotating input copies: 4 x 84 MB > 129 MB of L2
 
 
@@ -72,22 +79,22 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback (no MEASURED_PEAKS.json)"
 
 
-def kernel_hash():
+def kernel_hash(kind="prefill"):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in PROFILES[kind][1]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
+def profiled_traffic(kind="prefill"):
     """DRAM bytes per launch from the committed ncu summary, if it matches the kernel."""
     try:
-        with open(PROFILE_FILE) as f:
+        with open(PROFILES[kind][0]) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None, None
-    if rec.get("kernel_hash") != kernel_hash():
+    if rec.get("kernel_hash") != kernel_hash(kind):
         return None, None
     return rec.get("dram_bytes_per_launch"), rec.get("workload")
 
@@ -356,7 +363,8 @@ def run_gda(args, world, rank, local):
     value = world * flops * args.steps / (prefill_ms * 1e-3) / 1e12
     per_launch_s = ms_per_step * 1e-3
     achieved = flops / per_launch_s / 1e12
-    traffic, traffic_wl = profiled_traffic()
+    traffic, traffic_wl = profiled_traffic("prefill")
+    dec_traffic, dec_traffic_wl = profiled_traffic("decode")
     dec_bytes = decode_bytes(lens_host, dw.h_s, dw.h_n, dw.d, dw.dv)
     dec_ms_step = decode_ms / dec_steps
     dec_gbs = dec_bytes / (dec_ms_step * 1e-3) / 1e9
@@ -406,7 +414,8 @@ def run_gda(args, world, rank, local):
             "gpu_launches": 2 * dec_steps,
             "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
-                         "traffic": None, "peak_source": f"{peak_src}: HBM copy"},
+                         "traffic": dec_traffic, "traffic_workload": dec_traffic_wl,
+                         "peak_source": f"{peak_src}: HBM copy"},
         },
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
