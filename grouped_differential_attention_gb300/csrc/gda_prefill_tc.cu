@@ -48,12 +48,11 @@
 #include "gda.h"
 #include "gda_device.cuh"
 #include "gda_internal.h"
+#include "gda_prefill_common.cuh"
 
 namespace gda {
 namespace {
 
-constexpr int kBM = 128;          // query rows per CTA (= TMEM lanes)
-constexpr int kDVS = 128;         // dv columns per CTA
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = 32 * (2 + kSoftmaxWarps);
 constexpr float kSumLimit = 65536.0f;       // per-tile P sum that triggers a new reference
@@ -112,68 +111,6 @@ struct TcParams {
     int B, L, hs, hn, dv, causal, nslices, nqt, no_norm;
 };
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-__device__ __forceinline__ void st_cluster_f32(const float *local, uint32_t peer, float v) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(peer));
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
-}
-
-// Wait used while winding down: ignores the abort flag, still bounded.
-__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
-    int dummy = 0;
-    mbar_wait(bar, parity, err, GDA_DEVERR_PREFILL_TIMEOUT, &dummy);
-}
-
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, unsigned *err,
-                                         volatile int *abort) {
-    return mbar_wait(bar, parity, err, GDA_DEVERR_PREFILL_TIMEOUT, abort);
-}
-
-// Whole-warp wait: every lane polls, the result is agreed by vote so the
-// warp stays converged for the .sync.aligned tcgen05 instructions after it.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, unsigned *err,
-                                          volatile int *abort) {
-    bool ok = wait_bar(bar, parity, err, abort);
-    return __all_sync(0xffffffffu, ok);
-}
-
-template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t qa, uint32_t ka) {
-    using LY = Layout<D>;
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, LY::BN, 0);
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
-        // K-major, 128-byte swizzle: 64-element column blocks, 8-row groups 1 KiB apart
-        const uint32_t blk = k / 4, sub = (k % 4) * 32;
-        const uint64_t a = smem_desc_sw128(qa + blk * (kBM * 128) + sub, 16, 1024);
-        const uint64_t b = smem_desc_sw128(ka + blk * (LY::BN * 128) + sub, 16, 1024);
-        mma_ss(tS, a, b, idesc, k > 0 ? 1u : 0u);
-    }
-}
-
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t va, bool acc) {
-    using LY = Layout<D>;
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kDVS, 1);
-#pragma unroll
-    for (int k = 0; k < LY::BN / 16; ++k) {
-        // V stage: two [BN x 64] column blocks, rows of 128 B, 128-B swizzle.
-        // MN-major B: 8-row K groups 1024 B apart, 64-column N blocks BN*128 B apart.
-        const uint64_t b = smem_desc_sw128(va + k * 2048, LY::BN * 128, 1024);
-        mma_ts(tO, tP + k * 8, b, idesc, (acc || k > 0) ? 1u : 0u);
-    }
-}
-
 // Work item = (query tile, batch, signal head); item 0 is the longest (last
 // query tile).  Persistent CTAs (or CTA pairs for dv = 256) take items in a
 // snake order: round r takes item r*G + c for even r and r*G + G-1-c for odd
@@ -197,54 +134,6 @@ __device__ __forceinline__ bool item_of(const TcParams &p, int r, int G, int cid
     const int kv_end = p.causal ? min(p.L, it.q0 + kBM) : p.L;
     it.nkv = (kv_end + bn - 1) / bn;
     return true;
-}
-
-// OR of `pred` over the `count` threads that reach named barrier `id`.
-__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred) {
-    uint32_t out;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(out)
-        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
-        : "memory");
-    return out != 0;
-}
-
-// Arrive on the peer CTA's mbarrier (release at cluster scope: the data
-// stored to the peer before this arrive is visible to its waiter).
-__device__ __forceinline__ void mbar_arrive_remote(uint64_t *local_bar, uint32_t peer) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_bar)), "r"(peer));
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
-}
-
-// Bounded wait with acquire at cluster scope (pairs with mbar_arrive_remote).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, unsigned *err,
-                                                  volatile int *abort) {
-    const uint32_t a = smem_u32(bar);
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 0;; ++it) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(a), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if ((it & 15u) == 15u) {
-            if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-                atomicOr(err, GDA_DEVERR_PREFILL_TIMEOUT);
-                *abort = 1;
-                return false;
-            }
-        }
-    }
 }
 
 template <int D>
@@ -407,9 +296,9 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                     if (!wait_bar(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t ka = k0a + (gk % KS) * LY::KST_BYTES;
-                    issue_qk<D>(tS1 + (gs & 1) * BN, q1a, ka);
+                    issue_qk<D, BN>(tS1 + (gs & 1) * BN, q1a, ka);
                     mma_commit(&ctl->s_full[0][gs & 1]);
-                    issue_qk<D>(tS2 + (gs & 1) * BN, q2a, ka + LY::K_BYTES);
+                    issue_qk<D, BN>(tS2 + (gs & 1) * BN, q2a, ka + LY::K_BYTES);
                     mma_commit(&ctl->s_full[1][gs & 1]);
                     mma_commit(&ctl->k_empty[gk % KS]);
                 }
@@ -429,22 +318,22 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                     if (!wait_bar(&ctl->p_full[0][bb], (gs >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
                     if (!wait_bar(&ctl->v_full[gv % VS], (gv / VS) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    issue_pv<D>(tO1, tS1 + bb * BN, va, j > 0);
+                    issue_pv<BN>(tO1, tS1 + bb * BN, va, j > 0);
                     mma_commit(&ctl->o_done[0]);
                     if (more) {
                         if (!wait_bar(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
                         tc_fence_after();
-                        issue_qk<D>(tS1 + bb * BN, q1a, kan);
+                        issue_qk<D, BN>(tS1 + bb * BN, q1a, kan);
                         mma_commit(&ctl->s_full[0][bb]);
                     }
                     // noise map: PV2(j), release V(j), then QK2(j+2) and release K(j+2)
                     if (!wait_bar(&ctl->p_full[1][bb], (gs >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    issue_pv<D>(tO2, tS2 + bb * BN, va, j > 0);
+                    issue_pv<BN>(tO2, tS2 + bb * BN, va, j > 0);
                     mma_commit(&ctl->o_done[1]);
                     mma_commit(&ctl->v_empty[gv % VS]);
                     if (more) {
-                        issue_qk<D>(tS2 + bb * BN, q2a, kan + LY::K_BYTES);
+                        issue_qk<D, BN>(tS2 + bb * BN, q2a, kan + LY::K_BYTES);
                         mma_commit(&ctl->s_full[1][bb]);
                         mma_commit(&ctl->k_empty[gk % KS]);
                         if (jn == nkv - 1) mma_commit(&ctl->q_empty);
