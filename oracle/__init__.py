@@ -182,3 +182,16 @@ def lambda_init_schedule(layer: int) -> float:
     starts at 0.2 in the first layer and approaches 0.8.
     """
     return 0.8 - 0.6 * math.exp(-0.3 * (layer - 1))
+
+
+def lambda_reparam(lq1, lk1, lq2, lk2, lambda_init: float) -> np.ndarray:
+    """lambda_h = exp(lq1_h . lk1_h) - exp(lq2_h . lk2_h) + lambda_init, float64.
+
+    "Differential Attention in Large Language Models ...", section "Learnable
+    Lambda Re-parameterization": four learnable vectors and the layer's
+    initialisation constant.  One set of vectors per signal head (arrays
+    [h_s, d]); a per-layer lambda is the case of identical rows.
+    """
+    a = np.sum(_f64(lq1) * _f64(lk1), axis=-1)
+    b = np.sum(_f64(lq2) * _f64(lk2), axis=-1)
+    return np.exp(a) - np.exp(b) + float(lambda_init)

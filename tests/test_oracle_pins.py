@@ -244,3 +244,48 @@ def test_oracle_rejects_bad_shapes(oracle_mod):
     q1, k1, q2, k2, v, lam = case(1, 4, 6, 4, 8, 16)   # 6 % 4 != 0
     with pytest.raises(ValueError):
         oracle_mod.prefill(q1, k1, q2, k2, v, lam, 0.8)
+
+
+# ------------------------------------------------------------ lambda reparam
+# "Differential Attention in Large Language Models ...", section "Learnable
+# Lambda Re-parameterization": lambda = exp(lq1.lk1) - exp(lq2.lk2) + lambda_init.
+
+def test_lambda_reparam_zero_vectors_give_lambda_init(oracle_mod):
+    z = np.zeros((5, 64))
+    got = oracle_mod.lambda_reparam(z, z, z, z, 0.37)
+    assert np.all(got == 0.37)
+
+
+def test_lambda_reparam_equal_branches_cancel_exactly(oracle_mod):
+    g = np.random.default_rng(3)
+    a, b = g.normal(size=(4, 32)), g.normal(size=(4, 32))
+    got = oracle_mod.lambda_reparam(a, b, a, b, 0.8)
+    assert np.all(got == 0.8)
+
+
+def test_lambda_reparam_single_component_closed_form(oracle_mod):
+    # one nonzero coordinate per vector: the dot products are plain products
+    d = 16
+    lq1, lk1, lq2, lk2 = (np.zeros((3, d)) for _ in range(4))
+    vals = [(0.5, -0.25, 0.1, 0.3), (1.0, 1.0, 0.0, 2.0), (-0.2, 0.7, 0.4, -0.9)]
+    for h, (a, b, c, e) in enumerate(vals):
+        lq1[h, h] = a
+        lk1[h, h] = b
+        lq2[h, d - 1 - h] = c
+        lk2[h, d - 1 - h] = e
+    got = oracle_mod.lambda_reparam(lq1, lk1, lq2, lk2, 0.2)
+    want = [math.exp(a * b) - math.exp(c * e) + 0.2 for (a, b, c, e) in vals]
+    assert np.allclose(got, want, rtol=0, atol=1e-15)
+
+
+def test_lambda_reparam_swapping_branches_mirrors_around_lambda_init(oracle_mod):
+    g = np.random.default_rng(4)
+    v = [g.normal(scale=0.3, size=(6, 64)) for _ in range(4)]
+    fwd = oracle_mod.lambda_reparam(v[0], v[1], v[2], v[3], 0.5)
+    rev = oracle_mod.lambda_reparam(v[2], v[3], v[0], v[1], 0.5)
+    assert np.allclose((fwd - 0.5) + (rev - 0.5), 0.0, atol=1e-14)
+    # one head through an explicit loop over the dimension
+    h = 2
+    a = sum(v[0][h, i] * v[1][h, i] for i in range(64))
+    b = sum(v[2][h, i] * v[3][h, i] for i in range(64))
+    assert abs(fwd[h] - (math.exp(a) - math.exp(b) + 0.5)) < 1e-13
