@@ -319,6 +319,22 @@ def run_gda(args, world, rank, local):
     torch.cuda.synchronize(dev)
     barrier(world)
     decode_ms = ev2.elapsed_time(ev3)
+
+    # ---- lambda re-parameterisation for one layer's heads (launch-latency bound)
+    g = torch.Generator().manual_seed(rank + 11)
+    lvec = [(0.1 * torch.randn(w.h_s, w.d, generator=g)).to(dev) for _ in range(4)]
+    lout = torch.empty(w.h_s, dtype=torch.float32, device=dev)
+    lam_steps = 200
+    for _ in range(5):
+        gda.gda_lambda_reparam(*lvec, w.lambda_init, out=lout)
+    torch.cuda.synchronize(dev)
+    ev4, ev5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev4.record(stream)
+    for _ in range(lam_steps):
+        gda.gda_lambda_reparam(*lvec, w.lambda_init, out=lout)
+    ev5.record(stream)
+    torch.cuda.synchronize(dev)
+    lam_us = ev4.elapsed_time(ev5) / lam_steps * 1e3
     clocks = sampler.stop()
     dev_err = gda.gda_device_error(clear=True)
 
@@ -417,6 +433,10 @@ def run_gda(args, world, rank, local):
                          "traffic": dec_traffic, "traffic_workload": dec_traffic_wl,
                          "peak_source": f"{peak_src}: HBM copy"},
         },
+        "lambda_reparam": {"workload": f"h_s={w.h_s} heads, d={w.d}", "us_per_call": lam_us,
+                           "calls": lam_steps, "gpu_launches": lam_steps,
+                           "bound": "host launch rate: back-to-back calls through the Python binding "
+                                    "(16 B x h_s x d read per call)"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": args.steps,

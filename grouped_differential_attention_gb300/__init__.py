@@ -85,6 +85,8 @@ def _load():
             lib.gda_status_string.restype = ctypes.c_char_p
             lib.gda_attn_decode_noalloc.argtypes = [P, P, P, P, P, P, P, F, P, I, I, I, I, I, I, F, P]
             lib.gda_attn_decode_noalloc.restype = I
+            lib.gda_lambda_reparam.argtypes = [P, P, P, P, F, P, I, I, P]
+            lib.gda_lambda_reparam.restype = I
             lib.gda_device_error.argtypes = [I]
             lib.gda_last_cuda_error.argtypes = []
             lib.gda_last_cuda_error.restype = I
@@ -164,6 +166,32 @@ def gda_attn_fwd_f32(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float,
     """float32 prefill on the CUDA cores; returns ``out``."""
     return _prefill(_load().gda_attn_fwd_f32_ex, torch.float32, q_sig, k_sig, q_noise, k_noise,
                     v, lam, lambda_init, causal, eps, out, flags)
+
+
+def gda_lambda_reparam(lambda_q1, lambda_k1, lambda_q2, lambda_k2, lambda_init: float, *, out=None):
+    """lambda[h] = exp(lq1[h].lk1[h]) - exp(lq2[h].lk2[h]) + lambda_init on the device.
+
+    The four vectors are float32 CUDA tensors [h_s, d]; returns ``out``
+    (float32 [h_s]), ready to pass as ``lam`` to the attention calls.
+    """
+    dev = lambda_q1.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if lambda_q1.dim() != 2:
+        raise ValueError("lambda vectors must be 2-D [h_s, d]")
+    hs, d = lambda_q1.shape
+    for t, name in ((lambda_q1, "lambda_q1"), (lambda_k1, "lambda_k1"), (lambda_q2, "lambda_q2"),
+                    (lambda_k2, "lambda_k2")):
+        _expect(t, name, torch.float32, (hs, d), dev)
+    if out is None:
+        out = torch.empty((hs,), dtype=torch.float32, device=dev)
+    _expect(out, "out", torch.float32, (hs,), dev)
+    with torch.cuda.device(dev):
+        rc = _load().gda_lambda_reparam(_ptr(lambda_q1), _ptr(lambda_k1), _ptr(lambda_q2),
+                                        _ptr(lambda_k2), float(lambda_init), _ptr(out), hs, d,
+                                        _stream(dev))
+    _check(rc, "gda lambda re-parameterisation")
+    return out
 
 
 def gda_attn_decode_workspace_size(B: int, Lcap: int, h_s: int, h_n: int, dv: int) -> int:

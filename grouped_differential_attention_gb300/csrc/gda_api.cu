@@ -209,6 +209,23 @@ int gda_attn_decode(const void *q_sig, const void *q_noise, const void *k_sig_ca
     return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int gda_lambda_reparam(const float *lambda_q1, const float *lambda_k1, const float *lambda_q2,
+                       const float *lambda_k2, float lambda_init, float *lambda_out, int h_s, int d,
+                       gda_stream_t stream) {
+    if (!lambda_q1 || !lambda_k1 || !lambda_q2 || !lambda_k2 || !lambda_out) return GDA_ERR_INVALID_ARG;
+    if (h_s < 1 || d < 1 || !std::isfinite(lambda_init)) return GDA_ERR_INVALID_ARG;
+    if (static_cast<long long>(h_s) * d > 0x7fffffffLL) return GDA_ERR_INVALID_ARG;
+    const uintptr_t any = reinterpret_cast<uintptr_t>(lambda_q1) | reinterpret_cast<uintptr_t>(lambda_k1) |
+                          reinterpret_cast<uintptr_t>(lambda_q2) | reinterpret_cast<uintptr_t>(lambda_k2) |
+                          reinterpret_cast<uintptr_t>(lambda_out);
+    if (any & 3u) return GDA_ERR_MISALIGNED;
+    unsigned *err = nullptr;
+    const int st = current_device(&err);
+    if (st != GDA_OK) return st;
+    return launch_lambda_reparam(lambda_q1, lambda_k1, lambda_q2, lambda_k2, lambda_init, lambda_out, h_s, d,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char *gda_status_string(int status) {
     switch (status) {
         case GDA_OK: return "success";

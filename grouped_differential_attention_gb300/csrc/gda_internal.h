@@ -47,6 +47,8 @@ int device_state(unsigned **err_word);
 int launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
 int launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream);
 int launch_decode(const DecodeArgs &a, cudaStream_t stream);
+int launch_lambda_reparam(const float *lq1, const float *lk1, const float *lq2, const float *lk2,
+                          float lambda_init, float *out, int hs, int d, cudaStream_t stream);
 
 // Split plan of the decode kernel (positions per split and split count).
 struct DecodePlan {

@@ -176,6 +176,25 @@ int gda_attn_decode_noalloc(const void *q_sig, const void *q_noise, const void *
                             const float *lambda, float lambda_init, void *out, int B, int Lcap,
                             int h_s, int h_n, int d, int dv, float eps, gda_stream_t stream);
 
+/*
+ * Re-parameterised lambda of every signal head ("Differential Attention in
+ * Large Language Models ...", section "Learnable Lambda Re-parameterization"):
+ *   lambda_out[h] = exp(lambda_q1[h] . lambda_k1[h]) - exp(lambda_q2[h] . lambda_k2[h])
+ *                   + lambda_init
+ *   lambda_q1, lambda_k1, lambda_q2, lambda_k2: [h_s, d] float32 device arrays
+ *   (one set of vectors per signal head; a per-layer lambda is the case of
+ *   identical rows), 4-byte aligned, owned by the caller.
+ *   lambda_out: [h_s] float32 device, the array gda_attn_fwd and
+ *   gda_attn_decode take as lambda.  lambda_init: the layer's constant (for
+ *   example 0.8 - 0.6 exp(-0.3 (l - 1)) for layer l).
+ * float32 dot products (fused multiply-adds over d) and expf.  Enqueued on
+ * `stream`; returns GDA_OK, GDA_ERR_INVALID_ARG (null pointer, h_s < 1,
+ * d < 1, non-finite lambda_init), GDA_ERR_MISALIGNED or a device error.
+ */
+int gda_lambda_reparam(const float *lambda_q1, const float *lambda_k1, const float *lambda_q2,
+                       const float *lambda_k2, float lambda_init, float *lambda_out, int h_s, int d,
+                       gda_stream_t stream);
+
 /* Static English description of a gda_status value. */
 const char *gda_status_string(int status);
 

@@ -142,3 +142,16 @@ def test_binding_checks_tensors_before_the_library():
     with pytest.raises(ValueError):
         gda.gda_attn_fwd(x, x, x, x, torch.zeros(1, 4, 2, 128, dtype=torch.bfloat16),
                          torch.zeros(2), 0.8)
+
+
+def test_lambda_reparam_rejects_bad_arguments(lib):
+    # every call below fails validation before any device work
+    F = ctypes.c_float
+    P = [ctypes.c_void_p(A)] * 4
+    out = ctypes.c_void_p(A)
+    assert lib.gda_lambda_reparam(None, *P[1:], F(0.8), out, 12, 64, None) == INVALID
+    assert lib.gda_lambda_reparam(*P, F(0.8), None, 12, 64, None) == INVALID
+    assert lib.gda_lambda_reparam(*P, F(0.8), out, 0, 64, None) == INVALID
+    assert lib.gda_lambda_reparam(*P, F(0.8), out, 12, 0, None) == INVALID
+    assert lib.gda_lambda_reparam(*P, F(float("nan")), out, 12, 64, None) == INVALID
+    assert lib.gda_lambda_reparam(ctypes.c_void_p(A + 2), *P[1:], F(0.8), out, 12, 64, None) == MISALIGNED
