@@ -57,3 +57,39 @@ def gda_dense(q1, k1, q2, k2, v, lam, lambda_init, causal=True, eps=1e-5, norm=T
         rms = np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
         o = (1.0 - lambda_init) * o / rms
     return o
+
+
+def gda_decode_dense(q1, q2, k1c, k2c, vc, lens, lam, lambda_init, eps=1e-5, norm=True,
+                     k1_scale=None, k2_scale=None, v_scale=None):
+    """Decode of one query token per sequence over its cache, float64.
+
+    q1: [B, hs, d]; q2: [B, hn, d]; k1c: [B, Lcap, hs, d]; k2c: [B, Lcap, hn, d];
+    vc: [B, Lcap, hs, dv]; lens: [B] (rows 0 .. lens[b]-1 are attended);
+    lam: [hs].  Optional per-head scales multiply the cached values first
+    (k1_scale, v_scale: [hs]; k2_scale: [hn]), which is how a quantised cache
+    (codes times a per-head scale) is dequantised.  The decode is the last
+    row of the causal prefill over the first lens[b] cache rows.
+    """
+    q1, q2, k1c, k2c, vc = (np.asarray(t, dtype=np.float64) for t in (q1, q2, k1c, k2c, vc))
+    lam = np.asarray(lam, dtype=np.float64).reshape(-1)
+    B, hs, d = q1.shape
+    hn = q2.shape[1]
+    if k1_scale is not None:
+        k1c = k1c * np.asarray(k1_scale, dtype=np.float64)[None, None, :, None]
+    if k2_scale is not None:
+        k2c = k2c * np.asarray(k2_scale, dtype=np.float64)[None, None, :, None]
+    if v_scale is not None:
+        vc = vc * np.asarray(v_scale, dtype=np.float64)[None, None, :, None]
+    group_of = contiguous_groups(hs, hn)
+    out = np.empty((B, hs, vc.shape[3]))
+    for b in range(B):
+        n = int(lens[b])
+        s1 = np.einsum("hd,jhd->hj", q1[b], k1c[b, :n]) / np.sqrt(d)
+        s2 = np.einsum("gd,jgd->gj", q2[b], k2c[b, :n]) / np.sqrt(d)
+        a1 = _softmax_last(s1)
+        a2 = _softmax_last(s2)[group_of]
+        o = np.einsum("hj,jhe->he", a1 - lam[:, None] * a2, vc[b, :n])
+        if norm:
+            o = (1.0 - lambda_init) * o / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+        out[b] = o
+    return out

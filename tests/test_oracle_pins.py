@@ -289,3 +289,40 @@ def test_lambda_reparam_swapping_branches_mirrors_around_lambda_init(oracle_mod)
     a = sum(v[0][h, i] * v[1][h, i] for i in range(64))
     b = sum(v[2][h, i] * v[3][h, i] for i in range(64))
     assert abs(fwd[h] - (math.exp(a) - math.exp(b) + 0.5)) < 1e-13
+
+
+# ------------------------------------------------------ dense float64 decode
+def test_dense_decode_matches_c_oracle(oracle_mod):
+    """The NumPy decode (used for scaled / quantised caches) agrees with the pinned C decode."""
+    g = torch.Generator().manual_seed(21)
+    B, Lcap, hs, hn, d, dv = 3, 40, 6, 2, 16, 32
+    q1, q2 = torch.randn(B, hs, d, generator=g), torch.randn(B, hn, d, generator=g)
+    k1, k2 = torch.randn(B, Lcap, hs, d, generator=g), torch.randn(B, Lcap, hn, d, generator=g)
+    v = torch.randn(B, Lcap, hs, dv, generator=g)
+    lens = torch.tensor([1, 17, 40], dtype=torch.int32)
+    lam = torch.rand(hs, generator=g)
+    ref = oracle_mod.decode(q1, q2, k1, k2, v, lens, lam, 0.8)
+    got = ref_numpy.gda_decode_dense(q1, q2, k1, k2, v, lens, lam, 0.8)
+    assert np.allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_dense_decode_scales_equal_prescaled_caches(oracle_mod):
+    """Per-head scales multiply the cached values: same as scaling the caches first."""
+    g = torch.Generator().manual_seed(22)
+    B, Lcap, hs, hn, d, dv = 2, 24, 4, 2, 8, 16
+    q1, q2 = torch.randn(B, hs, d, generator=g), torch.randn(B, hn, d, generator=g)
+    k1, k2 = torch.randn(B, Lcap, hs, d, generator=g), torch.randn(B, Lcap, hn, d, generator=g)
+    v = torch.randn(B, Lcap, hs, dv, generator=g)
+    lens = torch.tensor([24, 9], dtype=torch.int32)
+    lam = torch.rand(hs, generator=g)
+    s1, s2, sv = torch.rand(hs, generator=g) + 0.5, torch.rand(hn, generator=g) + 0.5, torch.rand(hs, generator=g) + 0.5
+    got = ref_numpy.gda_decode_dense(q1, q2, k1, k2, v, lens, lam, 0.8, k1_scale=s1, k2_scale=s2, v_scale=sv)
+    k1s = k1.double() * s1.double()[None, None, :, None]
+    k2s = k2.double() * s2.double()[None, None, :, None]
+    vs = v.double() * sv.double()[None, None, :, None]
+    want = ref_numpy.gda_decode_dense(q1, q2, k1s, k2s, vs, lens, lam, 0.8)
+    assert np.allclose(got, want, rtol=0, atol=1e-13)
+    # a V scale cancels in the headwise norm (up to eps): compare the pre-norm outputs instead
+    pre = ref_numpy.gda_decode_dense(q1, q2, k1, k2, v, lens, lam, 0.8, norm=False, v_scale=sv)
+    base = ref_numpy.gda_decode_dense(q1, q2, k1, k2, v, lens, lam, 0.8, norm=False)
+    assert np.allclose(pre, base * sv.double().numpy()[None, :, None], rtol=1e-13, atol=1e-14)
