@@ -320,6 +320,24 @@ def run_gda(args, world, rank, local):
     barrier(world)
     decode_ms = ev2.elapsed_time(ev3)
 
+    # ---- the same decode over fp8 (e4m3) caches with per-head scales
+    d8 = [t.to(dev) for t in W.make_decode_inputs_fp8(dw, seed=rank)]
+    d8_bytes = decode_bytes(d8[8].cpu(), dw.h_s, dw.h_n, dw.d, dw.dv) // 2
+
+    def d8step():
+        gda.gda_attn_decode_fp8(*d8, dw.lambda_init, eps=dw.eps, out=dout, workspace=ws)
+
+    for _ in range(max(3, args.warmup // 4)):
+        d8step()
+    torch.cuda.synchronize(dev)
+    ev6, ev7 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev6.record(stream)
+    for _ in range(dec_steps):
+        d8step()
+    ev7.record(stream)
+    torch.cuda.synchronize(dev)
+    d8_ms_step = ev6.elapsed_time(ev7) / dec_steps
+
     # ---- lambda re-parameterisation for one layer's heads (launch-latency bound)
     g = torch.Generator().manual_seed(rank + 11)
     lvec = [(0.1 * torch.randn(w.h_s, w.d, generator=g)).to(dev) for _ in range(4)]
@@ -433,6 +451,13 @@ def run_gda(args, world, rank, local):
                          "traffic": dec_traffic, "traffic_workload": dec_traffic_wl,
                          "peak_source": f"{peak_src}: HBM copy"},
         },
+        "decode_fp8": {"workload": dw.name + " with fp8 e4m3 caches (per-head scales)",
+                       "value": d8_bytes / (d8_ms_step * 1e-3) / 1e9, "unit": "GB/s",
+                       "ms_per_step": d8_ms_step, "steps": dec_steps, "bytes_per_step": d8_bytes,
+                       "speedup_vs_bf16_cache": dec_ms_step / d8_ms_step,
+                       "roofline": {"bound": "hbm", "achieved": d8_bytes / (d8_ms_step * 1e-3) / 1e9,
+                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                    "frac": d8_bytes / (d8_ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"]}},
         "lambda_reparam": {"workload": f"h_s={w.h_s} heads, d={w.d}", "us_per_call": lam_us,
                            "calls": lam_steps, "gpu_launches": lam_steps,
                            "bound": "host launch rate: back-to-back calls through the Python binding "

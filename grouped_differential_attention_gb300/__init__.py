@@ -85,6 +85,9 @@ def _load():
             lib.gda_status_string.restype = ctypes.c_char_p
             lib.gda_attn_decode_noalloc.argtypes = [P, P, P, P, P, P, P, F, P, I, I, I, I, I, I, F, P]
             lib.gda_attn_decode_noalloc.restype = I
+            lib.gda_attn_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, P, P, F, P, I, I, I, I, I, I, F,
+                                                P, Z, P]
+            lib.gda_attn_decode_fp8.restype = I
             lib.gda_lambda_reparam.argtypes = [P, P, P, P, F, P, I, I, P]
             lib.gda_lambda_reparam.restype = I
             lib.gda_device_error.argtypes = [I]
@@ -166,6 +169,53 @@ def gda_attn_fwd_f32(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float,
     """float32 prefill on the CUDA cores; returns ``out``."""
     return _prefill(_load().gda_attn_fwd_f32_ex, torch.float32, q_sig, k_sig, q_noise, k_noise,
                     v, lam, lambda_init, causal, eps, out, flags)
+
+
+def gda_attn_decode_fp8(q_sig, q_noise, k_sig_cache, k_noise_cache, v_cache, k_sig_scale,
+                        k_noise_scale, v_scale, cache_lens, lam, lambda_init: float, *,
+                        eps: float = 1e-5, out=None, workspace=None):
+    """bf16 decode over fp8 (e4m3) caches: cached value = code * scale of its head.
+
+    The caches are ``torch.float8_e4m3fn`` (or ``uint8`` holding the codes)
+    CUDA tensors [B, Lcap, heads, dim]; scales are float32 [h_s], [h_n], [h_s].
+    """
+    dev = q_sig.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, hs, d = q_sig.shape
+    hn = q_noise.shape[1]
+    Lcap = k_sig_cache.shape[1]
+    dv = v_cache.shape[3]
+    bf = torch.bfloat16
+    codes = []
+    for t, name, shape in ((k_sig_cache, "k_sig_cache", (B, Lcap, hs, d)),
+                           (k_noise_cache, "k_noise_cache", (B, Lcap, hn, d)),
+                           (v_cache, "v_cache", (B, Lcap, hs, dv))):
+        if t.dtype == torch.float8_e4m3fn:
+            t = t.view(torch.uint8)
+        _expect(t, name, torch.uint8, shape, dev)
+        codes.append(t)
+    _expect(q_sig, "q_sig", bf, (B, hs, d), dev)
+    _expect(q_noise, "q_noise", bf, (B, hn, d), dev)
+    _expect(k_sig_scale, "k_sig_scale", torch.float32, (hs,), dev)
+    _expect(k_noise_scale, "k_noise_scale", torch.float32, (hn,), dev)
+    _expect(v_scale, "v_scale", torch.float32, (hs,), dev)
+    _expect(cache_lens, "cache_lens", torch.int32, (B,), dev)
+    _expect(lam, "lam", torch.float32, (hs,), dev)
+    if out is None:
+        out = torch.empty((B, hs, dv), dtype=bf, device=dev)
+    _expect(out, "out", bf, (B, hs, dv), dev)
+    need = gda_attn_decode_workspace_size(B, Lcap, hs, hn, dv)
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = _load().gda_attn_decode_fp8(
+            _ptr(q_sig), _ptr(q_noise), _ptr(codes[0]), _ptr(codes[1]), _ptr(codes[2]),
+            _ptr(k_sig_scale), _ptr(k_noise_scale), _ptr(v_scale), _ptr(cache_lens), _ptr(lam),
+            float(lambda_init), _ptr(out), B, Lcap, hs, hn, d, dv, float(eps), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(dev))
+    _check(rc, "gda decode (fp8 cache)")
+    return out
 
 
 def gda_lambda_reparam(lambda_q1, lambda_k1, lambda_q2, lambda_k2, lambda_init: float, *, out=None):

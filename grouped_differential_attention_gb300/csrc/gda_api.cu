@@ -209,6 +209,42 @@ int gda_attn_decode(const void *q_sig, const void *q_noise, const void *k_sig_ca
     return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int gda_attn_decode_fp8(const void *q_sig, const void *q_noise, const void *k_sig_cache,
+                        const void *k_noise_cache, const void *v_cache, const float *k_sig_scale,
+                        const float *k_noise_scale, const float *v_scale, const int *cache_lens,
+                        const float *lambda, float lambda_init, void *out, int B, int Lcap, int h_s,
+                        int h_n, int d, int dv, float eps, void *workspace, size_t workspace_bytes,
+                        gda_stream_t stream) {
+    if (!q_sig || !q_noise || !k_sig_cache || !k_noise_cache || !v_cache || !k_sig_scale || !k_noise_scale ||
+        !v_scale || !cache_lens || !lambda || !out)
+        return GDA_ERR_INVALID_ARG;
+    if (B < 1 || Lcap < 1 || h_s < 1 || h_n < 1 || d < 1 || dv < 1 || h_s % h_n != 0)
+        return GDA_ERR_INVALID_ARG;
+    if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(lambda_init)) return GDA_ERR_INVALID_ARG;
+    if (static_cast<double>(B) * Lcap * h_s * (d > dv ? d : dv) > 9.0e15) return GDA_ERR_INVALID_ARG;
+    if (!(d == 64 || d == 128) || !(dv == 64 || dv == 128 || dv == 256)) return GDA_ERR_UNSUPPORTED;
+    if (h_s + h_n > 128 || B > 65535) return GDA_ERR_UNSUPPORTED;
+    if (!aligned16(q_sig) || !aligned16(q_noise) || !aligned16(k_sig_cache) || !aligned16(k_noise_cache) ||
+        !aligned16(v_cache) || !aligned16(cache_lens) || !aligned16(lambda) || !aligned16(out))
+        return GDA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(k_sig_scale) | reinterpret_cast<uintptr_t>(k_noise_scale) |
+         reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+        return GDA_ERR_MISALIGNED;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < gda_attn_decode_workspace_size(B, Lcap, h_s, h_n, dv))
+        return GDA_ERR_WORKSPACE;
+    unsigned *err = nullptr;
+    const int st = current_device(&err);
+    if (st != GDA_OK) return st;
+    DecodeArgs a{q_sig, q_noise, k_sig_cache, k_noise_cache, v_cache, cache_lens, lambda, lambda_init,
+                 out, B, Lcap, h_s, h_n, d, dv, eps, workspace, workspace_bytes, err};
+    a.fp8 = 1;
+    a.k1_scale = k_sig_scale;
+    a.k2_scale = k_noise_scale;
+    a.v_scale = v_scale;
+    return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int gda_lambda_reparam(const float *lambda_q1, const float *lambda_k1, const float *lambda_q2,
                        const float *lambda_k2, float lambda_init, float *lambda_out, int h_s, int d,
                        gda_stream_t stream) {

@@ -30,6 +30,8 @@
 // (1 - lambda_init) RMSNorm epilogue.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cstdint>
 #include <cmath>
 #include <algorithm>
@@ -45,7 +47,9 @@ namespace {
 constexpr int kMaxHeads = 128;    // h_s + h_n bound for the shared score arrays
 
 struct DecParams {
-    const __nv_bfloat16 *q1, *q2, *k1c, *k2c, *vc;
+    const __nv_bfloat16 *q1, *q2;
+    const uint8_t *k1c, *k2c, *vc;    // bf16 or fp8 (e4m3) cache elements
+    const float *k1_scale, *k2_scale, *v_scale;   // per-head dequantisation scales (fp8 caches)
     const int *lens;
     const float *lambda;
     __nv_bfloat16 *out;
@@ -59,6 +63,7 @@ struct DecParams {
     int ctas;          // CTAs of the split kernel
     int kc1, kc;       // chunk boundaries: K1 chunks [0,kc1), K2 [kc1,kc), V [kc, nchunks)
     int nchunks;
+    int es;            // cache element bytes: 2 (bf16) or 1 (fp8 e4m3)
 };
 
 __device__ __forceinline__ int clamp_len(int len, int Lcap, unsigned *err) {
@@ -125,7 +130,7 @@ template <int P>
 __device__ __forceinline__ void issue_tile(const DecParams &p, Cursor &c, int stages, uint8_t *ring,
                                            uint64_t *full, TileInfo *info) {
     if (c.done) return;
-    const uint32_t rk1 = p.hs * p.d * 2, rk2 = p.hn * p.d * 2, rv = p.hs * p.dv * 2;
+    const uint32_t rk1 = p.hs * p.d * p.es, rk2 = p.hn * p.d * p.es, rv = p.hs * p.dv * p.es;
     const int n = min(P, c.hi - c.pos);
     const int st = c.k % stages;
     uint8_t *sb = ring + static_cast<size_t>(st) * P * (rk1 + rk2 + rv);
@@ -152,10 +157,36 @@ __device__ __forceinline__ void issue_tile(const DecParams &p, Cursor &c, int st
     info[st] = TileInfo{n, b, flags};
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // prior generic reads of the stage
     mbar_arrive_expect_tx(&full[st], n * (rk1 + rk2 + rv));          // releases info[st]
-    bulk_copy_g2s(sb, p.k1c + row0 * (rk1 / 2), n * rk1, &full[st]);
-    bulk_copy_g2s(sb + P * rk1, p.k2c + row0 * (rk2 / 2), n * rk2, &full[st]);
-    bulk_copy_g2s(sb + P * (rk1 + rk2), p.vc + row0 * (rv / 2), n * rv, &full[st]);
+    bulk_copy_g2s(sb, p.k1c + row0 * rk1, n * rk1, &full[st]);
+    bulk_copy_g2s(sb + P * rk1, p.k2c + row0 * rk2, n * rk2, &full[st]);
+    bulk_copy_g2s(sb + P * (rk1 + rk2), p.vc + row0 * rv, n * rv, &full[st]);
     ++c.k;
+}
+
+// The EPC cache elements of one 16-byte chunk as floats: 8 bf16, or 16 fp8
+// (e4m3) through the packed fp8x2 -> half2 conversion.
+template <bool F8>
+__device__ __forceinline__ void unpack_chunk(const uint4 &c, float (&x)[F8 ? 16 : 8]) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    if constexpr (F8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+                    static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * hh)) & 0xFFFFu), __NV_E4M3);
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+                x[4 * i + 2 * hh] = f.x;
+                x[4 * i + 2 * hh + 1] = f.y;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = bf16_lo(w[i]);
+            x[2 * i + 1] = bf16_hi(w[i]);
+        }
+    }
 }
 
 // P consecutive floats from shared memory (16-byte aligned for P >= 4, 8-byte for P = 2).
@@ -206,9 +237,10 @@ __device__ __forceinline__ void load_weights(float (&w)[P], const float *src) {
 //     empty[stage], which hands the stage back to the producer.
 // Shared memory (dynamic): ring [stages][P rows of K1 | P rows of K2 |
 // P rows of V], weights [stages][h_s + h_n][P], rescale [stages][h_s + h_n].
-template <int D, int P, int kMaxThreads, int kMinBlocks>
+template <int D, int P, bool F8, int kMaxThreads, int kMinBlocks>
 __global__ void __launch_bounds__(kMaxThreads, kMinBlocks)
 gda_decode_split_kernel(const DecParams p, int stages) {
+    constexpr int EPC = F8 ? 16 : 8;              // cache elements per 16-byte chunk
     __shared__ uint64_t full[kMaxStages], wready[kMaxStages], empty[kMaxStages];
     __shared__ TileInfo info[kMaxStages];
     __shared__ long long red_s[32];
@@ -265,7 +297,7 @@ gda_decode_split_kernel(const DecParams p, int stages) {
     const int n_kwarps = (p.kc + 31) / 32;
     const int vbase = 32 + n_kwarps * 32;          // first V thread
     const int n_vwarps = (p.nchunks - p.kc + 31) / 32;
-    const uint32_t rk1 = p.hs * D * 2, rk2 = p.hn * D * 2, rv = p.hs * p.dv * 2;   // row bytes
+    const uint32_t rk1 = p.hs * D * p.es, rk2 = p.hn * D * p.es, rv = p.hs * p.dv * p.es;   // row bytes
     const uint32_t stage_bytes = P * (rk1 + rk2 + rv);
     float *wts = reinterpret_cast<float *>(ring + static_cast<size_t>(stages) * stage_bytes);  // [stages][nheads][P]
     float *alph = wts + stages * nheads * P;                                                    // [stages][nheads]
@@ -309,7 +341,7 @@ gda_decode_split_kernel(const DecParams p, int stages) {
 
     if (t < vbase) {
         // ------------------------------------------------------ K warps
-        constexpr int CPH = D / 8;                 // lanes (16-byte chunks) per head row of K
+        constexpr int CPH = D / EPC;               // lanes (16-byte chunks) per head row of K
         const int kk = t - 32;                     // chunk index in [K1 | K2]
         const bool is_k = kk < p.kc;
         uint32_t off = 0, stride = 0;
@@ -325,20 +357,28 @@ gda_decode_split_kernel(const DecParams p, int stages) {
         }
         const int gl = kk % CPH;                   // lane within the head's group
 
-        float q[8];
+        // query chunk of a K thread, pre-scaled into exp2 units (and by the
+        // head's K dequantisation scale for an fp8 cache)
+        float q[EPC];
         auto load_q = [&](int b) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = 0.f;
+            for (int i = 0; i < EPC; ++i) q[i] = 0.f;
             if (!is_k) return;
-            const __nv_bfloat16 *qp = (kk < p.kc1)
-                ? p.q1 + static_cast<size_t>(b) * p.hs * D + static_cast<size_t>(kk) * 8
-                : p.q2 + static_cast<size_t>(b) * p.hn * D + static_cast<size_t>(kk - p.kc1) * 8;
-            const uint4 qv = *reinterpret_cast<const uint4 *>(qp);
-            const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+            const bool sig = kk < p.kc1;
+            const int c = sig ? kk : kk - p.kc1;
+            const __nv_bfloat16 *qp = sig ? p.q1 + static_cast<size_t>(b) * p.hs * D + static_cast<size_t>(c) * EPC
+                                          : p.q2 + static_cast<size_t>(b) * p.hn * D + static_cast<size_t>(c) * EPC;
+            float f = p.scale_log2;
+            if constexpr (F8) f *= sig ? p.k1_scale[sh] : p.k2_scale[sh - p.hs];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                q[2 * i] = bf16_lo(w[i]) * p.scale_log2;
-                q[2 * i + 1] = bf16_hi(w[i]) * p.scale_log2;
+            for (int h8 = 0; h8 < EPC / 8; ++h8) {
+                const uint4 qv = reinterpret_cast<const uint4 *>(qp)[h8];
+                const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    q[8 * h8 + 2 * i] = bf16_lo(w[i]) * f;
+                    q[8 * h8 + 2 * i + 1] = bf16_hi(w[i]) * f;
+                }
             }
         };
         load_q(b_first);
@@ -357,11 +397,10 @@ gda_decode_split_kernel(const DecParams p, int stages) {
             for (int i = 0; i < P; ++i) {
                 float a0 = 0.f, a1 = 0.f;
                 if (is_k && i < ti.n) {
-                    const uint4 kv = *reinterpret_cast<const uint4 *>(sb + i * stride);
-                    const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+                    float kx[EPC];
+                    unpack_chunk<F8>(*reinterpret_cast<const uint4 *>(sb + i * stride), kx);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        ffma2_acc(a0, a1, q[2 * e], q[2 * e + 1], bf16_lo(w[e]), bf16_hi(w[e]));
+                    for (int e = 0; e < EPC; e += 2) ffma2_acc(a0, a1, q[e], q[e + 1], kx[e], kx[e + 1]);
                 }
                 s[i] = a0 + a1;
             }
@@ -389,9 +428,11 @@ gda_decode_split_kernel(const DecParams p, int stages) {
             m_run = mt;
             if (is_k) {
                 float *wrow = wts + (st * nheads + sh) * P;
+                // every lane of the group holds all P weights; lane gl writes
+                // the positions i with i % CPH == gl (CPH may be below P)
 #pragma unroll
                 for (int i = 0; i < P; ++i)
-                    if (gl == i) wrow[i] = s[i];
+                    if (gl == i % CPH) wrow[i] = s[i];
                 if (gl == 0) alph[st * nheads + sh] = a;
             }
             __syncwarp();
@@ -413,14 +454,14 @@ gda_decode_split_kernel(const DecParams p, int stages) {
 
     // ---------------------------------------------------------- V warps
     const int vv = t - vbase;                      // chunk index in the V row
-    const bool is_v = vv < p.hs * p.dv / 8;
-    const int vh = is_v ? vv / (p.dv / 8) : 0;     // signal head
+    const bool is_v = vv < p.hs * p.dv / EPC;
+    const int vh = is_v ? vv / (p.dv / EPC) : 0;   // signal head
     const int vg = p.hs + vh / (p.hs / p.hn);      // its noise head's score index
-    const int vcol = is_v ? vv % (p.dv / 8) * 8 : 0;
+    const int vcol = is_v ? vv % (p.dv / EPC) * EPC : 0;
     const uint32_t off = P * (rk1 + rk2) + (is_v ? vv : 0) * 16;
-    float o1[8], o2[8];
+    float o1[EPC], o2[EPC];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o1[i] = o2[i] = 0.f;
+    for (int i = 0; i < EPC; ++i) o1[i] = o2[i] = 0.f;
 
     for (int it = 0;; ++it) {
         const int st = it % stages;
@@ -434,7 +475,7 @@ gda_decode_split_kernel(const DecParams p, int stages) {
             load_weights<P>(w1, wts + (st * nheads + vh) * P);
             load_weights<P>(w2, wts + (st * nheads + vg) * P);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
+            for (int e = 0; e < EPC; ++e) {
                 o1[e] *= a1;
                 o2[e] *= a2;
             }
@@ -442,13 +483,12 @@ gda_decode_split_kernel(const DecParams p, int stages) {
 #pragma unroll
             for (int i = 0; i < P; ++i) {
                 if (i >= ti.n) break;                  // rows outside the range were never copied
-                const uint4 vq = *reinterpret_cast<const uint4 *>(sb + i * rv);
-                const uint32_t w[4] = {vq.x, vq.y, vq.z, vq.w};
+                float vx[EPC];
+                unpack_chunk<F8>(*reinterpret_cast<const uint4 *>(sb + i * rv), vx);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float v0 = bf16_lo(w[e]), v1 = bf16_hi(w[e]);
-                    ffma2_acc(o1[2 * e], o1[2 * e + 1], w1[i], w1[i], v0, v1);
-                    ffma2_acc(o2[2 * e], o2[2 * e + 1], w2[i], w2[i], v0, v1);
+                for (int e = 0; e < EPC; e += 2) {
+                    ffma2_acc(o1[e], o1[e + 1], w1[i], w1[i], vx[e], vx[e + 1]);
+                    ffma2_acc(o2[e], o2[e + 1], w2[i], w2[i], vx[e], vx[e + 1]);
                 }
             }
         }
@@ -460,14 +500,19 @@ gda_decode_split_kernel(const DecParams p, int stages) {
             if (is_v) {
                 const size_t slot = static_cast<size_t>(cta) + ti.b;
                 float *dst = p.ws_o + ((slot * p.hs + vh) * 2) * p.dv + vcol;
-                reinterpret_cast<float4 *>(dst)[0] = make_float4(o1[0], o1[1], o1[2], o1[3]);
-                reinterpret_cast<float4 *>(dst)[1] = make_float4(o1[4], o1[5], o1[6], o1[7]);
-                reinterpret_cast<float4 *>(dst + p.dv)[0] = make_float4(o2[0], o2[1], o2[2], o2[3]);
-                reinterpret_cast<float4 *>(dst + p.dv)[1] = make_float4(o2[4], o2[5], o2[6], o2[7]);
+                // an fp8 cache's V scale multiplies the whole accumulator
+                const float vs = F8 ? p.v_scale[vh] : 1.f;
+#pragma unroll
+                for (int e = 0; e < EPC; e += 4) {
+                    reinterpret_cast<float4 *>(dst)[e / 4] =
+                        make_float4(o1[e] * vs, o1[e + 1] * vs, o1[e + 2] * vs, o1[e + 3] * vs);
+                    reinterpret_cast<float4 *>(dst + p.dv)[e / 4] =
+                        make_float4(o2[e] * vs, o2[e + 1] * vs, o2[e + 2] * vs, o2[e + 3] * vs);
+                }
             }
             if (ti.flags & kLast) return;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o1[i] = o2[i] = 0.f;
+            for (int i = 0; i < EPC; ++i) o1[i] = o2[i] = 0.f;
         }
     }
 }
@@ -514,11 +559,12 @@ gda_decode_combine_kernel(const DecParams p) {
     p.out[(static_cast<size_t>(b) * p.hs + h) * p.dv + col] = __float2bfloat16_rn(y);
 }
 
-template <int D, int P>
+template <int D, int P, bool F8>
 cudaError_t launch_split(dim3 grid, int threads, size_t smem, cudaStream_t stream, const DecParams &p, int stages) {
     // up to 384 threads: two CTAs per SM with up to 80 registers a thread;
     // else at most 64 registers (two CTAs of up to 512 threads, or one)
-    auto kern = threads <= 384 ? gda_decode_split_kernel<D, P, 384, 2> : gda_decode_split_kernel<D, P, 1024, 1>;
+    auto kern = threads <= 384 ? gda_decode_split_kernel<D, P, F8, 384, 2>
+                               : gda_decode_split_kernel<D, P, F8, 1024, 1>;
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<grid, threads, smem, stream>>>(p, stages);
@@ -547,9 +593,15 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     DecParams p;
     p.q1 = static_cast<const __nv_bfloat16 *>(a.q1);
     p.q2 = static_cast<const __nv_bfloat16 *>(a.q2);
-    p.k1c = static_cast<const __nv_bfloat16 *>(a.k1c);
-    p.k2c = static_cast<const __nv_bfloat16 *>(a.k2c);
-    p.vc = static_cast<const __nv_bfloat16 *>(a.vc);
+    p.k1c = static_cast<const uint8_t *>(a.k1c);
+    p.k2c = static_cast<const uint8_t *>(a.k2c);
+    p.vc = static_cast<const uint8_t *>(a.vc);
+    p.k1_scale = a.k1_scale;
+    p.k2_scale = a.k2_scale;
+    p.v_scale = a.v_scale;
+    const bool f8 = a.fp8 != 0;
+    const int epc = f8 ? 16 : 8;                  // cache elements per 16-byte chunk
+    p.es = f8 ? 1 : 2;
     p.lens = a.lens;
     p.lambda = a.lambda;
     p.out = static_cast<__nv_bfloat16 *>(a.out);
@@ -566,9 +618,9 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     p.hn = a.hn;
     p.d = a.d;
     p.dv = a.dv;
-    p.kc1 = a.hs * a.d / 8;
-    p.kc = (a.hs + a.hn) * a.d / 8;
-    p.nchunks = p.kc + a.hs * a.dv / 8;
+    p.kc1 = a.hs * a.d / epc;
+    p.kc = (a.hs + a.hn) * a.d / epc;
+    p.nchunks = p.kc + a.hs * a.dv / epc;
     // producer warp, K warps, V warps (each role starts on a warp boundary)
     const int threads = 32 + (p.kc + 31) / 32 * 32 + (p.nchunks - p.kc + 31) / 32 * 32;
     if (threads > 1024 || a.hs + a.hn > kMaxHeads) return GDA_ERR_UNSUPPORTED;
@@ -576,8 +628,8 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
 
     // every copy in flight completes within the CTA's range (no position
     // outside it is copied), so the CTA can exit after its last tile
-    const size_t row_bytes = 2 * (static_cast<size_t>(a.hs) * a.d + static_cast<size_t>(a.hn) * a.d +
-                                  static_cast<size_t>(a.hs) * a.dv);
+    const size_t row_bytes = p.es * (static_cast<size_t>(a.hs) * a.d + static_cast<size_t>(a.hn) * a.d +
+                                     static_cast<size_t>(a.hs) * a.dv);
     const int nheads = a.hs + a.hn;
     // ring budget: two CTAs per SM fit in 228 KB when a CTA has at most 512
     // threads, else one; the largest stage of 8, 4 or 2 positions of which
@@ -599,13 +651,19 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     p.min_per_cta = 64;
     const dim3 grid(p.ctas);
     cudaError_t e0;
-    switch (a.d * 16 + P) {
-        case 64 * 16 + 8: e0 = launch_split<64, 8>(grid, threads, smem, stream, p, stages); break;
-        case 64 * 16 + 4: e0 = launch_split<64, 4>(grid, threads, smem, stream, p, stages); break;
-        case 64 * 16 + 2: e0 = launch_split<64, 2>(grid, threads, smem, stream, p, stages); break;
-        case 128 * 16 + 8: e0 = launch_split<128, 8>(grid, threads, smem, stream, p, stages); break;
-        case 128 * 16 + 4: e0 = launch_split<128, 4>(grid, threads, smem, stream, p, stages); break;
-        case 128 * 16 + 2: e0 = launch_split<128, 2>(grid, threads, smem, stream, p, stages); break;
+    switch ((a.d * 16 + P) * 2 + (f8 ? 1 : 0)) {
+        case (64 * 16 + 8) * 2: e0 = launch_split<64, 8, false>(grid, threads, smem, stream, p, stages); break;
+        case (64 * 16 + 4) * 2: e0 = launch_split<64, 4, false>(grid, threads, smem, stream, p, stages); break;
+        case (64 * 16 + 2) * 2: e0 = launch_split<64, 2, false>(grid, threads, smem, stream, p, stages); break;
+        case (128 * 16 + 8) * 2: e0 = launch_split<128, 8, false>(grid, threads, smem, stream, p, stages); break;
+        case (128 * 16 + 4) * 2: e0 = launch_split<128, 4, false>(grid, threads, smem, stream, p, stages); break;
+        case (128 * 16 + 2) * 2: e0 = launch_split<128, 2, false>(grid, threads, smem, stream, p, stages); break;
+        case (64 * 16 + 8) * 2 + 1: e0 = launch_split<64, 8, true>(grid, threads, smem, stream, p, stages); break;
+        case (64 * 16 + 4) * 2 + 1: e0 = launch_split<64, 4, true>(grid, threads, smem, stream, p, stages); break;
+        case (128 * 16 + 8) * 2 + 1: e0 = launch_split<128, 8, true>(grid, threads, smem, stream, p, stages); break;
+        case (128 * 16 + 4) * 2 + 1: e0 = launch_split<128, 4, true>(grid, threads, smem, stream, p, stages); break;
+        case (64 * 16 + 2) * 2 + 1: e0 = launch_split<64, 2, true>(grid, threads, smem, stream, p, stages); break;
+        case (128 * 16 + 2) * 2 + 1: e0 = launch_split<128, 2, true>(grid, threads, smem, stream, p, stages); break;
         default: return GDA_ERR_UNSUPPORTED;
     }
     if (e0 != cudaSuccess) return record_cuda_error(e0);

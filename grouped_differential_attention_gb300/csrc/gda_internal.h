@@ -32,6 +32,8 @@ struct DecodeArgs {
     void *workspace;
     size_t workspace_bytes;
     unsigned *dev_err;
+    int fp8 = 0;                                  // caches hold fp8 (e4m3) codes
+    const float *k1_scale = nullptr, *k2_scale = nullptr, *v_scale = nullptr;
 };
 
 // Remembers `e` as this thread's last CUDA error (see gda_last_cuda_error),

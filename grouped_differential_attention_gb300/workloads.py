@@ -143,6 +143,36 @@ def make_decode_inputs(w: DecodeWorkload, **overrides):
     return q1, q2, k1c, k2c, vc, lens, lam
 
 
+E4M3_MAX = 448.0   # largest finite float8 e4m3 value
+
+
+def quantize_e4m3_per_head(x: torch.Tensor):
+    """fp8 (e4m3) codes and per-head float32 scales of a cache [B, L, heads, dim].
+
+    scale_h = amax_h / 448 over the head's values (1.0 for an all-zero head);
+    codes = round-to-nearest e4m3 of x / scale_h.  The cached value a decode
+    sees is codes * scale_h.
+    """
+    xf = x.float()
+    amax = xf.abs().amax(dim=(0, 1, 3))
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).to(torch.float32)
+    codes = (xf / scale[None, None, :, None]).to(torch.float8_e4m3fn)
+    return codes, scale
+
+
+def make_decode_inputs_fp8(w: DecodeWorkload, **overrides):
+    """The decode inputs of make_decode_inputs with fp8 (e4m3) caches.
+
+    Returns (q1, q2, k1_codes, k2_codes, v_codes, k1_scale, k2_scale, v_scale,
+    lens, lam): the bf16 caches quantised per head by quantize_e4m3_per_head.
+    """
+    q1, q2, k1c, k2c, vc, lens, lam = make_decode_inputs(w, **overrides)
+    k1q, k1s = quantize_e4m3_per_head(k1c)
+    k2q, k2s = quantize_e4m3_per_head(k2c)
+    vq, vs = quantize_e4m3_per_head(vc)
+    return q1, q2, k1q, k2q, vq, k1s, k2s, vs, lens, lam
+
+
 def causal_pairs(L: int) -> int:
     """Number of (query, key <= query) pairs in one causal L x L map."""
     return L * (L + 1) // 2

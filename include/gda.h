@@ -149,6 +149,27 @@ int gda_attn_decode(const void *q_sig, const void *q_noise, const void *k_sig_ca
                     size_t workspace_bytes, gda_stream_t stream);
 
 /*
+ * Decode over an fp8 cache ("Hardware Implementations and Serving
+ * Considerations": low-bit KV cache quantisation on the serving path).
+ * Same operation, layouts and workspace as gda_attn_decode, except:
+ *   k_sig_cache, k_noise_cache, v_cache hold fp8 e4m3 codes (1 byte per
+ *   element, same [B, Lcap, heads, dim] layout, 16-byte aligned); the cached
+ *   value is code * scale of its head:
+ *   k_sig_scale [h_s], k_noise_scale [h_n], v_scale [h_s]: float32 device
+ *   arrays, 4-byte aligned.  Queries, lambda and the output stay as in
+ *   gda_attn_decode (bf16 q, float32 lambda, bf16 out).
+ * 2560 cache bytes per position for 12 + 4 heads, d = 64, dv = 128 (half of
+ * bf16).  Supported: d in {64, 128}; dv in {64, 128, 256}; h_s + h_n <= 128;
+ * 32 + up32((h_s + h_n) d / 16) + up32(h_s dv / 16) <= 1024.
+ */
+int gda_attn_decode_fp8(const void *q_sig, const void *q_noise, const void *k_sig_cache,
+                        const void *k_noise_cache, const void *v_cache, const float *k_sig_scale,
+                        const float *k_noise_scale, const float *v_scale, const int *cache_lens,
+                        const float *lambda, float lambda_init, void *out, int B, int Lcap, int h_s,
+                        int h_n, int d, int dv, float eps, void *workspace, size_t workspace_bytes,
+                        gda_stream_t stream);
+
+/*
  * Decode that allocates nothing and takes no workspace.  No counterpart on
  * the pages: it exists for callers that cannot allocate device memory, such
  * as a plugin or serving loop whose host framework owns all device memory in

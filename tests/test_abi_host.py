@@ -155,3 +155,24 @@ def test_lambda_reparam_rejects_bad_arguments(lib):
     assert lib.gda_lambda_reparam(*P, F(0.8), out, 12, 0, None) == INVALID
     assert lib.gda_lambda_reparam(*P, F(float("nan")), out, 12, 64, None) == INVALID
     assert lib.gda_lambda_reparam(ctypes.c_void_p(A + 2), *P[1:], F(0.8), out, 12, 64, None) == MISALIGNED
+
+
+def test_decode_fp8_rejects_bad_arguments(lib):
+    # every call below fails validation before any device work
+    F, Z = ctypes.c_float, ctypes.c_size_t
+    a = [ctypes.c_void_p(A)] * 10
+    ws = ctypes.c_void_p(A)
+    need = lib.gda_attn_decode_workspace_size(4, 256, 6, 2, 128)
+
+    def call(ptrs=None, B=4, Lcap=256, hs=6, hn=2, d=64, dv=128, ws_ptr=ws, ws_bytes=None):
+        p = ptrs or a
+        return lib.gda_attn_decode_fp8(*p, F(0.8), ctypes.c_void_p(A), B, Lcap, hs, hn, d, dv, F(1e-5),
+                                       ws_ptr, need if ws_bytes is None else ws_bytes, None)
+    assert call(ptrs=[None] + a[1:]) == INVALID
+    assert call(ptrs=a[:5] + [None] + a[6:]) == INVALID          # a missing scale array
+    assert call(hs=6, hn=4) == INVALID
+    assert call(d=96) == UNSUPPORTED
+    assert call(ptrs=a[:2] + [ctypes.c_void_p(A + 8)] + a[3:]) == MISALIGNED
+    assert call(ptrs=a[:6] + [ctypes.c_void_p(A + 2)] + a[7:]) == MISALIGNED   # scale not 4-byte aligned
+    assert call(ws_ptr=None) == WORKSPACE
+    assert call(ws_bytes=16) == WORKSPACE
