@@ -561,10 +561,12 @@ gda_decode_combine_kernel(const DecParams p) {
 
 template <int D, int P, bool F8>
 cudaError_t launch_split(dim3 grid, int threads, size_t smem, cudaStream_t stream, const DecParams &p, int stages) {
-    // up to 384 threads: two CTAs per SM with up to 80 registers a thread;
-    // else at most 64 registers (two CTAs of up to 512 threads, or one)
-    auto kern = threads <= 384 ? gda_decode_split_kernel<D, P, F8, 384, 2>
-                               : gda_decode_split_kernel<D, P, F8, 1024, 1>;
+    // up to 256 threads: three CTAs per SM with up to 85 registers a thread;
+    // up to 384: two with up to 80; else at most 64 registers (two CTAs of
+    // up to 512 threads, or one)
+    auto kern = threads <= 256   ? gda_decode_split_kernel<D, P, F8, 256, 3>
+                : threads <= 384 ? gda_decode_split_kernel<D, P, F8, 384, 2>
+                                 : gda_decode_split_kernel<D, P, F8, 1024, 1>;
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<grid, threads, smem, stream>>>(p, stages);
@@ -573,9 +575,9 @@ cudaError_t launch_split(dim3 grid, int threads, size_t smem, cudaStream_t strea
 
 }  // namespace
 
-// Upper bound on the split kernel's CTAs (two per SM on a 152-SM part); the
+// Upper bound on the split kernel's CTAs (three per SM on a 152-SM part); the
 // workspace holds one partial state per (CTA + sequence) slot.
-constexpr int kDecodeMaxCtas = 304;
+constexpr int kDecodeMaxCtas = 456;
 
 DecodePlan decode_plan(int B, int Lcap, int hs, int hn, int dv) {
     (void)Lcap;
@@ -631,13 +633,15 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     const size_t row_bytes = p.es * (static_cast<size_t>(a.hs) * a.d + static_cast<size_t>(a.hn) * a.d +
                                      static_cast<size_t>(a.hs) * a.dv);
     const int nheads = a.hs + a.hn;
-    // ring budget: two CTAs per SM fit in 228 KB when a CTA has at most 512
-    // threads, else one; the largest stage of 8, 4 or 2 positions of which
-    // at least four fit (a stage also holds its P weights and rescale factor
-    // per head)
-    const size_t budget = threads <= 512 ? 100 * 1024 : 200 * 1024;
+    // ring budget: three CTAs per SM when a CTA has at most 256 threads, two
+    // up to 512, else one (each with its static arrays within 228 KB); the
+    // largest stage of 8, 4 or 2 positions of which at least four fit (a
+    // stage also holds its P weights and rescale factor per head)
+    const int per_sm = threads <= 256 ? 3 : (threads <= 512 ? 2 : 1);
+    const size_t budget = per_sm == 3 ? 70 * 1024 : (per_sm == 2 ? 100 * 1024 : 200 * 1024);
     int P = 8;
-    while (P > 2 && (row_bytes * P + nheads * (P + 1) * 4) * 4 > budget) P /= 2;
+    const size_t min_stages = per_sm == 3 ? 3 : 4;
+    while (P > 2 && (row_bytes * P + nheads * (P + 1) * 4) * min_stages > budget) P /= 2;
     const size_t per_stage = row_bytes * P + static_cast<size_t>(nheads) * (P + 1) * 4;
     int stages = static_cast<int>(budget / per_stage);
     if (stages > kMaxStages) stages = kMaxStages;
@@ -647,7 +651,7 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     cudaError_t e1 = cudaGetDevice(&dev);
     if (e1 == cudaSuccess) e1 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e1 != cudaSuccess) return record_cuda_error(e1);
-    p.ctas = std::min(kDecodeMaxCtas, (threads <= 512 ? 2 : 1) * sms);
+    p.ctas = std::min(kDecodeMaxCtas, per_sm * sms);
     p.min_per_cta = 64;
     const dim3 grid(p.ctas);
     cudaError_t e0;
