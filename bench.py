@@ -337,6 +337,29 @@ def run_gda(args, world, rank, local):
     ev7.record(stream)
     torch.cuda.synchronize(dev)
     d8_ms_step = ev6.elapsed_time(ev7) / dec_steps
+    del d8
+
+    # ---- the same decode over paged caches (64-position pages, random page order)
+    page_size = 64
+    cpu_dec = W.make_decode_inputs(dw, seed=rank)
+    k1p, k2p, vp, table = W.page_caches(cpu_dec[2], cpu_dec[3], cpu_dec[4], page_size, seed=rank)
+    dpg = [t.to(dev) for t in (cpu_dec[0], cpu_dec[1], k1p, k2p, vp, table, cpu_dec[5], cpu_dec[6])]
+    del cpu_dec, k1p, k2p, vp
+
+    def dpstep():
+        gda.gda_attn_decode_paged(*dpg, dw.lambda_init, eps=dw.eps, out=dout, workspace=ws)
+
+    for _ in range(max(3, args.warmup // 4)):
+        dpstep()
+    torch.cuda.synchronize(dev)
+    ev8, ev9 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev8.record(stream)
+    for _ in range(dec_steps):
+        dpstep()
+    ev9.record(stream)
+    torch.cuda.synchronize(dev)
+    dp_ms_step = ev8.elapsed_time(ev9) / dec_steps
+    del dpg
 
     # ---- lambda re-parameterisation for one layer's heads (launch-latency bound)
     g = torch.Generator().manual_seed(rank + 11)
@@ -458,6 +481,12 @@ def run_gda(args, world, rank, local):
                        "roofline": {"bound": "hbm", "achieved": d8_bytes / (d8_ms_step * 1e-3) / 1e9,
                                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                     "frac": d8_bytes / (d8_ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"]}},
+        "decode_paged": {"workload": dw.name + f" with {page_size}-position pages in random pool order",
+                         "value": dec_bytes / (dp_ms_step * 1e-3) / 1e9, "unit": "GB/s",
+                         "ms_per_step": dp_ms_step, "steps": dec_steps, "bytes_per_step": dec_bytes,
+                         "roofline": {"bound": "hbm", "achieved": dec_bytes / (dp_ms_step * 1e-3) / 1e9,
+                                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                      "frac": dec_bytes / (dp_ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"]}},
         "lambda_reparam": {"workload": f"h_s={w.h_s} heads, d={w.d}", "us_per_call": lam_us,
                            "calls": lam_steps, "gpu_launches": lam_steps,
                            "bound": "host launch rate: back-to-back calls through the Python binding "

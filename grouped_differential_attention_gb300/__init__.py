@@ -42,6 +42,7 @@ GDA_FLAG_NO_NORM = 0x1
 GDA_DEVERR_PREFILL_TIMEOUT = 0x1
 GDA_DEVERR_BAD_LENGTH = 0x2
 GDA_DEVERR_DECODE_TIMEOUT = 0x4
+GDA_DEVERR_BAD_PAGE = 0x8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libgda.so")
@@ -88,6 +89,9 @@ def _load():
             lib.gda_attn_decode_fp8.argtypes = [P, P, P, P, P, P, P, P, P, P, F, P, I, I, I, I, I, I, F,
                                                 P, Z, P]
             lib.gda_attn_decode_fp8.restype = I
+            lib.gda_attn_decode_paged.argtypes = [P, P, P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, F,
+                                                  P, Z, P]
+            lib.gda_attn_decode_paged.restype = I
             lib.gda_lambda_reparam.argtypes = [P, P, P, P, F, P, I, I, P]
             lib.gda_lambda_reparam.restype = I
             lib.gda_device_error.argtypes = [I]
@@ -215,6 +219,47 @@ def gda_attn_decode_fp8(q_sig, q_noise, k_sig_cache, k_noise_cache, v_cache, k_s
             float(lambda_init), _ptr(out), B, Lcap, hs, hn, d, dv, float(eps), _ptr(workspace),
             workspace.numel() * workspace.element_size(), _stream(dev))
     _check(rc, "gda decode (fp8 cache)")
+    return out
+
+
+def gda_attn_decode_paged(q_sig, q_noise, k_sig_pool, k_noise_pool, v_pool, block_table, cache_lens,
+                          lam, lambda_init: float, *, eps: float = 1e-5, out=None, workspace=None):
+    """bf16 decode over paged caches.
+
+    Pools [num_pages, page_size, heads, dim] (bf16); block_table [B,
+    max_pages] int32: position j of sequence b is row j % page_size of page
+    block_table[b, j // page_size].
+    """
+    dev = q_sig.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, hs, d = q_sig.shape
+    hn = q_noise.shape[1]
+    num_pages, page_size = k_sig_pool.shape[0], k_sig_pool.shape[1]
+    dv = v_pool.shape[3]
+    max_pages = block_table.shape[1]
+    bf = torch.bfloat16
+    _expect(q_sig, "q_sig", bf, (B, hs, d), dev)
+    _expect(q_noise, "q_noise", bf, (B, hn, d), dev)
+    _expect(k_sig_pool, "k_sig_pool", bf, (num_pages, page_size, hs, d), dev)
+    _expect(k_noise_pool, "k_noise_pool", bf, (num_pages, page_size, hn, d), dev)
+    _expect(v_pool, "v_pool", bf, (num_pages, page_size, hs, dv), dev)
+    _expect(block_table, "block_table", torch.int32, (B, max_pages), dev)
+    _expect(cache_lens, "cache_lens", torch.int32, (B,), dev)
+    _expect(lam, "lam", torch.float32, (hs,), dev)
+    if out is None:
+        out = torch.empty((B, hs, dv), dtype=bf, device=dev)
+    _expect(out, "out", bf, (B, hs, dv), dev)
+    need = gda_attn_decode_workspace_size(B, max_pages * page_size, hs, hn, dv)
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = _load().gda_attn_decode_paged(
+            _ptr(q_sig), _ptr(q_noise), _ptr(k_sig_pool), _ptr(k_noise_pool), _ptr(v_pool),
+            _ptr(block_table), _ptr(cache_lens), _ptr(lam), float(lambda_init), _ptr(out), B,
+            max_pages, page_size, num_pages, hs, hn, d, dv, float(eps), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(dev))
+    _check(rc, "gda decode (paged caches)")
     return out
 
 

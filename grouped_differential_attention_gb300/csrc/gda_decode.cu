@@ -64,6 +64,11 @@ struct DecParams {
     int kc1, kc;       // chunk boundaries: K1 chunks [0,kc1), K2 [kc1,kc), V [kc, nchunks)
     int nchunks;
     int es;            // cache element bytes: 2 (bf16) or 1 (fp8 e4m3)
+    // paged caches: the caches are page pools [num_pages, page_size, heads,
+    // dim]; position j of sequence b is row j % page_size of page
+    // block_table[b * max_pages + j / page_size]
+    const int *block_table;   // nullptr: contiguous caches [B, Lcap, heads, dim]
+    int page_size, max_pages, num_pages;
 };
 
 __device__ __forceinline__ int clamp_len(int len, int Lcap, unsigned *err) {
@@ -135,7 +140,7 @@ __device__ __forceinline__ void issue_tile(const DecParams &p, Cursor &c, int st
     const int st = c.k % stages;
     uint8_t *sb = ring + static_cast<size_t>(st) * P * (rk1 + rk2 + rv);
     const size_t row0 = static_cast<size_t>(c.b) * p.Lcap + c.pos;
-    const int b = c.b;
+    const int b = c.b, pos0 = c.pos;
 
     // advance the cursor
     int flags = 0;
@@ -157,9 +162,29 @@ __device__ __forceinline__ void issue_tile(const DecParams &p, Cursor &c, int st
     info[st] = TileInfo{n, b, flags};
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // prior generic reads of the stage
     mbar_arrive_expect_tx(&full[st], n * (rk1 + rk2 + rv));          // releases info[st]
-    bulk_copy_g2s(sb, p.k1c + row0 * rk1, n * rk1, &full[st]);
-    bulk_copy_g2s(sb + P * rk1, p.k2c + row0 * rk2, n * rk2, &full[st]);
-    bulk_copy_g2s(sb + P * (rk1 + rk2), p.vc + row0 * rv, n * rv, &full[st]);
+    if (p.block_table == nullptr) {
+        bulk_copy_g2s(sb, p.k1c + row0 * rk1, n * rk1, &full[st]);
+        bulk_copy_g2s(sb + P * rk1, p.k2c + row0 * rk2, n * rk2, &full[st]);
+        bulk_copy_g2s(sb + P * (rk1 + rk2), p.vc + row0 * rv, n * rv, &full[st]);
+    } else {
+        // one run of rows per page the tile touches; a page id outside the
+        // pool is reported and read as page 0 instead
+        for (int i = 0; i < n;) {
+            const int pos = pos0 + i;
+            const int pg = pos / p.page_size, in_pg = pos % p.page_size;
+            const int run = min(n - i, p.page_size - in_pg);
+            int phys = p.block_table[static_cast<size_t>(b) * p.max_pages + pg];
+            if (phys < 0 || phys >= p.num_pages) {
+                atomicOr(p.err, GDA_DEVERR_BAD_PAGE);
+                phys = 0;
+            }
+            const size_t r0 = static_cast<size_t>(phys) * p.page_size + in_pg;
+            bulk_copy_g2s(sb + i * rk1, p.k1c + r0 * rk1, run * rk1, &full[st]);
+            bulk_copy_g2s(sb + P * rk1 + i * rk2, p.k2c + r0 * rk2, run * rk2, &full[st]);
+            bulk_copy_g2s(sb + P * (rk1 + rk2) + i * rv, p.vc + r0 * rv, run * rv, &full[st]);
+            i += run;
+        }
+    }
     ++c.k;
 }
 
@@ -598,6 +623,10 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     p.k1c = static_cast<const uint8_t *>(a.k1c);
     p.k2c = static_cast<const uint8_t *>(a.k2c);
     p.vc = static_cast<const uint8_t *>(a.vc);
+    p.block_table = a.block_table;
+    p.page_size = a.page_size;
+    p.max_pages = a.max_pages;
+    p.num_pages = a.num_pages;
     p.k1_scale = a.k1_scale;
     p.k2_scale = a.k2_scale;
     p.v_scale = a.v_scale;

@@ -33,6 +33,8 @@ struct DecodeArgs {
     size_t workspace_bytes;
     unsigned *dev_err;
     int fp8 = 0;                                  // caches hold fp8 (e4m3) codes
+    const int *block_table = nullptr;             // paged caches (see gda_attn_decode_paged)
+    int page_size = 0, max_pages = 0, num_pages = 0;
     const float *k1_scale = nullptr, *k2_scale = nullptr, *v_scale = nullptr;
 };
 

@@ -173,6 +173,29 @@ def make_decode_inputs_fp8(w: DecodeWorkload, **overrides):
     return q1, q2, k1q, k2q, vq, k1s, k2s, vs, lens, lam
 
 
+def page_caches(k1c, k2c, vc, page_size: int, seed: int = 0, spare_pages: int = 3):
+    """Scatter contiguous caches [B, Lcap, heads, dim] into page pools.
+
+    Lcap must be a multiple of page_size.  Returns (k1_pool, k2_pool, v_pool,
+    block_table): the sequences' pages go to a seeded random permutation of
+    the pool's pages (spare pages stay as noise), block_table[b, j] naming the
+    page that holds cache rows j*page_size .. (j+1)*page_size - 1 of b.
+    """
+    B, Lcap = k1c.shape[0], k1c.shape[1]
+    assert Lcap % page_size == 0
+    max_pages = Lcap // page_size
+    num_pages = B * max_pages + spare_pages
+    g = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=g)[:B * max_pages]
+    table = perm.view(B, max_pages).to(torch.int32)
+
+    def pool(c):
+        out = torch.randn((num_pages, page_size) + tuple(c.shape[2:]), generator=g).to(c.dtype)
+        out[perm] = c.reshape((B * max_pages, page_size) + tuple(c.shape[2:]))
+        return out
+    return pool(k1c), pool(k2c), pool(vc), table
+
+
 def causal_pairs(L: int) -> int:
     """Number of (query, key <= query) pairs in one causal L x L map."""
     return L * (L + 1) // 2

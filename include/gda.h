@@ -170,6 +170,27 @@ int gda_attn_decode_fp8(const void *q_sig, const void *q_noise, const void *k_si
                         gda_stream_t stream);
 
 /*
+ * Decode over paged caches (the paged KV layout of serving stacks; the pages
+ * put the KV cache on the serving path, "Hardware Implementations and
+ * Serving Considerations").  Same operation and result as gda_attn_decode;
+ * the caches are page pools shared by all sequences:
+ *   k_sig_pool [num_pages, page_size, h_s, d], k_noise_pool [num_pages,
+ *   page_size, h_n, d], v_pool [num_pages, page_size, h_s, dv]      bf16
+ *   block_table [B, max_pages] int32 device: cache position j of sequence b
+ *   is row j % page_size of page block_table[b][j / page_size]
+ *   cache_lens [B]: 1 <= cache_lens[b] <= max_pages * page_size
+ * Workspace: gda_attn_decode_workspace_size(B, max_pages * page_size, h_s,
+ * h_n, dv) bytes.  A block-table entry outside [0, num_pages) is read as page
+ * 0 and reported through gda_device_error (GDA_DEVERR_BAD_PAGE).  Supported
+ * sizes as gda_attn_decode; page_size >= 1.
+ */
+int gda_attn_decode_paged(const void *q_sig, const void *q_noise, const void *k_sig_pool,
+                          const void *k_noise_pool, const void *v_pool, const int *block_table,
+                          const int *cache_lens, const float *lambda, float lambda_init, void *out, int B,
+                          int max_pages, int page_size, int num_pages, int h_s, int h_n, int d, int dv,
+                          float eps, void *workspace, size_t workspace_bytes, gda_stream_t stream);
+
+/*
  * Decode that allocates nothing and takes no workspace.  No counterpart on
  * the pages: it exists for callers that cannot allocate device memory, such
  * as a plugin or serving loop whose host framework owns all device memory in
@@ -229,6 +250,7 @@ int gda_last_cuda_error(void);
 #define GDA_DEVERR_PREFILL_TIMEOUT 0x1u  /* a prefill pipeline wait ran out */
 #define GDA_DEVERR_BAD_LENGTH      0x2u  /* a decode cache length was outside [1, Lcap] */
 #define GDA_DEVERR_DECODE_TIMEOUT  0x4u  /* a decode cache-streaming wait ran out */
+#define GDA_DEVERR_BAD_PAGE        0x8u  /* a paged decode's block table named a page outside the pool */
 
 /*
  * Reads the error word of the current device (synchronises the device

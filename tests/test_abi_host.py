@@ -176,3 +176,25 @@ def test_decode_fp8_rejects_bad_arguments(lib):
     assert call(ptrs=a[:6] + [ctypes.c_void_p(A + 2)] + a[7:]) == MISALIGNED   # scale not 4-byte aligned
     assert call(ws_ptr=None) == WORKSPACE
     assert call(ws_bytes=16) == WORKSPACE
+
+
+def test_decode_paged_rejects_bad_arguments(lib):
+    # every call below fails validation before any device work
+    F = ctypes.c_float
+    a = [ctypes.c_void_p(A)] * 8
+    ws = ctypes.c_void_p(A)
+    need = lib.gda_attn_decode_workspace_size(4, 256, 6, 2, 128)
+
+    def call(ptrs=None, B=4, max_pages=8, page_size=32, num_pages=40, hs=6, hn=2, d=64, dv=128, ws_ptr=ws,
+             ws_bytes=None):
+        p = ptrs or a
+        return lib.gda_attn_decode_paged(*p, F(0.8), ctypes.c_void_p(A), B, max_pages, page_size, num_pages,
+                                         hs, hn, d, dv, F(1e-5), ws_ptr, need if ws_bytes is None else ws_bytes,
+                                         None)
+    assert call(ptrs=a[:5] + [None] + a[6:]) == INVALID           # no block table
+    assert call(page_size=0) == INVALID
+    assert call(num_pages=0) == INVALID
+    assert call(hs=6, hn=4) == INVALID
+    assert call(dv=96) == UNSUPPORTED
+    assert call(ptrs=a[:5] + [ctypes.c_void_p(A + 2)] + a[6:]) == MISALIGNED
+    assert call(ws_bytes=16) == WORKSPACE
