@@ -361,6 +361,30 @@ def run_gda(args, world, rank, local):
     dp_ms_step = ev8.elapsed_time(ev9) / dec_steps
     del dpg
 
+    # ---- chunked prefill: 512 new rows continuing a 7680-row cached prefix
+    ck_L, ck_Lk = 512, 8192
+    g = torch.Generator().manual_seed(rank + 21)
+    ck = [torch.randn(w.B, ck_L, w.h_s, w.d, generator=g).to(torch.bfloat16),
+          torch.randn(w.B, ck_Lk, w.h_s, w.d, generator=g).to(torch.bfloat16),
+          torch.randn(w.B, ck_L, w.h_n, w.d, generator=g).to(torch.bfloat16),
+          torch.randn(w.B, ck_Lk, w.h_n, w.d, generator=g).to(torch.bfloat16),
+          torch.randn(w.B, ck_Lk, w.h_s, w.dv, generator=g).to(torch.bfloat16)]
+    ck = [t.to(dev) for t in ck] + [sets[0][5]]
+    ck_out = torch.empty(w.B, ck_L, w.h_s, w.dv, dtype=torch.bfloat16, device=dev)
+    ck_flops = row_flops(w.B, range(ck_Lk - ck_L, ck_Lk), w.h_s, w.h_n, w.d, w.dv)
+    for _ in range(5):
+        gda.gda_attn_fwd_chunk(*ck, w.lambda_init, eps=w.eps, out=ck_out)
+    torch.cuda.synchronize(dev)
+    ck_steps = 50
+    eva, evb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    eva.record(stream)
+    for _ in range(ck_steps):
+        gda.gda_attn_fwd_chunk(*ck, w.lambda_init, eps=w.eps, out=ck_out)
+    evb.record(stream)
+    torch.cuda.synchronize(dev)
+    ck_ms = eva.elapsed_time(evb) / ck_steps
+    del ck
+
     # ---- lambda re-parameterisation for one layer's heads (launch-latency bound)
     g = torch.Generator().manual_seed(rank + 11)
     lvec = [(0.1 * torch.randn(w.h_s, w.d, generator=g)).to(dev) for _ in range(4)]
@@ -487,6 +511,13 @@ def run_gda(args, world, rank, local):
                          "roofline": {"bound": "hbm", "achieved": dec_bytes / (dp_ms_step * 1e-3) / 1e9,
                                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": dec_bytes / (dp_ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"]}},
+        "prefill_chunk": {"workload": f"B={w.B}, {ck_L} new rows after a {ck_Lk - ck_L}-row cached prefix, "
+                                      f"{w.h_s}+{w.h_n} heads, d={w.d}, dv={w.dv}",
+                          "value": ck_flops / (ck_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ck_ms,
+                          "steps": ck_steps,
+                          "roofline": {"bound": "tensor", "achieved": ck_flops / (ck_ms * 1e-3) / 1e12,
+                                       "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                       "frac": ck_flops / (ck_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}},
         "lambda_reparam": {"workload": f"h_s={w.h_s} heads, d={w.d}", "us_per_call": lam_us,
                            "calls": lam_steps, "gpu_launches": lam_steps,
                            "bound": "host launch rate: back-to-back calls through the Python binding "

@@ -92,6 +92,8 @@ def _load():
             lib.gda_attn_decode_paged.argtypes = [P, P, P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, F,
                                                   P, Z, P]
             lib.gda_attn_decode_paged.restype = I
+            lib.gda_attn_fwd_chunk.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, F, U, P]
+            lib.gda_attn_fwd_chunk.restype = I
             lib.gda_lambda_reparam.argtypes = [P, P, P, P, F, P, I, I, P]
             lib.gda_lambda_reparam.restype = I
             lib.gda_device_error.argtypes = [I]
@@ -166,6 +168,38 @@ def gda_attn_fwd(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float, *,
     """bf16 prefill on the tensor cores (tcgen05/TMEM, TMA); returns ``out``."""
     return _prefill(_load().gda_attn_fwd_ex, torch.bfloat16, q_sig, k_sig, q_noise, k_noise, v,
                     lam, lambda_init, causal, eps, out, flags)
+
+
+def gda_attn_fwd_chunk(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float, *,
+                       causal: bool = True, eps: float = 1e-5, out=None, flags: int = 0):
+    """Chunked bf16 prefill: L query rows at key positions Lk - L .. Lk - 1.
+
+    q_sig [B, L, h_s, d], q_noise [B, L, h_n, d]; k_sig [B, Lk, h_s, d],
+    k_noise [B, Lk, h_n, d], v [B, Lk, h_s, dv]; returns out [B, L, h_s, dv].
+    """
+    dev = q_sig.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, L, hs, d = q_sig.shape
+    hn = q_noise.shape[2]
+    Lk = k_sig.shape[1]
+    dv = v.shape[3]
+    bf = torch.bfloat16
+    _expect(q_sig, "q_sig", bf, (B, L, hs, d), dev)
+    _expect(k_sig, "k_sig", bf, (B, Lk, hs, d), dev)
+    _expect(q_noise, "q_noise", bf, (B, L, hn, d), dev)
+    _expect(k_noise, "k_noise", bf, (B, Lk, hn, d), dev)
+    _expect(v, "v", bf, (B, Lk, hs, dv), dev)
+    _expect(lam, "lam", torch.float32, (hs,), dev)
+    if out is None:
+        out = torch.empty((B, L, hs, dv), dtype=bf, device=dev)
+    _expect(out, "out", bf, (B, L, hs, dv), dev)
+    with torch.cuda.device(dev):
+        rc = _load().gda_attn_fwd_chunk(_ptr(q_sig), _ptr(k_sig), _ptr(q_noise), _ptr(k_noise), _ptr(v),
+                                        _ptr(lam), float(lambda_init), _ptr(out), B, L, Lk, hs, hn, d, dv,
+                                        int(bool(causal)), float(eps), int(flags), _stream(dev))
+    _check(rc, "gda chunked prefill")
+    return out
 
 
 def gda_attn_fwd_f32(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float, *,

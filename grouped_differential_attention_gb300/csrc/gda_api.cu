@@ -142,6 +142,26 @@ int gda_attn_fwd_ex(const void *q_sig, const void *k_sig, const void *q_noise, c
     return launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int gda_attn_fwd_chunk(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,
+                       const void *v, const float *lambda, float lambda_init, void *out, int B, int L,
+                       int Lk, int h_s, int h_n, int d, int dv, int causal, float eps, unsigned flags,
+                       gda_stream_t stream) {
+    int st = check_prefill_common(q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L,
+                                  h_s, h_n, d, dv, causal, eps, flags);
+    if (st != GDA_OK) return st;
+    if (Lk < 1 || (causal && Lk < L)) return GDA_ERR_INVALID_ARG;
+    if (static_cast<double>(B) * Lk * (h_s > h_n ? h_s : h_n) * (d > dv ? d : dv) > 9.0e15)
+        return GDA_ERR_INVALID_ARG;
+    if (!(d == 64 || d == 128) || !(dv == 128 || dv == 256)) return GDA_ERR_UNSUPPORTED;
+    unsigned *err = nullptr;
+    st = current_device(&err);
+    if (st != GDA_OK) return st;
+    PrefillArgs a{q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L, h_s, h_n,
+                  d, dv, causal, eps, flags, err};
+    a.Lk = Lk;
+    return launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int gda_attn_fwd(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,
                  const void *v, const float *lambda, float lambda_init, void *out, int B, int L,
                  int h_s, int h_n, int d, int dv, int causal, float eps, gda_stream_t stream) {

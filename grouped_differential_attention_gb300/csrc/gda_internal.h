@@ -19,6 +19,7 @@ struct PrefillArgs {
     float eps;
     unsigned flags;
     unsigned *dev_err;                  // device error word of the current device
+    int Lk = 0;                         // keys per sequence (0: L); query row i is key position Lk - L + i
 };
 
 struct DecodeArgs {

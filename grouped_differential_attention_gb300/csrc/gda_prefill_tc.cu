@@ -109,6 +109,7 @@ struct TcParams {
     unsigned *err;
     float lambda_init, eps, scale_log2;
     int B, L, hs, hn, dv, causal, nslices, nqt, no_norm;
+    int Lk, koff;      // keys per sequence; query row i sits at key position koff + i (koff = Lk - L)
 };
 
 // Work item = (query tile, batch, signal head); item 0 is the longest (last
@@ -131,7 +132,7 @@ __device__ __forceinline__ bool item_of(const TcParams &p, int r, int G, int cid
     it.h = rem % p.hs;
     it.g = it.h / (p.hs / p.hn);
     it.q0 = qt * kBM;
-    const int kv_end = p.causal ? min(p.L, it.q0 + kBM) : p.L;
+    const int kv_end = p.causal ? min(p.Lk, p.koff + it.q0 + kBM) : p.Lk;
     it.nkv = (kv_end + bn - 1) / bn;
     return true;
 }
@@ -364,7 +365,7 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
         for (int r = 0; item_of(p, r, G, cid, BN, it); ++r) {
             const int nkv = it.nkv;
             const int qrow = it.q0 + row;
-            const int last_key = p.causal ? min(qrow, p.L - 1) : p.L - 1;
+            const int last_key = p.causal ? min(p.koff + qrow, p.Lk - 1) : p.Lk - 1;
             const float lam = p.lambda[it.h];     // loaded now, used by the epilogue
             float m_ref = -INFINITY;
             float l = 0.f;
@@ -388,7 +389,7 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                 const uint32_t gs = gt + j;
                 const uint32_t tS = tSm + (gs & 1) * BN;
                 const int k0 = j * BN;
-                const bool need_mask = (p.causal && k0 + BN - 1 > it.q0) || (k0 + BN > p.L);
+                const bool need_mask = (p.causal && k0 + BN - 1 > p.koff + it.q0) || (k0 + BN > p.Lk);
                 if (need_mask) {
 #pragma unroll
                     for (int e = 0; e < BN; ++e)
@@ -638,31 +639,34 @@ template <int D>
 int launch_impl(const PrefillArgs &a, cudaStream_t stream) {
     using LY = Layout<D>;
     CUtensorMap mQ1, mK1, mQ2, mK2, mV, mO;
-    const uint64_t B = a.B, L = a.L, hs = a.hs, hn = a.hn, d = a.d, dv = a.dv;
+    // queries and output: L rows; keys and values: Lk rows
+    const uint64_t B = a.B, L = a.L, Lk = a.Lk > 0 ? a.Lk : a.L, hs = a.hs, hn = a.hn, d = a.d, dv = a.dv;
     {
-        const uint64_t dims[4] = {d, hs, L, B};
-        const uint64_t str[3] = {d * 2, hs * d * 2, L * hs * d * 2};
+        const uint64_t dq[4] = {d, hs, L, B}, dk[4] = {d, hs, Lk, B};
+        const uint64_t sq[3] = {d * 2, hs * d * 2, L * hs * d * 2}, sk[3] = {d * 2, hs * d * 2, Lk * hs * d * 2};
         const uint32_t boxq[4] = {64, 1, kBM, 1};
         const uint32_t boxk[4] = {64, 1, (uint32_t)LY::BN, 1};
-        if (!encode_tmap_4d_bf16(&mQ1, a.q1, dims, str, boxq)) return GDA_ERR_CUDA;
-        if (!encode_tmap_4d_bf16(&mK1, a.k1, dims, str, boxk)) return GDA_ERR_CUDA;
+        if (!encode_tmap_4d_bf16(&mQ1, a.q1, dq, sq, boxq)) return GDA_ERR_CUDA;
+        if (!encode_tmap_4d_bf16(&mK1, a.k1, dk, sk, boxk)) return GDA_ERR_CUDA;
     }
     {
-        const uint64_t dims[4] = {d, hn, L, B};
-        const uint64_t str[3] = {d * 2, hn * d * 2, L * hn * d * 2};
+        const uint64_t dq[4] = {d, hn, L, B}, dk[4] = {d, hn, Lk, B};
+        const uint64_t sq[3] = {d * 2, hn * d * 2, L * hn * d * 2}, sk[3] = {d * 2, hn * d * 2, Lk * hn * d * 2};
         const uint32_t boxq[4] = {64, 1, kBM, 1};
         const uint32_t boxk[4] = {64, 1, (uint32_t)LY::BN, 1};
-        if (!encode_tmap_4d_bf16(&mQ2, a.q2, dims, str, boxq)) return GDA_ERR_CUDA;
-        if (!encode_tmap_4d_bf16(&mK2, a.k2, dims, str, boxk)) return GDA_ERR_CUDA;
+        if (!encode_tmap_4d_bf16(&mQ2, a.q2, dq, sq, boxq)) return GDA_ERR_CUDA;
+        if (!encode_tmap_4d_bf16(&mK2, a.k2, dk, sk, boxk)) return GDA_ERR_CUDA;
     }
     {
-        const uint64_t dims[4] = {dv, hs, L, B};
-        const uint64_t str[3] = {dv * 2, hs * dv * 2, L * hs * dv * 2};
+        const uint64_t dk[4] = {dv, hs, Lk, B};
+        const uint64_t sk[3] = {dv * 2, hs * dv * 2, Lk * hs * dv * 2};
         const uint32_t box[4] = {64, 1, (uint32_t)LY::BN, 1};
-        if (!encode_tmap_4d_bf16(&mV, a.v, dims, str, box)) return GDA_ERR_CUDA;
+        if (!encode_tmap_4d_bf16(&mV, a.v, dk, sk, box)) return GDA_ERR_CUDA;
         // output: 32 query rows x 64 columns of one head per store
+        const uint64_t dq[4] = {dv, hs, L, B};
+        const uint64_t sq[3] = {dv * 2, hs * dv * 2, L * hs * dv * 2};
         const uint32_t boxo[4] = {64, 1, 32, 1};
-        if (!encode_tmap_4d_bf16(&mO, a.out, dims, str, boxo)) return GDA_ERR_CUDA;
+        if (!encode_tmap_4d_bf16(&mO, a.out, dq, sq, boxo)) return GDA_ERR_CUDA;
     }
     TcParams p;
     p.lambda = a.lambda;
@@ -673,6 +677,8 @@ int launch_impl(const PrefillArgs &a, cudaStream_t stream) {
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.d)));
     p.B = a.B;
     p.L = a.L;
+    p.Lk = static_cast<int>(Lk);
+    p.koff = static_cast<int>(Lk) - a.L;
     p.hs = a.hs;
     p.hn = a.hn;
     p.dv = a.dv;

@@ -86,6 +86,24 @@ int gda_attn_fwd(const void *q_sig, const void *k_sig, const void *q_noise,
                  float lambda_init, void *out, int B, int L, int h_s, int h_n,
                  int d, int dv, int causal, float eps, gda_stream_t stream);
 
+/*
+ * Chunked prefill: L new query rows continuing a sequence whose keys and
+ * values (the cached prefix plus the chunk itself) are Lk >= L rows long.
+ * Query row i sits at key position Lk - L + i and, when causal, attends keys
+ * 0 .. Lk - L + i; non-causal, all Lk keys.  The result equals the last L
+ * rows of gda_attn_fwd over the whole Lk-row sequence.  (Prefill that
+ * continues from a cache is on the serving path of "Hardware Implementations
+ * and Serving Considerations".)
+ *   q_sig [B, L, h_s, d], q_noise [B, L, h_n, d], out [B, L, h_s, dv];
+ *   k_sig [B, Lk, h_s, d], k_noise [B, Lk, h_n, d], v [B, Lk, h_s, dv].
+ * Other arguments, flags, support and errors as gda_attn_fwd_ex;
+ * GDA_ERR_INVALID_ARG also for Lk < 1 or (causal and Lk < L).
+ */
+int gda_attn_fwd_chunk(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,
+                       const void *v, const float *lambda, float lambda_init, void *out, int B, int L,
+                       int Lk, int h_s, int h_n, int d, int dv, int causal, float eps, unsigned flags,
+                       gda_stream_t stream);
+
 /* gda_attn_fwd with flags (GDA_FLAG_NO_NORM). */
 int gda_attn_fwd_ex(const void *q_sig, const void *k_sig, const void *q_noise,
                     const void *k_noise, const void *v, const float *lambda,

@@ -198,3 +198,18 @@ def test_decode_paged_rejects_bad_arguments(lib):
     assert call(dv=96) == UNSUPPORTED
     assert call(ptrs=a[:5] + [ctypes.c_void_p(A + 2)] + a[6:]) == MISALIGNED
     assert call(ws_bytes=16) == WORKSPACE
+
+
+def test_chunked_prefill_rejects_bad_arguments(lib):
+    # every call below fails validation before any device work
+    F, U = ctypes.c_float, ctypes.c_uint
+    P = [ctypes.c_void_p(A)] * 6
+
+    def call(L=128, Lk=512, causal=1, hs=6, hn=2, d=64, dv=128):
+        return lib.gda_attn_fwd_chunk(*P, F(0.8), ctypes.c_void_p(A), 2, L, Lk, hs, hn, d, dv, causal,
+                                      F(1e-5), U(0), None)
+    assert call(Lk=0) == INVALID
+    assert call(L=128, Lk=100) == INVALID            # causal chunk longer than its sequence
+    assert call(hs=6, hn=4) == INVALID
+    assert call(d=96) == UNSUPPORTED
+    assert call(dv=64) == UNSUPPORTED
