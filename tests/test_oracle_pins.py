@@ -326,3 +326,61 @@ def test_dense_decode_scales_equal_prescaled_caches(oracle_mod):
     pre = ref_numpy.gda_decode_dense(q1, q2, k1, k2, v, lens, lam, 0.8, norm=False, v_scale=sv)
     base = ref_numpy.gda_decode_dense(q1, q2, k1, k2, v, lens, lam, 0.8, norm=False)
     assert np.allclose(pre, base * sv.double().numpy()[None, :, None], rtol=1e-13, atol=1e-14)
+
+
+# ------------------------------------------------------------- gradients
+from oracle import ref_torch_grad
+
+
+def _grad_case(seed, B=1, L=5, hs=4, hn=2, d=4, dv=6):
+    g = torch.Generator().manual_seed(seed)
+    t = lambda *shape: torch.randn(*shape, generator=g, dtype=torch.float64)
+    return (t(B, L, hs, d), t(B, L, hs, d), t(B, L, hn, d), t(B, L, hn, d), t(B, L, hs, dv),
+            torch.rand(hs, generator=g, dtype=torch.float64) * 0.6 + 0.2, t(B, L, hs, dv))
+
+
+def test_torch_forward_matches_numpy_dense():
+    q1, k1, q2, k2, v, lam, _ = _grad_case(31, B=2, L=7)
+    for causal in (True, False):
+        got = ref_torch_grad.gda_forward_torch(q1, k1, q2, k2, v, lam, 0.8, causal=causal).numpy()
+        want = ref_numpy.gda_dense(q1, k1, q2, k2, v, lam, 0.8, causal=causal)
+        assert np.allclose(got, want, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal,norm", [(True, True), (False, True), (True, False)])
+def test_backward_matches_central_finite_differences(causal, norm):
+    """d/dx sum(dy * y) against (f(x + h) - f(x - h)) / 2h, coordinate by coordinate."""
+    inputs = _grad_case(32)
+    *fwd_in, dy = inputs
+    grads = ref_torch_grad.gda_backward(*fwd_in, 0.8, dy, causal=causal, norm=norm)
+
+    def f(args):
+        y = ref_torch_grad.gda_forward_torch(*args, 0.8, causal=causal, norm=norm)
+        return float((y * dy).sum())
+    h = 1e-6
+    for which in range(6):
+        base = [t.clone() for t in fwd_in]
+        flat = base[which].view(-1)
+        for k in range(0, flat.numel(), max(1, flat.numel() // 7)):
+            orig = float(flat[k])
+            flat[k] = orig + h
+            fp = f(base)
+            flat[k] = orig - h
+            fm = f(base)
+            flat[k] = orig
+            fd = (fp - fm) / (2 * h)
+            an = float(grads[which].reshape(-1)[k])
+            assert abs(fd - an) <= 1e-6 * (1 + abs(an)), (which, k, fd, an)
+
+
+def test_noise_gradient_collects_the_whole_group():
+    """dK2 of a noise head equals the sum over its signal heads of the per-head terms:
+    with explicit repetition (h_n = h_s, K2 repeated) the repeated copies' gradients sum to it."""
+    q1, k1, q2, k2, v, lam, dy = _grad_case(33, hs=4, hn=2)
+    grads = ref_torch_grad.gda_backward(q1, k1, q2, k2, v, lam, 0.8, dy)
+    q2r, k2r = q2.repeat_interleave(2, dim=2), k2.repeat_interleave(2, dim=2)
+    rep = ref_torch_grad.gda_backward(q1, k1, q2r, k2r, v, lam, 0.8, dy)
+    assert torch.allclose(grads[2], rep[2].view(1, 5, 2, 2, 4).sum(3), atol=1e-12)
+    assert torch.allclose(grads[3], rep[3].view(1, 5, 2, 2, 4).sum(3), atol=1e-12)
+    for i in (0, 1, 4, 5):
+        assert torch.allclose(grads[i], rep[i], atol=1e-12)
