@@ -65,6 +65,19 @@ def row_flops(B, rows, hs, hn, d, dv):
     return sum(B * (i + 1) * (2 * d * (hs + hn) + 4 * dv * hs) for i in rows)
 
 
+def backward_flops(B, L, hs, hn, d, dv):
+    """Algorithmic flops of the backward over the causal pairs: the two logit
+    maps (2d per signal and per noise head), dA = dO . v and dV (4dv per
+    signal head), dq_sig and dk_sig (4d per signal head), dq_noise and
+    dk_noise after summing the group's score gradients (4d per noise head)."""
+    pairs = B * L * (L + 1) // 2
+    return pairs * (2 * d * (hs + hn) + 4 * dv * hs + 4 * d * hs + 4 * d * hn)
+
+
+# float32 FMA throughput of the CUDA cores: 152 SMs x 128 lanes x 2 flops x 2.07 GHz
+FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
 def decode_bytes(lens, hs, hn, d, dv):
     return int(sum(int(n) for n in lens)) * 2 * (hs * d + hn * d + hs * dv)
 
@@ -385,6 +398,32 @@ def run_gda(args, world, rank, local):
     ck_ms = eva.elapsed_time(evb) / ck_steps
     del ck
 
+    # ---- float32 backward (gradients of all six inputs) at the prefill workload's sizes
+    bw_in = [t.to(dev) for t in W.make_backward_inputs(w, dtype="f32", seed=rank + 31)]
+    bw_ws = torch.empty(gda.gda_attn_bwd_workspace_size(w.B, w.L, w.h_s, w.d, w.dv), dtype=torch.uint8,
+                        device=dev)
+    bw_grads = None
+
+    def bwstep():
+        return gda.gda_attn_bwd(*bw_in[:6], w.lambda_init, bw_in[6], causal=w.causal, eps=w.eps,
+                                workspace=bw_ws, grads=bw_grads)
+
+    bw_grads = bwstep()
+    for _ in range(3):
+        bwstep()
+    torch.cuda.synchronize(dev)
+    bw_steps = 10
+    evc, evd = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evc.record(stream)
+    for _ in range(bw_steps):
+        bwstep()
+    evd.record(stream)
+    torch.cuda.synchronize(dev)
+    bw_ms = evc.elapsed_time(evd) / bw_steps
+    bw_flops = backward_flops(w.B, w.L, w.h_s, w.h_n, w.d, w.dv)
+    bw_tflops = bw_flops / (bw_ms * 1e-3) / 1e12
+    del bw_in, bw_ws, bw_grads
+
     # ---- lambda re-parameterisation for one layer's heads (launch-latency bound)
     g = torch.Generator().manual_seed(rank + 11)
     lvec = [(0.1 * torch.randn(w.h_s, w.d, generator=g)).to(dev) for _ in range(4)]
@@ -518,6 +557,13 @@ def run_gda(args, world, rank, local):
                           "roofline": {"bound": "tensor", "achieved": ck_flops / (ck_ms * 1e-3) / 1e12,
                                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                        "frac": ck_flops / (ck_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}},
+        "backward_f32": {"workload": f"float32 gradients of q_sig, k_sig, q_noise, k_noise, v, lambda at "
+                                     f"B={w.B}, L={w.L}, {w.h_s}+{w.h_n} heads, d={w.d}, dv={w.dv}, causal",
+                         "value": bw_tflops, "unit": "TFLOP/s", "ms_per_step": bw_ms, "steps": bw_steps,
+                         "gpu_launches": 3 * bw_steps,
+                         "roofline": {"bound": "alu", "achieved": bw_tflops, "peak": FP32_SIMT_TFLOPS,
+                                      "unit": "TFLOP/s", "frac": bw_tflops / FP32_SIMT_TFLOPS,
+                                      "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz"}},
         "lambda_reparam": {"workload": f"h_s={w.h_s} heads, d={w.d}", "us_per_call": lam_us,
                            "calls": lam_steps, "gpu_launches": lam_steps,
                            "bound": "host launch rate: back-to-back calls through the Python binding "

@@ -29,6 +29,7 @@ __all__ = [
     "GDAError", "gda_attn_fwd", "gda_attn_fwd_f32", "gda_attn_decode",
     "gda_attn_decode_workspace_size", "gda_status_string", "gda_device_error",
     "lambda_init_schedule", "library_path", "GDA_FLAG_NO_NORM", "gda_attn_decode_noalloc",
+    "gda_attn_bwd", "gda_attn_bwd_workspace_size",
 ]
 
 GDA_OK = 0
@@ -96,6 +97,11 @@ def _load():
             lib.gda_attn_fwd_chunk.restype = I
             lib.gda_lambda_reparam.argtypes = [P, P, P, P, F, P, I, I, P]
             lib.gda_lambda_reparam.restype = I
+            lib.gda_attn_bwd.argtypes = [P, P, P, P, P, P, F, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
+                                         U, P, Z, P]
+            lib.gda_attn_bwd.restype = I
+            lib.gda_attn_bwd_workspace_size.argtypes = [I, I, I, I, I]
+            lib.gda_attn_bwd_workspace_size.restype = Z
             lib.gda_device_error.argtypes = [I]
             lib.gda_last_cuda_error.argtypes = []
             lib.gda_last_cuda_error.restype = I
@@ -295,6 +301,48 @@ def gda_attn_decode_paged(q_sig, q_noise, k_sig_pool, k_noise_pool, v_pool, bloc
             workspace.numel() * workspace.element_size(), _stream(dev))
     _check(rc, "gda decode (paged caches)")
     return out
+
+
+def gda_attn_bwd_workspace_size(B: int, L: int, h_s: int, d: int, dv: int) -> int:
+    return int(_load().gda_attn_bwd_workspace_size(B, L, h_s, d, dv))
+
+
+def gda_attn_bwd(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float, dy, *,
+                 causal: bool = True, eps: float = 1e-5, flags: int = 0, workspace=None, grads=None):
+    """float32 gradients of the operation; returns (dq_sig, dk_sig, dq_noise, dk_noise, dv, dlambda).
+
+    Inputs as for ``gda_attn_fwd_f32`` plus ``dy`` [B, L, h_s, dv] (the
+    gradient of the loss with respect to the output).  ``grads`` may hold the
+    six output tensors to overwrite.
+    """
+    dev = q_sig.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if q_sig.dim() != 4 or q_noise.dim() != 4 or v.dim() != 4:
+        raise ValueError("q_sig, q_noise and v must be 4-D [B, L, heads, dim]")
+    f32 = torch.float32
+    B, L, hs, d = q_sig.shape
+    hn = q_noise.shape[2]
+    dv = v.shape[3]
+    shapes = ((B, L, hs, d), (B, L, hs, d), (B, L, hn, d), (B, L, hn, d), (B, L, hs, dv), (hs,))
+    for t, name, shape in zip((q_sig, k_sig, q_noise, k_noise, v, lam), ("q_sig", "k_sig", "q_noise",
+                              "k_noise", "v", "lam"), shapes):
+        _expect(t, name, f32, shape, dev)
+    _expect(dy, "dy", f32, (B, L, hs, dv), dev)
+    if grads is None:
+        grads = tuple(torch.empty(s, dtype=f32, device=dev) for s in shapes)
+    for t, name, shape in zip(grads, ("dq_sig", "dk_sig", "dq_noise", "dk_noise", "dv", "dlambda"), shapes):
+        _expect(t, name, f32, shape, dev)
+    need = gda_attn_bwd_workspace_size(B, L, hs, d, dv)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = _load().gda_attn_bwd(
+            _ptr(q_sig), _ptr(k_sig), _ptr(q_noise), _ptr(k_noise), _ptr(v), _ptr(lam),
+            float(lambda_init), _ptr(dy), *[_ptr(t) for t in grads], B, L, hs, hn, d, dv,
+            int(bool(causal)), float(eps), int(flags), _ptr(workspace), workspace.numel(), _stream(dev))
+    _check(rc, "gda backward")
+    return tuple(grads)
 
 
 def gda_lambda_reparam(lambda_q1, lambda_k1, lambda_q2, lambda_k2, lambda_init: float, *, out=None):

@@ -39,6 +39,17 @@ struct DecodeArgs {
     const float *k1_scale = nullptr, *k2_scale = nullptr, *v_scale = nullptr;
 };
 
+struct BackwardArgs {
+    const float *q1, *k1, *q2, *k2, *v, *lambda, *dy;   // float32, layouts of gda_attn_fwd
+    float lambda_init;
+    float *dq1, *dk1, *dq2, *dk2, *dv_out, *dlambda;
+    int B, L, hs, hn, d, dv;
+    int causal;
+    float eps;
+    unsigned flags;
+    void *workspace;
+};
+
 // Remembers `e` as this thread's last CUDA error (see gda_last_cuda_error),
 // clears the runtime's sticky-free error state and returns GDA_ERR_CUDA.
 int record_cuda_error(cudaError_t e);
@@ -52,6 +63,8 @@ int device_state(unsigned **err_word);
 int launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
 int launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream);
 int launch_decode(const DecodeArgs &a, cudaStream_t stream);
+int launch_backward_f32(const BackwardArgs &a, cudaStream_t stream);
+size_t backward_f32_workspace_bytes(int B, int L, int hs, int d, int dv);
 int launch_lambda_reparam(const float *lq1, const float *lk1, const float *lq2, const float *lk2,
                           float lambda_init, float *out, int hs, int d, cudaStream_t stream);
 

@@ -118,6 +118,18 @@ def make_prefill_inputs(w: PrefillWorkload, **overrides):
     return (q1.to(dt), k1.to(dt), q2.to(dt), k2.to(dt), v.to(dt), lam.to(torch.float32))
 
 
+def make_backward_inputs(w: PrefillWorkload, **overrides):
+    """Draw (q1, k1, q2, k2, v, lam, dy) on the CPU: the prefill inputs of
+    ``make_prefill_inputs`` plus an upstream gradient dy [B, L, h_s, dv]
+    drawn from N(0, 1) with a generator seeded by seed + 1.
+    """
+    p = dataclasses.replace(w, **overrides) if overrides else w
+    inputs = make_prefill_inputs(p)
+    g = torch.Generator().manual_seed(p.seed + 1)
+    dy = torch.randn(p.B, p.L, p.h_s, p.dv, generator=g).to(_io_dtype(p.dtype))
+    return inputs + (dy,)
+
+
 def make_decode_inputs(w: DecodeWorkload, **overrides):
     """Draw (q1, q2, k1_cache, k2_cache, v_cache, lens, lam) on the CPU (bf16 I/O).
 

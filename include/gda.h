@@ -129,6 +129,41 @@ int gda_attn_fwd_f32_ex(const float *q_sig, const float *k_sig, const float *q_n
                         gda_stream_t stream);
 
 /*
+ * Backward (gradients) of the float32 operation above: given dy = dL/dy
+ * (dL/do with GDA_FLAG_NO_NORM), the gradients of L with respect to the
+ * signal and noise projections, the values and lambda.  Chain rule through
+ * the two softmax maps (Differential Transformer, section "Differential
+ * Attention"), the shared noise heads of a group (Grouped Differential
+ * Attention, abstract and method: dq_noise and dk_noise sum over the h_s/h_n
+ * signal heads that read each noise head) and the headwise RMSNorm (section
+ * "Headwise Normalization", scale 1 - lambda_init, no learned gain).
+ *   Inputs: the float32 tensors of gda_attn_fwd_f32 plus dy [B, L, h_s, dv].
+ *   Outputs (float32 device, overwritten, no accumulation into them):
+ *     dq_sig, dk_sig [B, L, h_s, d]; dq_noise, dk_noise [B, L, h_n, d];
+ *     dv_out [B, L, h_s, dv]; dlambda [h_s] (summed over batch and rows).
+ *   Supported: d in {64, 128}, dv in {64, 128, 256}.
+ *   workspace: device memory of at least gda_attn_bwd_workspace_size(B, L,
+ *   h_s, d, dv) bytes, 16-byte aligned, owned by the caller, not read across
+ *   calls (holds each row's softmax statistics, dL/do and per-signal-head
+ *   shares of the noise gradients).
+ *   The forward is recomputed from the inputs (no forward state is passed).
+ *   Results are deterministic (fixed summation orders).
+ *   Returns GDA_OK, GDA_ERR_INVALID_ARG, GDA_ERR_UNSUPPORTED,
+ *   GDA_ERR_MISALIGNED, GDA_ERR_WORKSPACE or GDA_ERR_CUDA; all argument
+ *   checks run before any device work.
+ */
+int gda_attn_bwd(const float *q_sig, const float *k_sig, const float *q_noise,
+                 const float *k_noise, const float *v, const float *lambda,
+                 float lambda_init, const float *dy, float *dq_sig, float *dk_sig,
+                 float *dq_noise, float *dk_noise, float *dv_out, float *dlambda,
+                 int B, int L, int h_s, int h_n, int d, int dv, int causal,
+                 float eps, unsigned flags, void *workspace,
+                 size_t workspace_bytes, gda_stream_t stream);
+
+/* Bytes of workspace gda_attn_bwd needs (0 for invalid sizes). */
+size_t gda_attn_bwd_workspace_size(int B, int L, int h_s, int d, int dv);
+
+/*
  * Bytes of device workspace gda_attn_decode needs for these sizes (it holds
  * the partial softmax states of the cache segments that the split kernel's
  * CTAs produce; the size does not depend on Lcap).  Returns 0 for invalid

@@ -213,3 +213,38 @@ def test_chunked_prefill_rejects_bad_arguments(lib):
     assert call(hs=6, hn=4) == INVALID
     assert call(d=96) == UNSUPPORTED
     assert call(dv=64) == UNSUPPORTED
+
+
+def test_backward_workspace_size(lib):
+    assert lib.gda_attn_bwd_workspace_size(0, 128, 6, 64, 128) == 0
+    assert lib.gda_attn_bwd_workspace_size(2, 128, 6, 64, -1) == 0
+    small = lib.gda_attn_bwd_workspace_size(2, 128, 6, 64, 128)
+    big = lib.gda_attn_bwd_workspace_size(2, 256, 6, 64, 128)
+    # per (b, row, signal head): 6 statistics, dv of dL/do, 2 d of noise-gradient shares, 1 dlambda term
+    assert small >= 4 * 2 * 128 * 6 * (6 + 128 + 2 * 64 + 1)
+    assert big > small
+
+
+def test_backward_rejects_bad_arguments(lib):
+    # every call below fails validation before any device work
+    F, U = ctypes.c_float, ctypes.c_uint
+    P = [ctypes.c_void_p(A)] * 6
+
+    def call(first=None, grads=None, L=128, hs=6, hn=2, d=64, dv=128, causal=1, eps=1e-5, flags=0,
+             ws=ctypes.c_void_p(A), ws_bytes=1 << 30):
+        ins = first if first is not None else P
+        outs = grads if grads is not None else P
+        return lib.gda_attn_bwd(*ins, F(0.8), ctypes.c_void_p(A), *outs, 2, L, hs, hn, d, dv, causal,
+                                F(eps), U(flags), ws, ws_bytes, None)
+    assert call(first=[None] + P[1:]) == INVALID
+    assert call(grads=P[:5] + [None]) == INVALID
+    assert call(L=0) == INVALID
+    assert call(hs=6, hn=4) == INVALID
+    assert call(causal=2) == INVALID
+    assert call(eps=-1.0) == INVALID
+    assert call(flags=0x10) == INVALID
+    assert call(d=96) == UNSUPPORTED
+    assert call(dv=96) == UNSUPPORTED
+    assert call(grads=P[:4] + [ctypes.c_void_p(A + 4), P[5]]) == MISALIGNED
+    assert call(ws=None) == WORKSPACE
+    assert call(ws_bytes=16) == WORKSPACE
