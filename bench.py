@@ -41,6 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 PROFILES = {
     "prefill": (os.path.join(ROOT, "profiles", "prefill_tc_counters.json"),
                 ["grouped_differential_attention_gb300/csrc/gda_prefill_tc.cu",
+                 "grouped_differential_attention_gb300/csrc/gda_prefill_common.cuh",
                  "grouped_differential_attention_gb300/csrc/gda_device.cuh"]),
     "decode": (os.path.join(ROOT, "profiles", "decode_split_counters.json"),
                ["grouped_differential_attention_gb300/csrc/gda_decode.cu",

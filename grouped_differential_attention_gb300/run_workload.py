@@ -3,6 +3,7 @@
     python -m grouped_differential_attention_gb300.run_workload prefill \
         gda_3to1_prefill_bf16_B4_L2048_h12+4_d64_dv128 --launches 3
     python -m grouped_differential_attention_gb300.run_workload decode --launches 3
+    python -m grouped_differential_attention_gb300.run_workload backward --launches 1
 
 Inputs are the seeded synthetic tensors of ``workloads``; prints the mean
 device time per launch measured with CUDA events (not meaningful under a
@@ -21,7 +22,7 @@ from grouped_differential_attention_gb300 import workloads as W
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=["prefill", "decode"])
+    ap.add_argument("kind", choices=["prefill", "decode", "backward"])
     ap.add_argument("workload", nargs="?", default=None)
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args(argv)
@@ -34,6 +35,17 @@ def main(argv=None):
 
         def launch():
             fn(*inp, w.lambda_init, causal=w.causal, eps=w.eps, out=out)
+    elif args.kind == "backward":
+        # float32 gradients at a prefill workload's sizes (default: the 3:1 B=4 L=2048 one)
+        w = W.PREFILL_WORKLOADS[args.workload or W.GDA3_PREFILL_L2048.name]
+        inp = [t.to(dev) for t in W.make_backward_inputs(w, dtype="f32")]
+        ws = torch.empty(gda.gda_attn_bwd_workspace_size(w.B, w.L, w.h_s, w.d, w.dv), dtype=torch.uint8,
+                         device=dev)
+        grads = gda.gda_attn_bwd(*inp[:6], w.lambda_init, inp[6], causal=w.causal, eps=w.eps, workspace=ws)
+
+        def launch():
+            gda.gda_attn_bwd(*inp[:6], w.lambda_init, inp[6], causal=w.causal, eps=w.eps, workspace=ws,
+                             grads=grads)
     else:
         w = W.GDA3_DECODE_B64
         inp = [t.to(dev) for t in W.make_decode_inputs(w)]
