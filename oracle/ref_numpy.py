@@ -93,3 +93,22 @@ def gda_decode_dense(q1, q2, k1c, k2c, vc, lens, lam, lambda_init, eps=1e-5, nor
             o = (1.0 - lambda_init) * o / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
         out[b] = o
     return out
+
+
+def row_logsumexp(q, k, causal=True):
+    """Log-sum-exp (natural log) of every query row's scaled logits, float64.
+
+    q, k: [B, L, heads, d] -> [B, heads, L]; entry (b, h, i) is
+    log sum_{j visible} exp(q_i . k_j / sqrt d), the normaliser of that row's
+    softmax map ("Differential Attention in Large Language Models ...",
+    section "Differential Attention Architecture": each map is a softmax of
+    the scaled logits).  Visible keys: j <= i when causal, all j otherwise.
+    Written with the usual maximum shift: m + log sum exp(s - m).
+    """
+    q, k = (np.asarray(t, dtype=np.float64) for t in (q, k))
+    B, L, H, d = q.shape
+    s = np.einsum("bihd,bjhd->bhij", q, k) / np.sqrt(d)
+    if causal:
+        s = np.where(np.triu(np.ones((L, L), dtype=bool), k=1), -np.inf, s)
+    m = np.max(s, axis=-1)
+    return m + np.log(np.sum(np.exp(s - m[..., None]), axis=-1))

@@ -384,3 +384,22 @@ def test_noise_gradient_collects_the_whole_group():
     assert torch.allclose(grads[3], rep[3].view(1, 5, 2, 2, 4).sum(3), atol=1e-12)
     for i in (0, 1, 4, 5):
         assert torch.allclose(grads[i], rep[i], atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_row_logsumexp_matches_library_and_normalises(causal):
+    """The rows' log-sum-exp equals torch.logsumexp of the masked scaled
+    logits (library routine), exp(s - lse) sums to 1 over the visible keys,
+    and the first causal row (one visible key) has lse = its single logit."""
+    from oracle.ref_numpy import row_logsumexp
+    g = torch.Generator().manual_seed(71)
+    q = torch.randn(2, 37, 3, 16, generator=g, dtype=torch.float64)
+    k = torch.randn(2, 37, 3, 16, generator=g, dtype=torch.float64)
+    got = row_logsumexp(q.numpy(), k.numpy(), causal=causal)
+    s = torch.einsum("bihd,bjhd->bhij", q, k) / 4.0
+    if causal:
+        s = s.masked_fill(torch.triu(torch.ones(37, 37, dtype=torch.bool), diagonal=1), float("-inf"))
+    np.testing.assert_allclose(got, torch.logsumexp(s, dim=-1).numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(np.exp(s.numpy() - got[..., None]).sum(-1), 1.0, rtol=0, atol=1e-12)
+    if causal:
+        np.testing.assert_allclose(got[:, :, 0], s[:, :, 0, 0].numpy(), rtol=0, atol=1e-12)
