@@ -399,6 +399,30 @@ def run_gda(args, world, rank, local):
     ck_ms = eva.elapsed_time(evb) / ck_steps
     del ck
 
+    # ---- two-pass prefill (difference map before the value product) on the same inputs
+    tp_ws = torch.empty(gda.gda_attn_fwd_2pass_workspace_size(w.B, w.L, w.h_s, w.h_n), dtype=torch.uint8,
+                        device=dev)
+    tp_out = torch.empty_like(out)
+
+    def tpstep(i):
+        q1, k1, q2, k2, v, lam = sets[i % N_INPUT_SETS]
+        gda.gda_attn_fwd_2pass(q1, k1, q2, k2, v, lam, w.lambda_init, causal=w.causal, eps=w.eps, out=tp_out,
+                               workspace=tp_ws)
+
+    for i in range(5):
+        tpstep(i)
+    torch.cuda.synchronize(dev)
+    tp_steps = 50
+    eve, evf = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    eve.record(stream)
+    for i in range(tp_steps):
+        tpstep(i)
+    evf.record(stream)
+    torch.cuda.synchronize(dev)
+    tp_ms = eve.elapsed_time(evf) / tp_steps
+    tp_tflops = prefill_flops(w.B, w.L, w.h_s, w.h_n, w.d, w.dv, w.causal) / (tp_ms * 1e-3) / 1e12
+    del tp_ws, tp_out
+
     # ---- float32 backward (gradients of all six inputs) at the prefill workload's sizes
     bw_in = [t.to(dev) for t in W.make_backward_inputs(w, dtype="f32", seed=rank + 31)]
     bw_ws = torch.empty(gda.gda_attn_bwd_workspace_size(w.B, w.L, w.h_s, w.d, w.dv), dtype=torch.uint8,
@@ -558,6 +582,15 @@ def run_gda(args, world, rank, local):
                           "roofline": {"bound": "tensor", "achieved": ck_flops / (ck_ms * 1e-3) / 1e12,
                                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                        "frac": ck_flops / (ck_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}},
+        "prefill_2pass": {"workload": w.name + ": pass 1 row log-sum-exp of every signal and noise map, "
+                                            "pass 2 one P V product per head with P = A1 - lambda A2",
+                          "value": tp_tflops, "unit": "TFLOP/s", "ms_per_step": tp_ms, "steps": tp_steps,
+                          "gpu_launches": 2 * tp_steps,
+                          "speed_vs_single_pass": tp_tflops / achieved,
+                          "flops_counted": "the single-pass kernel's algorithmic count, so value ratios are "
+                                           "time ratios",
+                          "roofline": {"bound": "tensor", "achieved": tp_tflops, "peak": peaks["bf16_tflops"],
+                                       "unit": "TFLOP/s", "frac": tp_tflops / peaks["bf16_tflops"]}},
         "backward_f32": {"workload": f"float32 gradients of q_sig, k_sig, q_noise, k_noise, v, lambda at "
                                      f"B={w.B}, L={w.L}, {w.h_s}+{w.h_n} heads, d={w.d}, dv={w.dv}, causal",
                          "value": bw_tflops, "unit": "TFLOP/s", "ms_per_step": bw_ms, "steps": bw_steps,

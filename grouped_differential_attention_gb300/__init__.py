@@ -29,7 +29,8 @@ __all__ = [
     "GDAError", "gda_attn_fwd", "gda_attn_fwd_f32", "gda_attn_decode",
     "gda_attn_decode_workspace_size", "gda_status_string", "gda_device_error",
     "lambda_init_schedule", "library_path", "GDA_FLAG_NO_NORM", "gda_attn_decode_noalloc",
-    "gda_attn_bwd", "gda_attn_bwd_workspace_size",
+    "gda_attn_bwd", "gda_attn_bwd_workspace_size", "gda_attn_fwd_2pass",
+    "gda_attn_fwd_2pass_workspace_size",
 ]
 
 GDA_OK = 0
@@ -97,6 +98,10 @@ def _load():
             lib.gda_attn_fwd_chunk.restype = I
             lib.gda_lambda_reparam.argtypes = [P, P, P, P, F, P, I, I, P]
             lib.gda_lambda_reparam.restype = I
+            lib.gda_attn_fwd_2pass.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, F, U, P, Z, P]
+            lib.gda_attn_fwd_2pass.restype = I
+            lib.gda_attn_fwd_2pass_workspace_size.argtypes = [I, I, I, I]
+            lib.gda_attn_fwd_2pass_workspace_size.restype = Z
             lib.gda_attn_bwd.argtypes = [P, P, P, P, P, P, F, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
                                          U, P, Z, P]
             lib.gda_attn_bwd.restype = I
@@ -301,6 +306,32 @@ def gda_attn_decode_paged(q_sig, q_noise, k_sig_pool, k_noise_pool, v_pool, bloc
             workspace.numel() * workspace.element_size(), _stream(dev))
     _check(rc, "gda decode (paged caches)")
     return out
+
+
+def gda_attn_fwd_2pass_workspace_size(B: int, L: int, h_s: int, h_n: int) -> int:
+    return int(_load().gda_attn_fwd_2pass_workspace_size(B, L, h_s, h_n))
+
+
+def gda_attn_fwd_2pass(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float, *,
+                       causal: bool = True, eps: float = 1e-5, out=None, flags: int = 0, workspace=None):
+    """Two-pass bf16 prefill (difference map before the value product); returns ``out``.
+
+    ``workspace`` (uint8 CUDA tensor) receives the rows' base-2 log-sum-exp
+    values as float32 [B, h_s + h_n, L].
+    """
+    B, L, hs, _ = q_sig.shape
+    hn = q_noise.shape[2]
+    need = gda_attn_fwd_2pass_workspace_size(B, L, hs, hn)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=q_sig.device)
+    _expect(workspace, "workspace", torch.uint8, (workspace.numel(),), q_sig.device)
+    ws = workspace
+
+    def entry(*args):
+        *head, fl, stream = args
+        return _load().gda_attn_fwd_2pass(*head, fl, _ptr(ws), ws.numel(), stream)
+    return _prefill(entry, torch.bfloat16, q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init, causal,
+                    eps, out, flags)
 
 
 def gda_attn_bwd_workspace_size(B: int, L: int, h_s: int, d: int, dv: int) -> int:

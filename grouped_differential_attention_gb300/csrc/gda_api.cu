@@ -194,6 +194,31 @@ int gda_attn_fwd_f32(const float *q_sig, const float *k_sig, const float *q_nois
                                h_s, h_n, d, dv, causal, eps, 0u, stream);
 }
 
+size_t gda_attn_fwd_2pass_workspace_size(int B, int L, int h_s, int h_n) {
+    if (B < 1 || L < 1 || h_s < 1 || h_n < 1) return 0;
+    if (static_cast<double>(B) * L * (h_s + h_n) > 9.0e15) return 0;
+    return prefill_2pass_workspace_bytes(B, L, h_s, h_n);
+}
+
+int gda_attn_fwd_2pass(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,
+                       const void *v, const float *lambda, float lambda_init, void *out, int B, int L,
+                       int h_s, int h_n, int d, int dv, int causal, float eps, unsigned flags,
+                       void *workspace, size_t workspace_bytes, gda_stream_t stream) {
+    int st = check_prefill_common(q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L,
+                                  h_s, h_n, d, dv, causal, eps, flags);
+    if (st != GDA_OK) return st;
+    if (!(d == 64 || d == 128) || !(dv == 128 || dv == 256)) return GDA_ERR_UNSUPPORTED;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < gda_attn_fwd_2pass_workspace_size(B, L, h_s, h_n))
+        return GDA_ERR_WORKSPACE;
+    unsigned *err = nullptr;
+    st = current_device(&err);
+    if (st != GDA_OK) return st;
+    PrefillArgs a{q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L, h_s, h_n,
+                  d, dv, causal, eps, flags, err};
+    return launch_prefill_2pass(a, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t gda_attn_bwd_workspace_size(int B, int L, int h_s, int d, int dv) {
     if (B < 1 || L < 1 || h_s < 1 || d < 1 || dv < 1) return 0;
     if (static_cast<double>(B) * L * h_s * (d > dv ? d : dv) > 9.0e15) return 0;

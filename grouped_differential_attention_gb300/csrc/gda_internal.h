@@ -63,6 +63,8 @@ int device_state(unsigned **err_word);
 int launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
 int launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream);
 int launch_decode(const DecodeArgs &a, cudaStream_t stream);
+int launch_prefill_2pass(const PrefillArgs &a, void *workspace, cudaStream_t stream);
+size_t prefill_2pass_workspace_bytes(int B, int L, int hs, int hn);
 int launch_backward_f32(const BackwardArgs &a, cudaStream_t stream);
 size_t backward_f32_workspace_bytes(int B, int L, int hs, int d, int dv);
 int launch_lambda_reparam(const float *lq1, const float *lk1, const float *lq2, const float *lk2,

@@ -129,6 +129,32 @@ int gda_attn_fwd_f32_ex(const float *q_sig, const float *k_sig, const float *q_n
                         gda_stream_t stream);
 
 /*
+ * Two-pass bf16 prefill: the same operation and layouts as gda_attn_fwd_ex,
+ * computed with the difference map formed before the value product
+ * (o = (A1 - lambda_h A2) V_h; Differential Transformer, section
+ * "Differential Attention": both maps are normalised softmax maps, so their
+ * difference is fixed once each row's softmax statistics are known).
+ *   Pass 1 writes each query row's base-2 log-sum-exp of every signal map
+ *   (per signal head) and every noise map (once per noise head) to
+ *   `workspace`; pass 2 recomputes the logits, forms P = A1 - lambda_h A2
+ *   in float32, rounds it once to bf16 and runs one P V product per head into
+ *   one float32 accumulator, then applies the headwise norm.
+ *   workspace: device memory of at least gda_attn_fwd_2pass_workspace_size(
+ *   B, L, h_s, h_n) bytes (float32 [B, h_s + h_n, L]), 16-byte aligned,
+ *   owned by the caller; on return it holds the log-sum-exp values.
+ *   Supported: d in {64, 128}, dv in {128, 256} (dv = 256 in one CTA).
+ *   Returns as gda_attn_fwd_ex, plus GDA_ERR_WORKSPACE.
+ */
+int gda_attn_fwd_2pass(const void *q_sig, const void *k_sig, const void *q_noise,
+                       const void *k_noise, const void *v, const float *lambda,
+                       float lambda_init, void *out, int B, int L, int h_s, int h_n,
+                       int d, int dv, int causal, float eps, unsigned flags,
+                       void *workspace, size_t workspace_bytes, gda_stream_t stream);
+
+/* Bytes of workspace gda_attn_fwd_2pass needs (0 for invalid sizes). */
+size_t gda_attn_fwd_2pass_workspace_size(int B, int L, int h_s, int h_n);
+
+/*
  * Backward (gradients) of the float32 operation above: given dy = dL/dy
  * (dL/do with GDA_FLAG_NO_NORM), the gradients of L with respect to the
  * signal and noise projections, the values and lambda.  Chain rule through

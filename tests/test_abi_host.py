@@ -248,3 +248,26 @@ def test_backward_rejects_bad_arguments(lib):
     assert call(grads=P[:4] + [ctypes.c_void_p(A + 4), P[5]]) == MISALIGNED
     assert call(ws=None) == WORKSPACE
     assert call(ws_bytes=16) == WORKSPACE
+
+
+def test_two_pass_prefill_rejects_bad_arguments(lib):
+    # every call below fails validation before any device work
+    F, U = ctypes.c_float, ctypes.c_uint
+    P = [ctypes.c_void_p(A)] * 6
+
+    def call(L=128, hs=6, hn=2, d=64, dv=128, causal=1, ws=ctypes.c_void_p(A), ws_bytes=1 << 30, first=None):
+        ins = first if first is not None else P
+        return lib.gda_attn_fwd_2pass(*ins, F(0.8), ctypes.c_void_p(A), 2, L, hs, hn, d, dv, causal, F(1e-5),
+                                      U(0), ws, ws_bytes, None)
+    assert lib.gda_attn_fwd_2pass_workspace_size(2, 128, 6, 2) == 4 * 2 * 128 * 8
+    assert lib.gda_attn_fwd_2pass_workspace_size(2, 0, 6, 2) == 0
+    assert call(first=[None] + P[1:]) == INVALID
+    assert call(L=0) == INVALID
+    assert call(hs=6, hn=4) == INVALID
+    assert call(causal=3) == INVALID
+    assert call(d=96) == UNSUPPORTED
+    assert call(dv=64) == UNSUPPORTED
+    assert call(first=[ctypes.c_void_p(A + 8)] + P[1:]) == MISALIGNED
+    assert call(ws=None) == WORKSPACE
+    assert call(ws_bytes=4 * 2 * 128 * 8 - 4) == WORKSPACE
+    assert call(ws=ctypes.c_void_p(A + 4)) == WORKSPACE
