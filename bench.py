@@ -423,6 +423,29 @@ def run_gda(args, world, rank, local):
     tp_tflops = prefill_flops(w.B, w.L, w.h_s, w.h_n, w.d, w.dv, w.causal) / (tp_ms * 1e-3) / 1e12
     del tp_ws, tp_out
 
+    # ---- the 4:1 d=128 dv=256 prefill through gda_attn_fwd (two-pass kernels at dv = 256), and
+    # the same call held to the single-pass kernel; one input set of 302 MB (larger than L2)
+    w4 = W.GDA4_PREFILL_L8192
+    in4 = [t.to(dev) for t in W.make_prefill_inputs(w4, seed=rank + 41)]
+    out4 = torch.empty((w4.B, w4.L, w4.h_s, w4.dv), dtype=torch.bfloat16, device=dev)
+    fl4 = prefill_flops(w4.B, w4.L, w4.h_s, w4.h_n, w4.d, w4.dv, w4.causal)
+    ms4 = {}
+    for tag, fl in (("default", 0), ("single_pass", gda.GDA_FLAG_SINGLE_PASS)):
+        def step4():
+            gda.gda_attn_fwd(*in4, w4.lambda_init, causal=w4.causal, eps=w4.eps, out=out4, flags=fl)
+        for _ in range(3):
+            step4()
+        torch.cuda.synchronize(dev)
+        n4 = 20
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(n4):
+            step4()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms4[tag] = ev0.elapsed_time(ev1) / n4
+    del in4, out4
+
     # ---- float32 backward (gradients of all six inputs) at the prefill workload's sizes
     bw_in = [t.to(dev) for t in W.make_backward_inputs(w, dtype="f32", seed=rank + 31)]
     bw_ws = torch.empty(gda.gda_attn_bwd_workspace_size(w.B, w.L, w.h_s, w.d, w.dv), dtype=torch.uint8,
@@ -591,6 +614,14 @@ def run_gda(args, world, rank, local):
                                            "time ratios",
                           "roofline": {"bound": "tensor", "achieved": tp_tflops, "peak": peaks["bf16_tflops"],
                                        "unit": "TFLOP/s", "frac": tp_tflops / peaks["bf16_tflops"]}},
+        "prefill_4to1": {"workload": w4.name + " through gda_attn_fwd (two-pass kernels at dv = 256)",
+                         "value": fl4 / (ms4["default"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                         "ms_per_step": ms4["default"], "steps": 20, "gpu_launches": 2 * 20,
+                         "single_pass_kernel_tflops": fl4 / (ms4["single_pass"] * 1e-3) / 1e12,
+                         "single_pass_kernel_ms": ms4["single_pass"],
+                         "roofline": {"bound": "tensor", "achieved": fl4 / (ms4["default"] * 1e-3) / 1e12,
+                                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                      "frac": fl4 / (ms4["default"] * 1e-3) / 1e12 / peaks["bf16_tflops"]}},
         "backward_f32": {"workload": f"float32 gradients of q_sig, k_sig, q_noise, k_noise, v, lambda at "
                                      f"B={w.B}, L={w.L}, {w.h_s}+{w.h_n} heads, d={w.d}, dv={w.dv}, causal",
                          "value": bw_tflops, "unit": "TFLOP/s", "ms_per_step": bw_ms, "steps": bw_steps,

@@ -28,7 +28,8 @@ import torch
 __all__ = [
     "GDAError", "gda_attn_fwd", "gda_attn_fwd_f32", "gda_attn_decode",
     "gda_attn_decode_workspace_size", "gda_status_string", "gda_device_error",
-    "lambda_init_schedule", "library_path", "GDA_FLAG_NO_NORM", "gda_attn_decode_noalloc",
+    "lambda_init_schedule", "library_path", "GDA_FLAG_NO_NORM", "GDA_FLAG_SINGLE_PASS",
+    "gda_attn_decode_noalloc",
     "gda_attn_bwd", "gda_attn_bwd_workspace_size", "gda_attn_fwd_2pass",
     "gda_attn_fwd_2pass_workspace_size",
 ]
@@ -41,6 +42,7 @@ GDA_ERR_WORKSPACE = -4
 GDA_ERR_CUDA = -5
 GDA_ERR_DEVICE_TIMEOUT = -6
 GDA_FLAG_NO_NORM = 0x1
+GDA_FLAG_SINGLE_PASS = 0x2
 GDA_DEVERR_PREFILL_TIMEOUT = 0x1
 GDA_DEVERR_BAD_LENGTH = 0x2
 GDA_DEVERR_DECODE_TIMEOUT = 0x4

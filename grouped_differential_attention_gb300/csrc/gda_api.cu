@@ -65,13 +65,13 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_prefill_common(const void *q1, const void *k1, const void *q2, const void *k2,
                          const void *v, const float *lam, float lambda_init, const void *out, int B,
                          int L, int hs, int hn, int d, int dv, int causal, float eps,
-                         unsigned flags) {
+                         unsigned flags, unsigned allowed_flags = GDA_FLAG_NO_NORM) {
     if (!q1 || !k1 || !q2 || !k2 || !v || !lam || !out) return GDA_ERR_INVALID_ARG;
     if (B < 1 || L < 1 || hs < 1 || hn < 1 || d < 1 || dv < 1) return GDA_ERR_INVALID_ARG;
     if (hs % hn != 0) return GDA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return GDA_ERR_INVALID_ARG;
     if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(lambda_init)) return GDA_ERR_INVALID_ARG;
-    if (flags & ~GDA_FLAG_NO_NORM) return GDA_ERR_INVALID_ARG;
+    if (flags & ~allowed_flags) return GDA_ERR_INVALID_ARG;
     // element counts must fit the 64-bit index arithmetic with room to spare
     const double elems = static_cast<double>(B) * L * (hs > hn ? hs : hn) * (d > dv ? d : dv);
     if (elems > 9.0e15) return GDA_ERR_INVALID_ARG;
@@ -131,15 +131,28 @@ int gda_attn_fwd_ex(const void *q_sig, const void *k_sig, const void *q_noise, c
                     int h_s, int h_n, int d, int dv, int causal, float eps, unsigned flags,
                     gda_stream_t stream) {
     int st = check_prefill_common(q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L,
-                                  h_s, h_n, d, dv, causal, eps, flags);
+                                  h_s, h_n, d, dv, causal, eps, flags,
+                                  GDA_FLAG_NO_NORM | GDA_FLAG_SINGLE_PASS);
     if (st != GDA_OK) return st;
     if (!(d == 64 || d == 128) || !(dv == 128 || dv == 256)) return GDA_ERR_UNSUPPORTED;
     unsigned *err = nullptr;
     st = current_device(&err);
     if (st != GDA_OK) return st;
     PrefillArgs a{q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L, h_s, h_n,
-                  d, dv, causal, eps, flags, err};
-    return launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream));
+                  d, dv, causal, eps, flags & GDA_FLAG_NO_NORM, err};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dv == 256 && !(flags & GDA_FLAG_SINGLE_PASS)) {
+        // one accumulator per CTA beats the CTA pair of the single-pass kernel here
+        void *lse = nullptr;
+        if (cudaMallocAsync(&lse, prefill_2pass_workspace_bytes(B, L, h_s, h_n), s) == cudaSuccess) {
+            const int st2 = launch_prefill_2pass(a, lse, s);
+            const cudaError_t fe = cudaFreeAsync(lse, s);
+            if (st2 != GDA_OK) return st2;
+            return fe == cudaSuccess ? GDA_OK : record_cuda_error(fe);
+        }
+        cudaGetLastError();   // no statistics buffer: the single-pass kernel needs none
+    }
+    return launch_prefill_tc(a, s);
 }
 
 int gda_attn_fwd_chunk(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,

@@ -71,6 +71,7 @@ typedef enum {
 
 /* Flags for the *_ex entry points. */
 #define GDA_FLAG_NO_NORM 0x1u    /* return o_h (pre-norm, float32 difference) instead of y_h */
+#define GDA_FLAG_SINGLE_PASS 0x2u /* gda_attn_fwd_ex only: keep the single-pass kernel at dv = 256 */
 
 /*
  * Prefill / full-sequence forward, bf16 I/O, float32 accumulation.
@@ -79,7 +80,14 @@ typedef enum {
  *   Supported: d in {64, 128}; dv in {128, 256}; B, L >= 1; h_s % h_n == 0;
  *   every pointer 16-byte aligned; device sm_103 (GB300).  causal in {0, 1}.
  *   Output is rounded once to bf16 (round to nearest even).
- * Computed by hand-written tcgen05/TMA kernels; uses no workspace.
+ * Computed by hand-written tcgen05/TMA kernels.  dv = 128: one pass with two
+ * running softmax states per row, no workspace.  dv = 256: the two-pass
+ * kernels of gda_attn_fwd_2pass (measured 1.2-1.4x faster there, one
+ * accumulator per CTA instead of a CTA pair), with the pass-1 statistics
+ * (4 B x B x (h_s + h_n) x L) taken from the stream-ordered allocator
+ * (cudaMallocAsync / cudaFreeAsync on `stream`); if that allocation fails,
+ * or with GDA_FLAG_SINGLE_PASS (gda_attn_fwd_ex), the single-pass kernel
+ * runs instead (same result within the bf16 bound, no allocation).
  */
 int gda_attn_fwd(const void *q_sig, const void *k_sig, const void *q_noise,
                  const void *k_noise, const void *v, const float *lambda,
@@ -104,7 +112,7 @@ int gda_attn_fwd_chunk(const void *q_sig, const void *k_sig, const void *q_noise
                        int Lk, int h_s, int h_n, int d, int dv, int causal, float eps, unsigned flags,
                        gda_stream_t stream);
 
-/* gda_attn_fwd with flags (GDA_FLAG_NO_NORM). */
+/* gda_attn_fwd with flags (GDA_FLAG_NO_NORM, GDA_FLAG_SINGLE_PASS). */
 int gda_attn_fwd_ex(const void *q_sig, const void *k_sig, const void *q_noise,
                     const void *k_noise, const void *v, const float *lambda,
                     float lambda_init, void *out, int B, int L, int h_s, int h_n,

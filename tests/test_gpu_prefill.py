@@ -1,6 +1,7 @@
 """GPU parity of the prefill paths against the float64 oracle (same seeded inputs).
 
-bf16 path (tcgen05/TMA kernel): |err| <= 3e-3 + 2e-2|ref| elementwise.
+bf16 path (tcgen05/TMA kernels; at dv = 256 gda_attn_fwd runs the two-pass
+kernels unless GDA_FLAG_SINGLE_PASS is given): |err| <= 3e-3 + 2e-2|ref| elementwise.
 f32 path (CUDA-core kernel): |err| <= 1e-4 (|ref| + rms_row(ref)).
 Small cases are compared on every element (several 128-row tiles, ragged
 tails, L = 1, non-causal, d = 128 with dv split over a CTA pair); the
@@ -64,6 +65,20 @@ def test_prefill_bf16_matches_oracle(oracle_mod, shape):
     inp = W.make_prefill_inputs(W.GDA3_PREFILL_L2048, B=B, L=L, h_s=hs, h_n=hn, d=d, dv=dv,
                                 seed=1000 + L + hs)
     got = run_bf16(inp, 0.8, causal)
+    ref = oracle_mod.prefill(*inp, 0.8, causal=causal)
+    assert_bf16_close(got, ref, str(shape))
+
+
+@pytest.mark.parametrize("shape", [s for s in SMALL_BF16 if s[5] == 256], ids=lambda s: "B%dL%dhs%dhn%dd%ddv%d%s" % (
+    s[0], s[1], s[2], s[3], s[4], s[5], "c" if s[6] else "f"))
+def test_prefill_bf16_single_pass_flag_at_dv256(oracle_mod, shape):
+    """At dv = 256 gda_attn_fwd runs the two-pass kernels; GDA_FLAG_SINGLE_PASS
+    keeps the single-pass kernel (dv split over a CTA pair), which must match
+    the oracle too."""
+    B, L, hs, hn, d, dv, causal = shape
+    inp = W.make_prefill_inputs(W.GDA3_PREFILL_L2048, B=B, L=L, h_s=hs, h_n=hn, d=d, dv=dv,
+                                seed=1000 + L + hs)
+    got = run_bf16(inp, 0.8, causal, flags=gda.GDA_FLAG_SINGLE_PASS)
     ref = oracle_mod.prefill(*inp, 0.8, causal=causal)
     assert_bf16_close(got, ref, str(shape))
 
