@@ -31,7 +31,7 @@ __all__ = [
     "lambda_init_schedule", "library_path", "GDA_FLAG_NO_NORM", "GDA_FLAG_SINGLE_PASS",
     "gda_attn_decode_noalloc",
     "gda_attn_bwd", "gda_attn_bwd_workspace_size", "gda_attn_fwd_2pass",
-    "gda_attn_fwd_2pass_workspace_size",
+    "gda_attn_fwd_2pass_workspace_size", "gda_attn_bwd_bf16", "gda_attn_bwd_bf16_workspace_size",
 ]
 
 GDA_OK = 0
@@ -104,6 +104,11 @@ def _load():
             lib.gda_attn_fwd_2pass.restype = I
             lib.gda_attn_fwd_2pass_workspace_size.argtypes = [I, I, I, I]
             lib.gda_attn_fwd_2pass_workspace_size.restype = Z
+            lib.gda_attn_bwd_bf16.argtypes = [P, P, P, P, P, P, F, P, P, P, P, P, P, P, I, I, I, I, I, I, I,
+                                              F, U, P, Z, P]
+            lib.gda_attn_bwd_bf16.restype = I
+            lib.gda_attn_bwd_bf16_workspace_size.argtypes = [I, I, I, I, I]
+            lib.gda_attn_bwd_bf16_workspace_size.restype = Z
             lib.gda_attn_bwd.argtypes = [P, P, P, P, P, P, F, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
                                          U, P, Z, P]
             lib.gda_attn_bwd.restype = I
@@ -375,6 +380,45 @@ def gda_attn_bwd(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float, dy,
             float(lambda_init), _ptr(dy), *[_ptr(t) for t in grads], B, L, hs, hn, d, dv,
             int(bool(causal)), float(eps), int(flags), _ptr(workspace), workspace.numel(), _stream(dev))
     _check(rc, "gda backward")
+    return tuple(grads)
+
+
+def gda_attn_bwd_bf16_workspace_size(B: int, L: int, h_s: int, h_n: int, dv: int) -> int:
+    return int(_load().gda_attn_bwd_bf16_workspace_size(B, L, h_s, h_n, dv))
+
+
+def gda_attn_bwd_bf16(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float, dy, *,
+                      causal: bool = True, eps: float = 1e-5, flags: int = 0, workspace=None, grads=None):
+    """Tensor-core gradients from bf16 inputs; returns float32
+    (dq_sig, dk_sig, dq_noise, dk_noise, dv, dlambda)."""
+    dev = q_sig.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if q_sig.dim() != 4 or q_noise.dim() != 4 or v.dim() != 4:
+        raise ValueError("q_sig, q_noise and v must be 4-D [B, L, heads, dim]")
+    bf, f32 = torch.bfloat16, torch.float32
+    B, L, hs, d = q_sig.shape
+    hn = q_noise.shape[2]
+    dv = v.shape[3]
+    shapes = ((B, L, hs, d), (B, L, hs, d), (B, L, hn, d), (B, L, hn, d), (B, L, hs, dv), (hs,))
+    for t, name, shape in zip((q_sig, k_sig, q_noise, k_noise, v), ("q_sig", "k_sig", "q_noise", "k_noise", "v"),
+                              shapes):
+        _expect(t, name, bf, shape, dev)
+    _expect(lam, "lam", f32, (hs,), dev)
+    _expect(dy, "dy", bf, (B, L, hs, dv), dev)
+    if grads is None:
+        grads = tuple(torch.empty(s, dtype=f32, device=dev) for s in shapes)
+    for t, name, shape in zip(grads, ("dq_sig", "dk_sig", "dq_noise", "dk_noise", "dv", "dlambda"), shapes):
+        _expect(t, name, f32, shape, dev)
+    need = gda_attn_bwd_bf16_workspace_size(B, L, hs, hn, dv)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = _load().gda_attn_bwd_bf16(
+            _ptr(q_sig), _ptr(k_sig), _ptr(q_noise), _ptr(k_noise), _ptr(v), _ptr(lam),
+            float(lambda_init), _ptr(dy), *[_ptr(t) for t in grads], B, L, hs, hn, d, dv,
+            int(bool(causal)), float(eps), int(flags), _ptr(workspace), workspace.numel(), _stream(dev))
+    _check(rc, "gda backward (bf16)")
     return tuple(grads)
 
 

@@ -207,6 +207,36 @@ int gda_attn_fwd_f32(const float *q_sig, const float *k_sig, const float *q_nois
                                h_s, h_n, d, dv, causal, eps, 0u, stream);
 }
 
+size_t gda_attn_bwd_bf16_workspace_size(int B, int L, int h_s, int h_n, int dv) {
+    if (B < 1 || L < 1 || h_s < 1 || h_n < 1 || dv < 1) return 0;
+    if (static_cast<double>(B) * L * (h_s + h_n) * (dv > 1 ? dv : 1) > 9.0e15) return 0;
+    return backward_tc_workspace_bytes(B, L, h_s, h_n, dv);
+}
+
+int gda_attn_bwd_bf16(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,
+                      const void *v, const float *lambda, float lambda_init, const void *dy, float *dq_sig,
+                      float *dk_sig, float *dq_noise, float *dk_noise, float *dv_out, float *dlambda, int B,
+                      int L, int h_s, int h_n, int d, int dv, int causal, float eps, unsigned flags,
+                      void *workspace, size_t workspace_bytes, gda_stream_t stream) {
+    int st = check_prefill_common(q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, dy, B, L, h_s,
+                                  h_n, d, dv, causal, eps, flags);
+    if (st != GDA_OK) return st;
+    if (!dq_sig || !dk_sig || !dq_noise || !dk_noise || !dv_out || !dlambda) return GDA_ERR_INVALID_ARG;
+    if (d != 64 || dv != 128) return GDA_ERR_UNSUPPORTED;
+    if (!aligned16(dq_sig) || !aligned16(dk_sig) || !aligned16(dq_noise) || !aligned16(dk_noise) ||
+        !aligned16(dv_out) || !aligned16(dlambda))
+        return GDA_ERR_MISALIGNED;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < gda_attn_bwd_bf16_workspace_size(B, L, h_s, h_n, dv))
+        return GDA_ERR_WORKSPACE;
+    unsigned *err = nullptr;
+    st = current_device(&err);
+    if (st != GDA_OK) return st;
+    BackwardTcArgs a{q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, dy, dq_sig, dk_sig, dq_noise,
+                     dk_noise, dv_out, dlambda, B, L, h_s, h_n, d, dv, causal, eps, flags, workspace, err};
+    return launch_backward_tc(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t gda_attn_fwd_2pass_workspace_size(int B, int L, int h_s, int h_n) {
     if (B < 1 || L < 1 || h_s < 1 || h_n < 1) return 0;
     if (static_cast<double>(B) * L * (h_s + h_n) > 9.0e15) return 0;

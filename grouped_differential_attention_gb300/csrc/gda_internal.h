@@ -50,6 +50,20 @@ struct BackwardArgs {
     void *workspace;
 };
 
+struct BackwardTcArgs {
+    const void *q1, *k1, *q2, *k2, *v;   // bf16, layouts of gda_attn_fwd
+    const float *lambda;
+    float lambda_init;
+    const void *dy;                      // bf16 [B, L, hs, dv]
+    float *dq1, *dk1, *dq2, *dk2, *dv_out, *dlambda;
+    int B, L, hs, hn, d, dv;
+    int causal;
+    float eps;
+    unsigned flags;
+    void *workspace;
+    unsigned *dev_err;
+};
+
 // Remembers `e` as this thread's last CUDA error (see gda_last_cuda_error),
 // clears the runtime's sticky-free error state and returns GDA_ERR_CUDA.
 int record_cuda_error(cudaError_t e);
@@ -65,7 +79,12 @@ int launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream);
 int launch_decode(const DecodeArgs &a, cudaStream_t stream);
 int launch_prefill_2pass(const PrefillArgs &a, void *workspace, cudaStream_t stream);
 size_t prefill_2pass_workspace_bytes(int B, int L, int hs, int hn);
+// Pass 1 alone: base-2 log-sum-exp of every signal and noise map row into
+// lse [B, hs + hn, lse_ld] (lse_ld >= L).
+int launch_lse_pass(const PrefillArgs &a, float *lse, int lse_ld, cudaStream_t stream);
 int launch_backward_f32(const BackwardArgs &a, cudaStream_t stream);
+int launch_backward_tc(const BackwardTcArgs &a, cudaStream_t stream);
+size_t backward_tc_workspace_bytes(int B, int L, int hs, int hn, int dv);
 size_t backward_f32_workspace_bytes(int B, int L, int hs, int d, int dv);
 int launch_lambda_reparam(const float *lq1, const float *lk1, const float *lq2, const float *lk2,
                           float lambda_init, float *out, int hs, int d, cudaStream_t stream);

@@ -47,11 +47,12 @@ constexpr int kBN2 = 64;            // keys per tile
 
 struct P2Params {
     const float *lambda;
-    float *lse;                     // [B, hs + hn, L] (base-2 log-sum-exp)
+    float *lse;                     // [B, hs + hn, lse_ld] (base-2 log-sum-exp)
     __nv_bfloat16 *out;
     unsigned *err;
     float lambda_init, eps, scale_log2;
     int B, L, hs, hn, dv, causal, nqt, no_norm;
+    int lse_ld;                     // row stride of lse (>= L)
 };
 
 // ---------------------------------------------------------------- items --
@@ -292,7 +293,7 @@ gda_lse_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                 const float mm = fmaxf(m0, m1);
                 const float ls = ctl->part_l[pb][0][row] * fast_exp2(m0 - mm) +
                                  (m1 == -INFINITY ? 0.f : ctl->part_l[pb][1][row] * fast_exp2(m1 - mm));
-                p.lse[(static_cast<size_t>(it.b) * heads + it.head) * p.L + qrow] = mm + __log2f(ls);
+                p.lse[(static_cast<size_t>(it.b) * heads + it.head) * p.lse_ld + qrow] = mm + __log2f(ls);
             }
             gt += it.nkv;
             if (bar_red_or(1, kSmThreads, !ok || *abort_flag)) break;
@@ -562,8 +563,8 @@ gda_diffmap_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_con
             const int last_key = p.causal ? min(qrow, p.L - 1) : p.L - 1;
             const float lam = p.lambda[h];
             // rows past L get lse = +inf, so every P of theirs is 0
-            const float neg1 = in ? -p.lse[(static_cast<size_t>(it.b) * heads + h) * p.L + qrow] : -INFINITY;
-            const float neg2 = in ? -p.lse[(static_cast<size_t>(it.b) * heads + p.hs + g) * p.L + qrow] : -INFINITY;
+            const float neg1 = in ? -p.lse[(static_cast<size_t>(it.b) * heads + h) * p.lse_ld + qrow] : -INFINITY;
+            const float neg2 = in ? -p.lse[(static_cast<size_t>(it.b) * heads + p.hs + g) * p.lse_ld + qrow] : -INFINITY;
             const float nlam = -lam;
             bool ok = true;
             for (int j = 0; j < it.nkv; ++j) {
@@ -672,31 +673,7 @@ int sm_count(int *sms) {
     return e == cudaSuccess ? GDA_OK : record_cuda_error(e);
 }
 
-template <int D, int DV>
-int launch_2pass_impl(const PrefillArgs &a, float *lse, cudaStream_t stream) {
-    CUtensorMap mQ1, mK1, mQ2, mK2, mV;
-    const uint64_t B = a.B, L = a.L, hs = a.hs, hn = a.hn, d = a.d, dv = a.dv;
-    {
-        const uint64_t dims[4] = {d, hs, L, B};
-        const uint64_t str[3] = {d * 2, hs * d * 2, L * hs * d * 2};
-        const uint32_t boxq[4] = {64, 1, kBM, 1}, boxk[4] = {64, 1, kBN2, 1};
-        if (!encode_tmap_4d_bf16(&mQ1, a.q1, dims, str, boxq)) return GDA_ERR_CUDA;
-        if (!encode_tmap_4d_bf16(&mK1, a.k1, dims, str, boxk)) return GDA_ERR_CUDA;
-    }
-    {
-        const uint64_t dims[4] = {d, hn, L, B};
-        const uint64_t str[3] = {d * 2, hn * d * 2, L * hn * d * 2};
-        const uint32_t boxq[4] = {64, 1, kBM, 1}, boxk[4] = {64, 1, kBN2, 1};
-        if (!encode_tmap_4d_bf16(&mQ2, a.q2, dims, str, boxq)) return GDA_ERR_CUDA;
-        if (!encode_tmap_4d_bf16(&mK2, a.k2, dims, str, boxk)) return GDA_ERR_CUDA;
-    }
-    {
-        const uint64_t dims[4] = {dv, hs, L, B};
-        const uint64_t str[3] = {dv * 2, hs * dv * 2, L * hs * dv * 2};
-        const uint32_t box[4] = {64, 1, kBN2, 1};
-        if (!encode_tmap_4d_bf16(&mV, a.v, dims, str, box)) return GDA_ERR_CUDA;
-    }
-    P2Params p;
+void fill_params(P2Params &p, const PrefillArgs &a, float *lse, int lse_ld) {
     p.lambda = a.lambda;
     p.lse = lse;
     p.out = static_cast<__nv_bfloat16 *>(a.out);
@@ -712,14 +689,29 @@ int launch_2pass_impl(const PrefillArgs &a, float *lse, cudaStream_t stream) {
     p.causal = a.causal;
     p.nqt = (a.L + kBM - 1) / kBM;
     p.no_norm = (a.flags & GDA_FLAG_NO_NORM) ? 1 : 0;
+    p.lse_ld = lse_ld;
+}
 
-    int sms = 0;
-    int st = sm_count(&sms);
-    if (st != GDA_OK) return st;
+bool qk_maps(const PrefillArgs &a, CUtensorMap *mQ1, CUtensorMap *mK1, CUtensorMap *mQ2, CUtensorMap *mK2) {
+    const uint64_t B = a.B, L = a.L, hs = a.hs, hn = a.hn, d = a.d;
+    const uint32_t boxq[4] = {64, 1, kBM, 1}, boxk[4] = {64, 1, kBN2, 1};
+    {
+        const uint64_t dims[4] = {d, hs, L, B};
+        const uint64_t str[3] = {d * 2, hs * d * 2, L * hs * d * 2};
+        if (!encode_tmap_4d_bf16(mQ1, a.q1, dims, str, boxq)) return false;
+        if (!encode_tmap_4d_bf16(mK1, a.k1, dims, str, boxk)) return false;
+    }
+    const uint64_t dims[4] = {d, hn, L, B};
+    const uint64_t str[3] = {d * 2, hn * d * 2, L * hn * d * 2};
+    if (!encode_tmap_4d_bf16(mQ2, a.q2, dims, str, boxq)) return false;
+    return encode_tmap_4d_bf16(mK2, a.k2, dims, str, boxk);
+}
+
+template <int D>
+int launch_lse_impl(const PrefillArgs &a, const CUtensorMap &mQ1, const CUtensorMap &mK1, const CUtensorMap &mQ2,
+                    const CUtensorMap &mK2, const P2Params &p, int sms, cudaStream_t stream) {
     const long long items1 = static_cast<long long>(p.nqt) * a.B * (a.hs + a.hn);
-    const long long items2 = static_cast<long long>(p.nqt) * a.B * a.hs;
     if (items1 > 0x7fffffffLL) return GDA_ERR_UNSUPPORTED;
-
     auto k1 = gda_lse_tc_kernel<D>;
     constexpr int smem1 = lse_smem_bytes<D>();
     cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, smem1);
@@ -728,12 +720,33 @@ int launch_2pass_impl(const PrefillArgs &a, float *lse, cudaStream_t stream) {
     if (g1 > items1) g1 = items1;
     k1<<<static_cast<unsigned>(g1), kThreads2, smem1, stream>>>(mQ1, mK1, mQ2, mK2, p);
     e = cudaGetLastError();
-    if (e != cudaSuccess) return record_cuda_error(e);
+    return e == cudaSuccess ? GDA_OK : record_cuda_error(e);
+}
+
+template <int D, int DV>
+int launch_2pass_impl(const PrefillArgs &a, float *lse, cudaStream_t stream) {
+    CUtensorMap mQ1, mK1, mQ2, mK2, mV;
+    const uint64_t B = a.B, L = a.L, hs = a.hs, dv = a.dv;
+    if (!qk_maps(a, &mQ1, &mK1, &mQ2, &mK2)) return GDA_ERR_CUDA;
+    {
+        const uint64_t dims[4] = {dv, hs, L, B};
+        const uint64_t str[3] = {dv * 2, hs * dv * 2, L * hs * dv * 2};
+        const uint32_t box[4] = {64, 1, kBN2, 1};
+        if (!encode_tmap_4d_bf16(&mV, a.v, dims, str, box)) return GDA_ERR_CUDA;
+    }
+    P2Params p;
+    fill_params(p, a, lse, a.L);
+    int sms = 0;
+    int st = sm_count(&sms);
+    if (st != GDA_OK) return st;
+    st = launch_lse_impl<D>(a, mQ1, mK1, mQ2, mK2, p, sms, stream);
+    if (st != GDA_OK) return st;
+    const long long items2 = static_cast<long long>(p.nqt) * a.B * a.hs;
 
     auto k2 = gda_diffmap_tc_kernel<D, DV>;
     constexpr int smem2 = dm_smem_bytes<D, DV>();
     static_assert(smem2 <= 232448, "shared memory budget");
-    e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, smem2);
+    cudaError_t e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, smem2);
     if (e != cudaSuccess) return record_cuda_error(e);
     long long g2 = sms;
     if (g2 > items2) g2 = items2;
@@ -746,6 +759,19 @@ int launch_2pass_impl(const PrefillArgs &a, float *lse, cudaStream_t stream) {
 
 size_t prefill_2pass_workspace_bytes(int B, int L, int hs, int hn) {
     return sizeof(float) * static_cast<size_t>(B) * static_cast<size_t>(hs + hn) * static_cast<size_t>(L);
+}
+
+int launch_lse_pass(const PrefillArgs &a, float *lse, int lse_ld, cudaStream_t stream) {
+    CUtensorMap mQ1, mK1, mQ2, mK2;
+    if (!qk_maps(a, &mQ1, &mK1, &mQ2, &mK2)) return GDA_ERR_CUDA;
+    P2Params p;
+    fill_params(p, a, lse, lse_ld);
+    int sms = 0;
+    const int st = sm_count(&sms);
+    if (st != GDA_OK) return st;
+    if (a.d == 64) return launch_lse_impl<64>(a, mQ1, mK1, mQ2, mK2, p, sms, stream);
+    if (a.d == 128) return launch_lse_impl<128>(a, mQ1, mK1, mQ2, mK2, p, sms, stream);
+    return GDA_ERR_UNSUPPORTED;
 }
 
 int launch_prefill_2pass(const PrefillArgs &a, void *workspace, cudaStream_t stream) {

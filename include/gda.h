@@ -198,6 +198,32 @@ int gda_attn_bwd(const float *q_sig, const float *k_sig, const float *q_noise,
 size_t gda_attn_bwd_workspace_size(int B, int L, int h_s, int d, int dv);
 
 /*
+ * Backward on the tensor cores: the gradients of gda_attn_bwd (same
+ * definitions, outputs, layouts and determinism) from bf16 inputs q_sig,
+ * k_sig, q_noise, k_noise, v and dy (layouts of gda_attn_fwd; dy [B, L, h_s,
+ * dv]); float32 lambda and float32 outputs.  Supported: d = 64, dv = 128.
+ * The maps' row statistics are recomputed (no forward state is passed); the
+ * norm's input gradient do is formed in float32 and rounded once to bf16,
+ * W = A1 - lambda A2, dS1 and dS2 are rounded to bf16 as tensor-core
+ * operands; every product accumulates in float32.  No atomics: each noise
+ * head's gradients accumulate over its group in one CTA.
+ *   workspace: device memory of at least gda_attn_bwd_bf16_workspace_size(B,
+ *   L, h_s, h_n, dv) bytes, 16-byte aligned, owned by the caller (row
+ *   statistics, do in bf16, D1 and D2).
+ *   Returns as gda_attn_bwd.
+ */
+int gda_attn_bwd_bf16(const void *q_sig, const void *k_sig, const void *q_noise,
+                      const void *k_noise, const void *v, const float *lambda,
+                      float lambda_init, const void *dy, float *dq_sig, float *dk_sig,
+                      float *dq_noise, float *dk_noise, float *dv_out, float *dlambda,
+                      int B, int L, int h_s, int h_n, int d, int dv, int causal,
+                      float eps, unsigned flags, void *workspace,
+                      size_t workspace_bytes, gda_stream_t stream);
+
+/* Bytes of workspace gda_attn_bwd_bf16 needs (0 for invalid sizes). */
+size_t gda_attn_bwd_bf16_workspace_size(int B, int L, int h_s, int h_n, int dv);
+
+/*
  * Bytes of device workspace gda_attn_decode needs for these sizes (it holds
  * the partial softmax states of the cache segments that the split kernel's
  * CTAs produce; the size does not depend on Lcap).  Returns 0 for invalid

@@ -403,3 +403,42 @@ def test_row_logsumexp_matches_library_and_normalises(causal):
     np.testing.assert_allclose(np.exp(s.numpy() - got[..., None]).sum(-1), 1.0, rtol=0, atol=1e-12)
     if causal:
         np.testing.assert_allclose(got[:, :, 0], s[:, :, 0, 0].numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal,norm", [(True, True), (False, False)])
+def test_gradient_magnitudes_bound_the_gradients(causal, norm):
+    """Triangle inequality: every sum of absolute terms is at least the
+    absolute value of the autograd gradient it belongs to."""
+    from oracle.ref_torch_grad import gda_backward, gda_grad_magnitudes
+    g = torch.Generator().manual_seed(81)
+    B, L, hs, hn, d, dv = 1, 9, 4, 2, 8, 16
+    args = [torch.randn(B, L, hs, d, generator=g, dtype=torch.float64),
+            torch.randn(B, L, hs, d, generator=g, dtype=torch.float64),
+            torch.randn(B, L, hn, d, generator=g, dtype=torch.float64),
+            torch.randn(B, L, hn, d, generator=g, dtype=torch.float64),
+            torch.randn(B, L, hs, dv, generator=g, dtype=torch.float64),
+            torch.rand(hs, generator=g, dtype=torch.float64)]
+    dy = torch.randn(B, L, hs, dv, generator=g, dtype=torch.float64)
+    grads = gda_backward(*args, 0.7, dy, causal=causal, norm=norm)
+    mags = gda_grad_magnitudes(*args, 0.7, dy, causal=causal, norm=norm)
+    for gr, m in zip(grads, mags):
+        assert gr.shape == m.shape
+        assert torch.all(m >= gr.abs() - 1e-12)
+
+
+def test_gradient_magnitudes_equal_gradients_when_terms_share_a_sign():
+    """lambda = 0, no norm, dy >= 0: every term of dv is non-negative, so the
+    magnitude equals dv itself; dlambda's magnitude is sum |do . O2|, equal to
+    -dlambda when every do . O2 is non-negative (dy >= 0 and V >= 0)."""
+    from oracle.ref_torch_grad import gda_backward, gda_grad_magnitudes
+    g = torch.Generator().manual_seed(82)
+    B, L, hs, hn, d, dv = 2, 7, 2, 1, 8, 16
+    q1, k1 = torch.randn(B, L, hs, d, generator=g, dtype=torch.float64), torch.randn(B, L, hs, d, generator=g, dtype=torch.float64)
+    q2, k2 = torch.randn(B, L, hn, d, generator=g, dtype=torch.float64), torch.randn(B, L, hn, d, generator=g, dtype=torch.float64)
+    v = torch.rand(B, L, hs, dv, generator=g, dtype=torch.float64)
+    dy = torch.rand(B, L, hs, dv, generator=g, dtype=torch.float64)
+    lam = torch.zeros(hs, dtype=torch.float64)
+    grads = gda_backward(q1, k1, q2, k2, v, lam, 0.5, dy, causal=True, norm=False)
+    mags = gda_grad_magnitudes(q1, k1, q2, k2, v, lam, 0.5, dy, causal=True, norm=False)
+    np.testing.assert_allclose(mags[4].numpy(), grads[4].numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(mags[5].numpy(), -grads[5].numpy(), rtol=0, atol=1e-12)
