@@ -472,6 +472,31 @@ def run_gda(args, world, rank, local):
     bw_tflops = bw_flops / (bw_ms * 1e-3) / 1e12
     del bw_in, bw_ws, bw_grads
 
+    # ---- tensor-core bf16 backward at the prefill workload's sizes
+    bb_in = [t.to(dev) for t in W.make_backward_inputs(w, seed=rank + 51)]
+    bb_ws = torch.empty(gda.gda_attn_bwd_bf16_workspace_size(w.B, w.L, w.h_s, w.h_n, w.dv), dtype=torch.uint8,
+                        device=dev)
+    bb_grads = gda.gda_attn_bwd_bf16(*bb_in[:6], w.lambda_init, bb_in[6], causal=w.causal, eps=w.eps,
+                                     workspace=bb_ws)
+
+    def bbstep():
+        gda.gda_attn_bwd_bf16(*bb_in[:6], w.lambda_init, bb_in[6], causal=w.causal, eps=w.eps, workspace=bb_ws,
+                              grads=bb_grads)
+
+    for _ in range(3):
+        bbstep()
+    torch.cuda.synchronize(dev)
+    bb_steps = 30
+    evg, evh = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evg.record(stream)
+    for _ in range(bb_steps):
+        bbstep()
+    evh.record(stream)
+    torch.cuda.synchronize(dev)
+    bb_ms = evg.elapsed_time(evh) / bb_steps
+    bb_tflops = backward_flops(w.B, w.L, w.h_s, w.h_n, w.d, w.dv) / (bb_ms * 1e-3) / 1e12
+    del bb_in, bb_ws, bb_grads
+
     # ---- lambda re-parameterisation for one layer's heads (launch-latency bound)
     g = torch.Generator().manual_seed(rank + 11)
     lvec = [(0.1 * torch.randn(w.h_s, w.d, generator=g)).to(dev) for _ in range(4)]
@@ -622,6 +647,13 @@ def run_gda(args, world, rank, local):
                          "roofline": {"bound": "tensor", "achieved": fl4 / (ms4["default"] * 1e-3) / 1e12,
                                       "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                       "frac": fl4 / (ms4["default"] * 1e-3) / 1e12 / peaks["bf16_tflops"]}},
+        "backward_bf16": {"workload": f"tensor-core gradients of q_sig, k_sig, q_noise, k_noise, v, lambda from bf16 "
+                                      f"inputs at B={w.B}, L={w.L}, {w.h_s}+{w.h_n} heads, d={w.d}, dv={w.dv}, causal",
+                          "value": bb_tflops, "unit": "TFLOP/s", "ms_per_step": bb_ms, "steps": bb_steps,
+                          "gpu_launches": 5 * bb_steps,
+                          "speedup_vs_f32": bw_ms / bb_ms,
+                          "roofline": {"bound": "tensor", "achieved": bb_tflops, "peak": peaks["bf16_tflops"],
+                                       "unit": "TFLOP/s", "frac": bb_tflops / peaks["bf16_tflops"]}},
         "backward_f32": {"workload": f"float32 gradients of q_sig, k_sig, q_noise, k_noise, v, lambda at "
                                      f"B={w.B}, L={w.L}, {w.h_s}+{w.h_n} heads, d={w.d}, dv={w.dv}, causal",
                          "value": bw_tflops, "unit": "TFLOP/s", "ms_per_step": bw_ms, "steps": bw_steps,

@@ -82,28 +82,39 @@ def assert_grad_close(got, ref, what=""):
             f"worst at {idx}: got {got[idx]!r} ref {ref[idx]!r}")
 
 
-GRAD_BF16_REL = 3e-2
+GRAD_BF16_REL = 2e-2
+GRAD_BF16_MAG = 2.0 ** -7
 
 
-def assert_grad_bf16_close(got, ref, what=""):
+def assert_grad_bf16_close(got, ref, mag, what=""):
     """Tensor-core gradients from bf16 operands:
-    |got - ref| <= 3e-2 (|ref| + rms_row(ref) + rms(ref)).
+    |got - ref| <= 2e-2 (|ref| + rms_row(ref) + rms(ref)) + 2^-7 mag,
+    mag = the oracle's sum of absolute terms of that gradient
+    (oracle.ref_torch_grad.gda_grad_magnitudes).
 
-    The kernels round the norm's input gradient and the score gradients
-    (W = A1 - lambda A2, dS1, dS2) to bf16 as tensor-core operands.  A float64
-    replay of exactly those roundings on the CPU (ragged shapes, groups of 1
-    to 4, L up to 512, causal and full) stays within 1.2e-2 of the float64
-    gradients in these units, so the bound leaves a 2.5x margin for float32
-    accumulation and the kernels' exponentials."""
-    got, ref = _np(got), _np(ref)
-    assert got.shape == ref.shape, (got.shape, ref.shape)
+    The kernels round P of the first pass, the norm's input gradient do and the
+    score gradients (W = A1 - lambda A2, dS1, dS2) to bf16 (relative error
+    2^-9 each).  Two kinds of error follow, and a float64 replay of exactly
+    those roundings on the CPU (41 ragged cases, groups of 1 to 4, L up to
+    512, causal and full; the replay reproduces the kernel's values to the
+    bit where checked) shows both:
+    - errors that scale with the output: the rounding of O1 and O2 reaches do
+      through o = O1 - lambda O2 and the norm; at most 1.2e-2 (|ref| +
+      rms_row + rms) for dv and 1.9e-2 elsewhere;
+    - errors that scale with the terms of a cancelling sum: in early causal
+      rows a gradient is a short sum of score gradients that add to ~0; there
+      the error stays below 0.46 x 2^-8 x mag.
+    The sum of the two bounds holds every replayed element with a margin of
+    at least 2x on its dominant term."""
+    got, ref, mag = _np(got), _np(ref), _np(mag)
+    assert got.shape == ref.shape == mag.shape, (got.shape, ref.shape, mag.shape)
     rms_all = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
     rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
-    bound = GRAD_BF16_REL * (np.abs(ref) + rms + rms_all)
+    bound = GRAD_BF16_REL * (np.abs(ref) + rms + rms_all) + GRAD_BF16_MAG * mag
     err = np.abs(got - ref)
     bad = ~(err <= bound)
     if bad.any():
         idx = np.unravel_index(np.argmax(np.where(bad, err / bound, 0)), err.shape)
         raise AssertionError(
-            f"{what}: {int(bad.sum())} of {bad.size} elements outside 3e-2(|ref|+rms_row+rms); "
-            f"worst at {idx}: got {got[idx]!r} ref {ref[idx]!r}")
+            f"{what}: {int(bad.sum())} of {bad.size} elements outside 2e-2(|ref|+rms_row+rms) + 2^-7 mag; "
+            f"worst at {idx}: got {got[idx]!r} ref {ref[idx]!r} mag {mag[idx]!r}")
