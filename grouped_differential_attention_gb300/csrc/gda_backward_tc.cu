@@ -89,6 +89,19 @@ __device__ __forceinline__ void issue_ts64(uint32_t tD, uint32_t tA, uint32_t ba
     }
 }
 
+// D[128 x N] (+)= A[128 x 64] B[64 x N]: A a K-major shared-memory tile
+// (128-byte rows, 128-byte swizzle), B as in issue_ts64.
+template <int N>
+__device__ __forceinline__ void issue_ss64(uint32_t tD, uint32_t aa, uint32_t ba, bool acc) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, N, 1);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint64_t a = smem_desc_sw128(aa + k * 32, 16, 1024);
+        const uint64_t b = smem_desc_sw128(ba + k * 2048, 64 * 128, 1024);
+        mma_ss(tD, a, b, idesc, (acc || k > 0) ? 1u : 0u);
+    }
+}
+
 // S[128 x 64] = A[128 x K] B[64 x K]^T with K-major operands: A in K/64
 // blocks of [128 x 64] (16 KiB apart), B in K/64 blocks of [64 x 64] (8 KiB apart).
 template <int K>
@@ -486,14 +499,17 @@ struct KvLayout {
     static constexpr int QST_BYTES = 2 * Q_BYTES + DO_BYTES + 1024;   // vectors padded to 1 KiB
     static constexpr int OFF_K1 = 0, OFF_K2 = K_BYTES, OFF_V = 2 * K_BYTES;
     static constexpr int OFF_Q = OFF_V + V_BYTES;
-    static constexpr int TILES = OFF_Q + QS * QST_BYTES;
+    static constexpr int W_BYTES = kBM * kN * 2;          // one of W / dS1 / dS2: 16 KiB
+    static constexpr int OFF_W = OFF_Q + QS * QST_BYTES;  // W | dS1 | dS2, K-major, 128-byte swizzle
+    static constexpr int TILES = OFF_W + 3 * W_BYTES;
 };
 
 struct KvCtrl {
     uint64_t g_full, g_empty;        // K2 of the item
     uint64_t h_full, h_empty;        // K1 and V of the current head
     uint64_t q_full[3], q_empty[3];  // query-side stages
-    uint64_t s_full, p_full;
+    uint64_t s_full, s_free;         // S^T tiles in TMEM / read into registers
+    uint64_t p_full, w_free;         // W, dS1, dS2 in shared memory / read by their products
     uint64_t acc_ready, acc_free;    // dV, dK1 of a head
     uint64_t k2_ready, k2_free;      // dK2 of an item
     uint64_t mma_idle;
@@ -524,7 +540,10 @@ __device__ __forceinline__ bool kv_item(const BwdTcParams &p, int r, int G, int 
     return true;
 }
 
-__global__ void __launch_bounds__(kThr, 1)
+constexpr int kEwKv = 512;          // dK/dV elementwise threads: 16 warps, four 16-column groups
+constexpr int kThrKv = 64 + kEwKv;
+
+__global__ void __launch_bounds__(kThrKv, 1)
 gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_constant__ CUtensorMap tmK2,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQ1,
                     const __grid_constant__ CUtensorMap tmQ2, const __grid_constant__ CUtensorMap tmdO,
@@ -550,11 +569,13 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
             mbar_init(&ctl->q_empty[s], 1);
         }
         mbar_init(&ctl->s_full, 1);
-        mbar_init(&ctl->p_full, kEw);
+        mbar_init(&ctl->s_free, kEwKv);
+        mbar_init(&ctl->p_full, kEwKv);
+        mbar_init(&ctl->w_free, 1);
         mbar_init(&ctl->acc_ready, 1);
-        mbar_init(&ctl->acc_free, kEw);
+        mbar_init(&ctl->acc_free, kEwKv);
         mbar_init(&ctl->k2_ready, 1);
-        mbar_init(&ctl->k2_free, kEw);
+        mbar_init(&ctl->k2_free, kEwKv);
         mbar_init(&ctl->mma_idle, 1);
         ctl->abort_flag = 0;
         fence_mbar_init();
@@ -629,9 +650,29 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
         if (elect_one()) {
             const uint32_t k1a = smem_u32(smem + LY::OFF_K1), k2a = smem_u32(smem + LY::OFF_K2);
             const uint32_t va = smem_u32(smem + LY::OFF_V), q0a = smem_u32(smem + LY::OFF_Q);
+            const uint32_t wa = smem_u32(smem + LY::OFF_W);
             uint32_t gq = 0, nh = 0;
             bool ok = true;
             int b, g, k0, i0, nq;
+            // dV, dK1 and dK2 updates of tile t (tile i of head hi of item r); they run
+            // after the logits of tile t + 1 were issued, so the tensor core computes
+            // those while the elementwise threads still work on tile t
+            auto finish = [&](uint32_t t, int i, int hi, int r) -> bool {
+                const int st = t % QS;
+                if (!wait_bar(&ctl->p_full, t & 1, p.err, abort_flag)) return false;
+                // accumulators of the previous head / item have been read
+                if (i == 0 && nh > 0 && !wait_bar(&ctl->acc_free, (nh - 1) & 1, p.err, abort_flag)) return false;
+                if (i == 0 && hi == 0 && r > 0 && !wait_bar(&ctl->k2_free, (r - 1) & 1, p.err, abort_flag))
+                    return false;
+                tc_fence_after();
+                const uint32_t sq = q0a + st * LY::QST_BYTES;
+                issue_ss64<kDV>(tmem + tdV, wa, sq + 2 * LY::Q_BYTES, i > 0);                     // dV += W dO
+                issue_ss64<kD>(tmem + tdK1, wa + LY::W_BYTES, sq, i > 0);                         // dK1 += dS1 Q1
+                issue_ss64<kD>(tmem + tdK2, wa + 2 * LY::W_BYTES, sq + LY::Q_BYTES, i > 0 || hi > 0);   // dK2 += dS2 Q2
+                mma_commit(&ctl->q_empty[st]);
+                mma_commit(&ctl->w_free);
+                return true;
+            };
             for (int r = 0; ok && kv_item(p, r, G, cid, b, g, k0, i0, nq); ++r) {
                 if (!wait_bar(&ctl->g_full, r & 1, p.err, abort_flag)) break;
                 for (int hi = 0; ok && hi < r_grp; ++hi) {
@@ -639,30 +680,18 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
                     for (int i = 0; i < nq; ++i) {
                         const int st = gq % QS;
                         if (!wait_bar(&ctl->q_full[st], (gq / QS) & 1, p.err, abort_flag)) { ok = false; break; }
+                        // the previous tile's logits have been read into registers
+                        if (gq > 0 && !wait_bar(&ctl->s_free, (gq - 1) & 1, p.err, abort_flag)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t sq = q0a + st * LY::QST_BYTES;
                         issue_nt<kD>(tmem + tS1, k1a, sq);                         // S1^T = K1 Q1^T
                         issue_nt<kD>(tmem + tS2, k2a, sq + LY::Q_BYTES);           // S2^T = K2 Q2^T
                         issue_nt<kDV>(tmem + tdP, va, sq + 2 * LY::Q_BYTES);       // dP^T = V dO^T
                         mma_commit(&ctl->s_full);
-                        if (!wait_bar(&ctl->p_full, gq & 1, p.err, abort_flag)) { ok = false; break; }
-                        // accumulators of the previous head / item have been read
-                        if (i == 0 && nh > 0 && !wait_bar(&ctl->acc_free, (nh - 1) & 1, p.err, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        if (i == 0 && hi == 0 && r > 0 && !wait_bar(&ctl->k2_free, (r - 1) & 1, p.err, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_ts64<kDV>(tmem + tdV, tmem + tS1, sq + 2 * LY::Q_BYTES, i > 0);   // dV += W dO
-                        issue_ts64<kD>(tmem + tdK1, tmem + tS2, sq, i > 0);                      // dK1 += dS1 Q1
-                        issue_ts64<kD>(tmem + tdK2, tmem + tdP, sq + LY::Q_BYTES, i > 0 || hi > 0);   // dK2 += dS2 Q2
-                        mma_commit(&ctl->q_empty[st]);
+                        if (i > 0 && !finish(gq - 1, i - 1, hi, r)) { ok = false; break; }
                         ++gq;
                     }
-                    if (!ok) break;
+                    if (!ok || !finish(gq - 1, nq - 1, hi, r)) { ok = false; break; }
                     mma_commit(&ctl->acc_ready);
                     mma_commit(&ctl->h_empty);
                     ++nh;
@@ -676,7 +705,7 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
         }
         __syncwarp();
     } else {
-        const int half = (warp - 2) / 4;
+        const int grp = (warp - 2) / 4;             // query columns [16 grp, 16 grp + 16) of each tile
         const int quarter = warp % 4;
         const int row = quarter * 32 + lane;        // key within the tile
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -684,13 +713,26 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
         uint32_t gq = 0, nh = 0;
         int b, g, k0, i0, nq;
         bool ok = true;
+        auto store16 = [&](float *dst, uint32_t taddr, float mul, bool kin) {
+            uint32_t o[16];
+            tmem_ld16(taddr, o);
+            tmem_ld_wait_regs16(o);
+            if (kin) {
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                    reinterpret_cast<float4 *>(dst)[v4] =
+                        make_float4(__uint_as_float(o[4 * v4]) * mul, __uint_as_float(o[4 * v4 + 1]) * mul,
+                                    __uint_as_float(o[4 * v4 + 2]) * mul, __uint_as_float(o[4 * v4 + 3]) * mul);
+            }
+        };
         for (int r = 0; ok && kv_item(p, r, G, cid, b, g, k0, i0, nq); ++r) {
             const int key = k0 + row;
+            const int wkey_last = k0 + quarter * 32 + 31;      // this warp's last key
             for (int hi = 0; ok && hi < r_grp; ++hi) {
                 const int h = g * r_grp + hi;
-                const float lam = p.lambda[h];
+                const float nlam = -p.lambda[h];
                 for (int i = 0; i < nq; ++i) {
-                    const int q0 = (i0 + i) * kN + half * 32;     // this half's first query column
+                    const int q0 = (i0 + i) * kN + grp * 16;     // this group's first query column
                     const int st = gq % QS;
                     // the stage's vectors were written by the copy engine: observe its barrier too
                     if (!warp_wait(&ctl->s_full, gq & 1, p.err, abort_flag) ||
@@ -699,42 +741,63 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
                         break;
                     }
                     tc_fence_after();
-                    uint32_t s1[32], s2[32], dp[32];
-                    tmem_ld32(tmem + lane_off + tS1 + half * 32, s1);
-                    tmem_ld32(tmem + lane_off + tS2 + half * 32, s2);
-                    tmem_ld32(tmem + lane_off + tdP + half * 32, dp);
-                    tmem_ld_wait_regs(s1);
-                    reg_fence(s2);
-                    reg_fence(dp);
+                    const uint32_t tcol = tmem + lane_off + grp * 16;
+                    uint32_t s1[16], s2[16], dp[16];
+                    tmem_ld16(tcol + tS1, s1);
+                    tmem_ld16(tcol + tS2, s2);
+                    tmem_ld16(tcol + tdP, dp);
+                    tmem_ld_wait_regs16(s1);
+                    reg_fence16(s2);
+                    reg_fence16(dp);
+                    tc_fence_before();
+                    mbar_arrive(&ctl->s_free);                  // the next tile's logits may overwrite S
                     const float *vec = reinterpret_cast<const float *>(smem + LY::OFF_Q + st * LY::QST_BYTES +
-                                                                       2 * LY::Q_BYTES + LY::DO_BYTES) + half * 32;
-                    uint32_t pw[16], pd1[16], pd2[16];
+                                                                       2 * LY::Q_BYTES + LY::DO_BYTES) + grp * 16;
+                    // every (key, query) pair of this warp and group is visible: no per-element mask
+                    const bool clean = q0 + 15 < p.L && wkey_last < p.L && (!p.causal || wkey_last <= q0);
+                    uint32_t pw[8], pd1[8], pd2[8];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
+                    for (int e = 0; e < 16; e += 2) {
                         float w2[2], a2[2], c2[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const int q = q0 + e + u;
-                            const bool vis = q < p.L && key < p.L && (!p.causal || key <= q);
-                            const float p1 = fast_exp2(__uint_as_float(s1[e + u]) * sl2 - vec[e + u]);
-                            const float p2 = fast_exp2(__uint_as_float(s2[e + u]) * sl2 - vec[64 + e + u]);
+                            const float p1 = fast_exp2(fmaf(__uint_as_float(s1[e + u]), sl2, -vec[e + u]));
+                            const float np2 = nlam * fast_exp2(fmaf(__uint_as_float(s2[e + u]), sl2, -vec[64 + e + u]));
                             const float dpv = __uint_as_float(dp[e + u]);
-                            const float w = fmaf(-lam, p2, p1);
-                            const float ds1 = p1 * (dpv - vec[128 + e + u]);
-                            const float ds2 = -lam * p2 * (dpv - vec[192 + e + u]);
-                            w2[u] = vis ? w : 0.f;
-                            a2[u] = vis ? ds1 : 0.f;
-                            c2[u] = vis ? ds2 : 0.f;
+                            w2[u] = p1 + np2;
+                            a2[u] = p1 * (dpv - vec[128 + e + u]);
+                            c2[u] = np2 * (dpv - vec[192 + e + u]);
+                        }
+                        if (!clean) {
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int q = q0 + e + u;
+                                const bool vis = q < p.L && key < p.L && (!p.causal || key <= q);
+                                w2[u] = vis ? w2[u] : 0.f;
+                                a2[u] = vis ? a2[u] : 0.f;
+                                c2[u] = vis ? c2[u] : 0.f;
+                            }
                         }
                         pw[e / 2] = pack_bf16x2(w2[0], w2[1]);
                         pd1[e / 2] = pack_bf16x2(a2[0], a2[1]);
                         pd2[e / 2] = pack_bf16x2(c2[0], c2[1]);
                     }
-                    tmem_st16(tmem + lane_off + tS1 + half * 32, pw);
-                    tmem_st16(tmem + lane_off + tS2 + half * 32, pd1);
-                    tmem_st16(tmem + lane_off + tdP + half * 32, pd2);
-                    tmem_st_wait();
-                    tc_fence_before();
+                    // the previous tile's products have read W / dS1 / dS2
+                    if (gq > 0 && !warp_wait(&ctl->w_free, (gq - 1) & 1, p.err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    // row `row` of each K-major tile: 16-byte chunks 2 grp and 2 grp + 1 (query
+                    // columns 16 grp .. 16 grp + 15), 128-byte swizzle: chunk c at c ^ (row % 8)
+                    uint8_t *wrow = smem + LY::OFF_W + row * 128;
+                    const int c0 = ((2 * grp) ^ (row & 7)) * 16, c1 = ((2 * grp + 1) ^ (row & 7)) * 16;
+                    *reinterpret_cast<uint4 *>(wrow + c0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    *reinterpret_cast<uint4 *>(wrow + c1) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+                    *reinterpret_cast<uint4 *>(wrow + LY::W_BYTES + c0) = make_uint4(pd1[0], pd1[1], pd1[2], pd1[3]);
+                    *reinterpret_cast<uint4 *>(wrow + LY::W_BYTES + c1) = make_uint4(pd1[4], pd1[5], pd1[6], pd1[7]);
+                    *reinterpret_cast<uint4 *>(wrow + 2 * LY::W_BYTES + c0) = make_uint4(pd2[0], pd2[1], pd2[2], pd2[3]);
+                    *reinterpret_cast<uint4 *>(wrow + 2 * LY::W_BYTES + c1) = make_uint4(pd2[4], pd2[5], pd2[6], pd2[7]);
+                    fence_proxy_async_smem();                   // visible to the tensor core's reads
                     mbar_arrive(&ctl->p_full);
                     ++gq;
                 }
@@ -744,37 +807,15 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
                 tc_fence_after();
                 if (ok) {
                     const bool kin = key < p.L;
-                    float *dvrow = p.dvo + ((static_cast<size_t>(b) * p.L + (kin ? key : 0)) * p.hs + h) * kDV + half * 64;
-                    float *dkrow = p.dk1 + ((static_cast<size_t>(b) * p.L + (kin ? key : 0)) * p.hs + h) * kD + half * 32;
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        uint32_t o[32];
-                        tmem_ld32(tmem + lane_off + tdV + half * 64 + cc * 32, o);
-                        tmem_ld_wait_regs(o);
-                        if (kin) {
-#pragma unroll
-                            for (int v4 = 0; v4 < 8; ++v4)
-                                reinterpret_cast<float4 *>(dvrow + cc * 32)[v4] =
-                                    make_float4(__uint_as_float(o[4 * v4]), __uint_as_float(o[4 * v4 + 1]),
-                                                __uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3]));
-                        }
-                    }
-                    uint32_t o[32];
-                    tmem_ld32(tmem + lane_off + tdK1 + half * 32, o);
-                    tmem_ld_wait_regs(o);
-                    if (kin) {
-#pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            reinterpret_cast<float4 *>(dkrow)[v4] =
-                                make_float4(__uint_as_float(o[4 * v4]) * p.scale, __uint_as_float(o[4 * v4 + 1]) * p.scale,
-                                            __uint_as_float(o[4 * v4 + 2]) * p.scale,
-                                            __uint_as_float(o[4 * v4 + 3]) * p.scale);
-                    }
+                    const size_t kix = (static_cast<size_t>(b) * p.L + (kin ? key : 0)) * p.hs + h;
+                    store16(p.dvo + kix * kDV + grp * 32, tmem + lane_off + tdV + grp * 32, 1.f, kin);
+                    store16(p.dvo + kix * kDV + grp * 32 + 16, tmem + lane_off + tdV + grp * 32 + 16, 1.f, kin);
+                    store16(p.dk1 + kix * kD + grp * 16, tmem + lane_off + tdK1 + grp * 16, p.scale, kin);
                 }
                 tc_fence_before();
                 mbar_arrive(&ctl->acc_free);
                 ++nh;
-                if (bar_red_or(1, kEw, !ok || *abort_flag)) ok = false;
+                if (bar_red_or(1, kEwKv, !ok || *abort_flag)) ok = false;
             }
             if (!ok) break;
             // ---- dK2 of the item (summed over the group's heads)
@@ -782,22 +823,12 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
             tc_fence_after();
             if (ok) {
                 const bool kin = key < p.L;
-                float *dkrow = p.dk2 + ((static_cast<size_t>(b) * p.L + (kin ? key : 0)) * p.hn + g) * kD + half * 32;
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + tdK2 + half * 32, o);
-                tmem_ld_wait_regs(o);
-                if (kin) {
-#pragma unroll
-                    for (int v4 = 0; v4 < 8; ++v4)
-                        reinterpret_cast<float4 *>(dkrow)[v4] =
-                            make_float4(__uint_as_float(o[4 * v4]) * p.scale, __uint_as_float(o[4 * v4 + 1]) * p.scale,
-                                        __uint_as_float(o[4 * v4 + 2]) * p.scale,
-                                        __uint_as_float(o[4 * v4 + 3]) * p.scale);
-                }
+                const size_t kix = (static_cast<size_t>(b) * p.L + (kin ? key : 0)) * p.hn + g;
+                store16(p.dk2 + kix * kD + grp * 16, tmem + lane_off + tdK2 + grp * 16, p.scale, kin);
             }
             tc_fence_before();
             mbar_arrive(&ctl->k2_free);
-            if (bar_red_or(1, kEw, !ok || *abort_flag)) break;
+            if (bar_red_or(1, kEwKv, !ok || *abort_flag)) break;
         }
         tmem_ld_wait();
     }
@@ -831,7 +862,7 @@ struct QCtrl {
     uint64_t g_full, g_empty;          // Q2 of the item
     uint64_t h_full, h_empty;          // Q1 and dO of the current head
     uint64_t k_full[3], k_empty[3];
-    uint64_t s_full, p_full;
+    uint64_t s_full[2], p_full[2];     // [S buffer]
     uint64_t acc_ready, acc_free;      // dQ1 of a head
     uint64_t q2_ready, q2_free;        // dQ2 of an item
     uint64_t mma_idle;
@@ -885,8 +916,10 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
             mbar_init(&ctl->k_full[s], 1);
             mbar_init(&ctl->k_empty[s], 1);
         }
-        mbar_init(&ctl->s_full, 1);
-        mbar_init(&ctl->p_full, kEw);
+        for (int bb = 0; bb < 2; ++bb) {
+            mbar_init(&ctl->s_full[bb], 1);
+            mbar_init(&ctl->p_full[bb], kEw);
+        }
         mbar_init(&ctl->acc_ready, 1);
         mbar_init(&ctl->acc_free, kEw);
         mbar_init(&ctl->q2_ready, 1);
@@ -904,8 +937,10 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort_flag = &ctl->abort_flag;
-    // TMEM: S1 [0,64) | S2 [64,128) | dP [128,192) | dQ1 [192,256) | dQ2 [256,320)
-    constexpr uint32_t tS1 = 0, tS2 = 64, tdP = 128, tdQ1 = 192, tdQ2 = 256;
+    // TMEM: two S buffers of S1 | S2 | dP (64 columns each) at [0,192) and
+    // [192,384) | dQ1 [384,448) | dQ2 [448,512).  The logits of tile j+2 are
+    // computed while the elementwise threads work on tile j+1.
+    constexpr uint32_t kSB = 192, tS1 = 0, tS2 = 64, tdP = 128, tdQ1 = 384, tdQ2 = 448;
 
     if (warp == 0) {
         if (elect_one()) {
@@ -965,16 +1000,26 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                 if (!wait_bar(&ctl->g_full, r & 1, p.err, abort_flag)) break;
                 for (int hi = 0; ok && hi < r_grp; ++hi) {
                     if (!wait_bar(&ctl->h_full, nh & 1, p.err, abort_flag)) { ok = false; break; }
-                    for (int j = 0; j < nkv; ++j) {
-                        const int st = gk % KS;
-                        if (!wait_bar(&ctl->k_full[st], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
+                    // logits of tile t into S buffer (gk + t) & 1
+                    auto issue_s = [&](int t) -> bool {
+                        const uint32_t gt = gk + t;
+                        const int st = gt % KS;
+                        if (!wait_bar(&ctl->k_full[st], (gt / KS) & 1, p.err, abort_flag)) return false;
                         tc_fence_after();
                         const uint32_t sk = k0a + st * LY::KST_BYTES;
-                        issue_nt<kD>(tmem + tS1, q1a, sk);                         // S1 = Q1 K1^T
-                        issue_nt<kD>(tmem + tS2, q2a, sk + LY::K_BYTES);           // S2 = Q2 K2^T
-                        issue_nt<kDV>(tmem + tdP, doa, sk + 2 * LY::K_BYTES);      // dP = dO V^T
-                        mma_commit(&ctl->s_full);
-                        if (!wait_bar(&ctl->p_full, gk & 1, p.err, abort_flag)) { ok = false; break; }
+                        const uint32_t sb = tmem + (gt & 1) * kSB;
+                        issue_nt<kD>(sb + tS1, q1a, sk);                           // S1 = Q1 K1^T
+                        issue_nt<kD>(sb + tS2, q2a, sk + LY::K_BYTES);             // S2 = Q2 K2^T
+                        issue_nt<kDV>(sb + tdP, doa, sk + 2 * LY::K_BYTES);        // dP = dO V^T
+                        mma_commit(&ctl->s_full[gt & 1]);
+                        return true;
+                    };
+                    for (int t = 0; ok && t < 2 && t < nkv; ++t) ok = issue_s(t);
+                    for (int j = 0; ok && j < nkv; ++j) {
+                        const uint32_t gj = gk + j;
+                        const int st = gj % KS;
+                        const int bb = gj & 1;
+                        if (!wait_bar(&ctl->p_full[bb], (gj >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
                         if (j == 0 && nh > 0 && !wait_bar(&ctl->acc_free, (nh - 1) & 1, p.err, abort_flag)) {
                             ok = false;
                             break;
@@ -984,11 +1029,15 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                             break;
                         }
                         tc_fence_after();
-                        issue_ts64<kD>(tmem + tdQ1, tmem + tS1, sk, j > 0);                        // dQ1 += dS1 K1
-                        issue_ts64<kD>(tmem + tdQ2, tmem + tS2, sk + LY::K_BYTES, j > 0 || hi > 0);  // dQ2 += dS2 K2
+                        const uint32_t sk = k0a + st * LY::KST_BYTES;
+                        const uint32_t sb = tmem + bb * kSB;
+                        issue_ts64<kD>(tmem + tdQ1, sb + tS1, sk, j > 0);                          // dQ1 += dS1 K1
+                        issue_ts64<kD>(tmem + tdQ2, sb + tS2, sk + LY::K_BYTES, j > 0 || hi > 0);  // dQ2 += dS2 K2
                         mma_commit(&ctl->k_empty[st]);
-                        ++gk;
+                        // the buffer just read by those products takes the logits of tile j + 2
+                        if (j + 2 < nkv) ok = issue_s(j + 2);
                     }
+                    gk += nkv;
                     if (!ok) break;
                     mma_commit(&ctl->acc_ready);
                     mma_commit(&ctl->h_empty);
@@ -1023,15 +1072,16 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                 const float D1 = in ? p.D1[(static_cast<size_t>(b) * p.hs + h) * p.Lp + qrow] : 0.f;
                 const float D2 = in ? p.D2[(static_cast<size_t>(b) * p.hs + h) * p.Lp + qrow] : 0.f;
                 for (int j = 0; j < nkv; ++j) {
-                    if (!warp_wait(&ctl->s_full, gk & 1, p.err, abort_flag)) {
+                    const uint32_t sb = tmem + lane_off + (gk & 1) * kSB;
+                    if (!warp_wait(&ctl->s_full[gk & 1], (gk >> 1) & 1, p.err, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     uint32_t s1[32], s2[32], dp[32];
-                    tmem_ld32(tmem + lane_off + tS1 + half * 32, s1);
-                    tmem_ld32(tmem + lane_off + tS2 + half * 32, s2);
-                    tmem_ld32(tmem + lane_off + tdP + half * 32, dp);
+                    tmem_ld32(sb + tS1 + half * 32, s1);
+                    tmem_ld32(sb + tS2 + half * 32, s2);
+                    tmem_ld32(sb + tdP + half * 32, dp);
                     tmem_ld_wait_regs(s1);
                     reg_fence(s2);
                     reg_fence(dp);
@@ -1054,11 +1104,11 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                         pd1[e / 2] = pack_bf16x2(a2[0], a2[1]);
                         pd2[e / 2] = pack_bf16x2(c2[0], c2[1]);
                     }
-                    tmem_st16(tmem + lane_off + tS1 + half * 32, pd1);
-                    tmem_st16(tmem + lane_off + tS2 + half * 32, pd2);
+                    tmem_st16(sb + tS1 + half * 32, pd1);
+                    tmem_st16(sb + tS2 + half * 32, pd2);
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(&ctl->p_full);
+                    mbar_arrive(&ctl->p_full[gk & 1]);
                     ++gk;
                 }
                 ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
@@ -1120,10 +1170,18 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
 __global__ void __launch_bounds__(256) gda_bwd_dlambda_kernel(const BwdTcParams p) {
     __shared__ float red[256];
     const int h = blockIdx.x;
-    float acc = 0.f;
-    for (int b = 0; b < p.B; ++b)
-        for (int i = threadIdx.x; i < p.L; i += blockDim.x) acc += p.D2[(static_cast<size_t>(b) * p.hs + h) * p.Lp + i];
-    red[threadIdx.x] = acc;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight loads in flight per thread
+    for (int b = 0; b < p.B; ++b) {
+        const float *row = p.D2 + (static_cast<size_t>(b) * p.hs + h) * p.Lp;
+        for (int i0 = 0; i0 < p.L; i0 += 8 * 256) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * 256 + static_cast<int>(threadIdx.x);
+                if (i < p.L) acc[u] += row[i];
+            }
+        }
+    }
+    red[threadIdx.x] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     __syncthreads();
     for (int s = 128; s > 0; s >>= 1) {
         if (static_cast<int>(threadIdx.x) < s) red[threadIdx.x] += red[threadIdx.x + s];
@@ -1223,7 +1281,7 @@ int launch_backward_tc(const BackwardTcArgs &a, cudaStream_t stream) {
     gda_bwd_prep_kernel<<<static_cast<unsigned>(gp), kThr, smem_p, stream>>>(q1_128, k1_64, q2_128, k2_64, v_64, p);
     long long gkv = nqt * a.B * a.hn;
     if (gkv > sms) gkv = sms;
-    gda_bwd_dkdv_kernel<<<static_cast<unsigned>(gkv), kThr, smem_kv, stream>>>(k1_128, k2_128, v_128, q1_64, q2_64,
+    gda_bwd_dkdv_kernel<<<static_cast<unsigned>(gkv), kThrKv, smem_kv, stream>>>(k1_128, k2_128, v_128, q1_64, q2_64,
                                                                                do_64, p);
     gda_bwd_dq_kernel<<<static_cast<unsigned>(gkv), kThr, smem_q, stream>>>(q1_128, q2_128, do_128, k1_64, k2_64,
                                                                             v_64, p);

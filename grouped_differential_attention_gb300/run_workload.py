@@ -4,6 +4,7 @@
         gda_3to1_prefill_bf16_B4_L2048_h12+4_d64_dv128 --launches 3
     python -m grouped_differential_attention_gb300.run_workload decode --launches 3
     python -m grouped_differential_attention_gb300.run_workload backward --launches 1
+    python -m grouped_differential_attention_gb300.run_workload backward_bf16 --launches 3
     python -m grouped_differential_attention_gb300.run_workload prefill2pass --launches 3
 
 Inputs are the seeded synthetic tensors of ``workloads``; prints the mean
@@ -23,7 +24,7 @@ from grouped_differential_attention_gb300 import workloads as W
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=["prefill", "prefill2pass", "decode", "backward"])
+    ap.add_argument("kind", choices=["prefill", "prefill2pass", "decode", "backward", "backward_bf16"])
     ap.add_argument("workload", nargs="?", default=None)
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args(argv)
@@ -45,6 +46,16 @@ def main(argv=None):
 
         def launch():
             gda.gda_attn_fwd_2pass(*inp, w.lambda_init, causal=w.causal, eps=w.eps, out=out, workspace=ws)
+    elif args.kind == "backward_bf16":
+        w = W.PREFILL_WORKLOADS[args.workload or W.GDA3_PREFILL_L2048.name]
+        inp = [t.to(dev) for t in W.make_backward_inputs(w)]
+        ws = torch.empty(gda.gda_attn_bwd_bf16_workspace_size(w.B, w.L, w.h_s, w.h_n, w.dv), dtype=torch.uint8,
+                         device=dev)
+        grads = gda.gda_attn_bwd_bf16(*inp[:6], w.lambda_init, inp[6], causal=w.causal, eps=w.eps, workspace=ws)
+
+        def launch():
+            gda.gda_attn_bwd_bf16(*inp[:6], w.lambda_init, inp[6], causal=w.causal, eps=w.eps, workspace=ws,
+                                  grads=grads)
     elif args.kind == "backward":
         # float32 gradients at a prefill workload's sizes (default: the 3:1 B=4 L=2048 one)
         w = W.PREFILL_WORKLOADS[args.workload or W.GDA3_PREFILL_L2048.name]
