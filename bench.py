@@ -446,6 +446,32 @@ def run_gda(args, world, rank, local):
         ms4[tag] = ev0.elapsed_time(ev1) / n4
     del in4, out4
 
+    # ---- one attention training step: forward, then the tensor-core backward of its inputs
+    tr_in = [t.to(dev) for t in W.make_backward_inputs(w, seed=rank + 61)]
+    tr_out = torch.empty((w.B, w.L, w.h_s, w.dv), dtype=torch.bfloat16, device=dev)
+    tr_ws = torch.empty(gda.gda_attn_bwd_bf16_workspace_size(w.B, w.L, w.h_s, w.h_n, w.dv), dtype=torch.uint8,
+                        device=dev)
+    tr_grads = gda.gda_attn_bwd_bf16(*tr_in[:6], w.lambda_init, tr_in[6], causal=w.causal, eps=w.eps,
+                                     workspace=tr_ws)
+
+    def trstep():
+        gda.gda_attn_fwd(*tr_in[:6], w.lambda_init, causal=w.causal, eps=w.eps, out=tr_out)
+        gda.gda_attn_bwd_bf16(*tr_in[:6], w.lambda_init, tr_in[6], causal=w.causal, eps=w.eps, workspace=tr_ws,
+                              grads=tr_grads)
+
+    for _ in range(3):
+        trstep()
+    torch.cuda.synchronize(dev)
+    tr_steps = 30
+    evi, evj = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evi.record(stream)
+    for _ in range(tr_steps):
+        trstep()
+    evj.record(stream)
+    torch.cuda.synchronize(dev)
+    tr_ms = evi.elapsed_time(evj) / tr_steps
+    del tr_in, tr_out, tr_ws, tr_grads
+
     # ---- float32 backward (gradients of all six inputs) at the prefill workload's sizes
     bw_in = [t.to(dev) for t in W.make_backward_inputs(w, dtype="f32", seed=rank + 31)]
     bw_ws = torch.empty(gda.gda_attn_bwd_workspace_size(w.B, w.L, w.h_s, w.d, w.dv), dtype=torch.uint8,
@@ -654,6 +680,12 @@ def run_gda(args, world, rank, local):
                           "speedup_vs_f32": bw_ms / bb_ms,
                           "roofline": {"bound": "tensor", "achieved": bb_tflops, "peak": peaks["bf16_tflops"],
                                        "unit": "TFLOP/s", "frac": bb_tflops / peaks["bf16_tflops"]}},
+        "train_step": {"workload": f"gda_attn_fwd then gda_attn_bwd_bf16 at B={w.B}, L={w.L}, {w.h_s}+{w.h_n} heads, "
+                                   f"d={w.d}, dv={w.dv}, causal",
+                       "value": w.B * w.L / (tr_ms * 1e-3), "unit": "tokens/s", "ms_per_step": tr_ms,
+                       "steps": tr_steps, "gpu_launches": 6 * tr_steps,
+                       "tflops": (prefill_flops(w.B, w.L, w.h_s, w.h_n, w.d, w.dv, w.causal)
+                                  + backward_flops(w.B, w.L, w.h_s, w.h_n, w.d, w.dv)) / (tr_ms * 1e-3) / 1e12},
         "backward_f32": {"workload": f"float32 gradients of q_sig, k_sig, q_noise, k_noise, v, lambda at "
                                      f"B={w.B}, L={w.L}, {w.h_s}+{w.h_n} heads, d={w.d}, dv={w.dv}, causal",
                          "value": bw_tflops, "unit": "TFLOP/s", "ms_per_step": bw_ms, "steps": bw_steps,
