@@ -3,6 +3,7 @@
     python -m grouped_differential_attention_gb300.run_workload prefill \
         gda_3to1_prefill_bf16_B4_L2048_h12+4_d64_dv128 --launches 3
     python -m grouped_differential_attention_gb300.run_workload decode --launches 3
+    python -m grouped_differential_attention_gb300.run_workload decode_fp8 --launches 3
     python -m grouped_differential_attention_gb300.run_workload backward --launches 1
     python -m grouped_differential_attention_gb300.run_workload backward_bf16 --launches 3
     python -m grouped_differential_attention_gb300.run_workload prefill2pass --launches 3
@@ -24,7 +25,7 @@ from grouped_differential_attention_gb300 import workloads as W
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=["prefill", "prefill2pass", "decode", "backward", "backward_bf16"])
+    ap.add_argument("kind", choices=["prefill", "prefill2pass", "decode", "decode_fp8", "backward", "backward_bf16"])
     ap.add_argument("workload", nargs="?", default=None)
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args(argv)
@@ -67,6 +68,15 @@ def main(argv=None):
         def launch():
             gda.gda_attn_bwd(*inp[:6], w.lambda_init, inp[6], causal=w.causal, eps=w.eps, workspace=ws,
                              grads=grads)
+    elif args.kind == "decode_fp8":
+        w = W.GDA3_DECODE_B64
+        inp = [t.to(dev) for t in W.make_decode_inputs_fp8(w)]
+        out = torch.empty((w.B, w.h_s, w.dv), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(gda.gda_attn_decode_workspace_size(w.B, w.Lcap, w.h_s, w.h_n, w.dv),
+                         dtype=torch.uint8, device=dev)
+
+        def launch():
+            gda.gda_attn_decode_fp8(*inp, w.lambda_init, eps=w.eps, out=out, workspace=ws)
     else:
         w = W.GDA3_DECODE_B64
         inp = [t.to(dev) for t in W.make_decode_inputs(w)]
