@@ -17,8 +17,9 @@
 //   dlambda_h = -sum_{b,i} D2_i
 //
 // Kernels (all persistent, roles as in the prefill kernels: warp 0 TMA
-// producer, warp 1 TMEM allocator + single-thread MMA issuer, warps 2-9 the
-// elementwise threads, warp 2 + 4w.. taking column half w of each tile):
+// producer, warp 1 TMEM allocator + single-thread MMA issuer, warps 2-17 the
+// elementwise threads, warps 2 + 4c .. 5 + 4c taking the 16-column group c of
+// each 64-column tile):
 //   pass 1 (gda_lse_tc_kernel, shared with the two-pass prefill): base-2
 //          log-sum-exp of every signal and noise map row;
 //   prep   (gda_bwd_prep_kernel): per (128 query rows, b, h) both maps with
@@ -49,8 +50,6 @@
 namespace gda {
 namespace {
 
-constexpr int kThr = 320;
-constexpr int kEw = 256;           // elementwise threads (warps 2-9)
 constexpr int kD = 64;
 constexpr int kDV = 128;
 constexpr int kN = 64;             // N-side tile
@@ -75,17 +74,17 @@ __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint3
         : "memory");
 }
 
-// TS MMA: D[128 x N] (+)= A[128 x 64] B[64 x N]; A = bf16 pairs in TMEM with
-// the split layout (rows 0-31 of K in columns tA .. tA+15, rows 32-63 in
-// tA+32 .. tA+47); B = MN-major smem tile of 64 K-rows, N/64 column blocks
-// 8 KiB apart (128-byte rows, 128-byte swizzle).
+// TS MMA: D[128 x N] (+)= A[128 x 64] B[64 x N]; A = bf16 pairs in TMEM,
+// written by four 16-column groups (K rows 16k .. 16k+15 in TMEM columns
+// tA + 16k .. tA + 16k + 7); B = MN-major smem tile of 64 K-rows, N/64
+// column blocks 8 KiB apart (128-byte rows, 128-byte swizzle).
 template <int N>
-__device__ __forceinline__ void issue_ts64(uint32_t tD, uint32_t tA, uint32_t ba, bool acc) {
+__device__ __forceinline__ void issue_ts64q(uint32_t tD, uint32_t tA, uint32_t ba, bool acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, N, 1);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const uint64_t b = smem_desc_sw128(ba + k * 2048, 64 * 128, 1024);
-        mma_ts(tD, tA + (k / 2) * 32 + (k % 2) * 8, b, idesc, (acc || k > 0) ? 1u : 0u);
+        mma_ts(tD, tA + k * 16, b, idesc, (acc || k > 0) ? 1u : 0u);
     }
 }
 
@@ -107,6 +106,13 @@ __device__ __forceinline__ void issue_ss64(uint32_t tD, uint32_t aa, uint32_t ba
 template <int K>
 __device__ __forceinline__ void issue_nt(uint32_t tS, uint32_t aa, uint32_t ba) {
     issue_qk<K, kN>(tS, aa, ba);
+}
+
+// 32 lanes x 32 bit, 8 consecutive columns per thread.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -133,8 +139,8 @@ struct PrepCtrl {
     uint64_t o_final, o_free, mma_idle;
     uint32_t tmem_base;
     int abort_flag;
-    float x1[2][kBM], x2[2][kBM];      // per-half partial sums, exchange 1 (ss, dy.o)
-    float y1[2][kBM], y2[2][kBM];      // exchange 2 (D1, D2)
+    float x1[4][kBM], x2[4][kBM];      // per-group partial sums, exchange 1 (ss, dy.o)
+    float y1[4][kBM], y2[4][kBM];      // exchange 2 (D1, D2)
 };
 
 constexpr int prep_smem_bytes() {
@@ -159,7 +165,10 @@ __device__ __forceinline__ bool prep_item(const BwdTcParams &p, int r, int G, in
     return true;
 }
 
-__global__ void __launch_bounds__(kThr, 1)
+constexpr int kEwP = 512;           // prep elementwise threads: 16 warps, four column groups
+constexpr int kThrP = 64 + kEwP;
+
+__global__ void __launch_bounds__(kThrP, 1)
 gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CUtensorMap tmK1,
                     const __grid_constant__ CUtensorMap tmQ2, const __grid_constant__ CUtensorMap tmK2,
                     const __grid_constant__ CUtensorMap tmV, const BwdTcParams p) {
@@ -186,10 +195,10 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
         }
         for (int bb = 0; bb < 2; ++bb) {
             mbar_init(&ctl->s_full[bb], 1);
-            mbar_init(&ctl->p_full[bb], kEw);
+            mbar_init(&ctl->p_full[bb], kEwP);
         }
         mbar_init(&ctl->o_final, 1);
-        mbar_init(&ctl->o_free, kEw);
+        mbar_init(&ctl->o_free, kEwP);
         mbar_init(&ctl->mma_idle, 1);
         ctl->abort_flag = 0;
         fence_mbar_init();
@@ -299,8 +308,8 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                     if (!wait_bar(&ctl->v_full[gv % VS], (gv / VS) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t va = v0a + (gv % VS) * LY::V_BYTES;
-                    issue_ts64<kDV>(tmem, tmem + tS1_0 + bb * kN, va, j > 0);
-                    issue_ts64<kDV>(tmem + tO2, tmem + tS2_0 + bb * kN, va, j > 0);
+                    issue_ts64q<kDV>(tmem, tmem + tS1_0 + bb * kN, va, j > 0);
+                    issue_ts64q<kDV>(tmem + tO2, tmem + tS2_0 + bb * kN, va, j > 0);
                     mma_commit(&ctl->v_empty[gv % VS]);
                     const int jn = j + 2;
                     if (jn < nkv) {
@@ -326,7 +335,7 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
         }
         __syncwarp();
     } else {
-        const int half = (warp - 2) / 4;
+        const int grp = (warp - 2) / 4;             // key columns [16 grp, +16) of each tile; dv columns [32 grp, +32)
         const int quarter = warp % 4;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -351,18 +360,18 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tS1 = tmem + lane_off + tS1_0 + bb * kN + half * 32;
-                const uint32_t tS2 = tmem + lane_off + tS2_0 + bb * kN + half * 32;
-                uint32_t r1[32], r2[32];
-                tmem_ld32(tS1, r1);
-                tmem_ld32(tS2, r2);
-                tmem_ld_wait_regs(r1);
-                reg_fence(r2);
-                const int k0 = j * kN + half * 32;
-                const bool need_mask = k0 + 31 > last_key;
-                uint32_t pk1[16], pk2[16];
+                const uint32_t tS1 = tmem + lane_off + tS1_0 + bb * kN + grp * 16;
+                const uint32_t tS2 = tmem + lane_off + tS2_0 + bb * kN + grp * 16;
+                uint32_t r1[16], r2[16];
+                tmem_ld16(tS1, r1);
+                tmem_ld16(tS2, r2);
+                tmem_ld_wait_regs16(r1);
+                reg_fence16(r2);
+                const int k0 = j * kN + grp * 16;
+                const bool need_mask = k0 + 15 > last_key;
+                uint32_t pk1[8], pk2[8];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
+                for (int e = 0; e < 16; e += 2) {
                     float x0 = __uint_as_float(r1[e]), x1 = __uint_as_float(r1[e + 1]);
                     float y0 = __uint_as_float(r2[e]), y1 = __uint_as_float(r2[e + 1]);
                     ffma2(x0, x1, sl2, sl2, neg1, neg1);
@@ -378,36 +387,36 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                     pk1[e / 2] = pack_bf16x2(x0, x1);
                     pk2[e / 2] = pack_bf16x2(y0, y1);
                 }
-                tmem_st16(tS1, pk1);
-                tmem_st16(tS2, pk2);
+                tmem_st8(tS1, pk1);
+                tmem_st8(tS2, pk2);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&ctl->p_full[bb]);
             }
             tmem_ld_wait();
 
-            // ---- epilogue: o, the norm's input gradient, D1, D2
+            // ---- epilogue: o, the norm's input gradient, D1, D2 (this group: 32 dv columns)
             ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
             if (ok) ok = warp_wait(&ctl->o_final, r & 1, p.err, abort_flag);
             tc_fence_after();
-            const int c0 = half * 64;                   // this half's dv columns
+            const int c0 = grp * 32;
             const size_t rowix = (static_cast<size_t>(b) * p.L + (in ? qrow : 0)) * p.hs + h;
             const uint4 *dyrow = reinterpret_cast<const uint4 *>(p.dy + rowix * kDV + c0);
             float ss = 0.f, dyo = 0.f;
             if (ok) {
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t o1[32], o2[32];
-                    tmem_ld32(tmem + lane_off + c0 + cc * 32, o1);
-                    tmem_ld32(tmem + lane_off + tO2 + c0 + cc * 32, o2);
-                    tmem_ld_wait_regs(o1);
-                    reg_fence(o2);
-                    uint4 dq[4];
+                    uint32_t o1[16], o2[16];
+                    tmem_ld16(tmem + lane_off + c0 + cc * 16, o1);
+                    tmem_ld16(tmem + lane_off + tO2 + c0 + cc * 16, o2);
+                    tmem_ld_wait_regs16(o1);
+                    reg_fence16(o2);
+                    uint4 dq[2];
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) dq[v4] = in ? dyrow[cc * 4 + v4] : make_uint4(0, 0, 0, 0);
+                    for (int v4 = 0; v4 < 2; ++v4) dq[v4] = in ? dyrow[cc * 2 + v4] : make_uint4(0, 0, 0, 0);
                     const uint32_t *dw = reinterpret_cast<const uint32_t *>(dq);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
+                    for (int e = 0; e < 16; e += 2) {
                         const float oa = __uint_as_float(o1[e]) - __fmul_rn(__uint_as_float(o2[e]), lam);
                         const float ob = __uint_as_float(o1[e + 1]) - __fmul_rn(__uint_as_float(o2[e + 1]), lam);
                         ss = fmaf(oa, oa, fmaf(ob, ob, ss));
@@ -415,12 +424,12 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                     }
                 }
             }
-            ctl->x1[half][row] = ss;
-            ctl->x2[half][row] = dyo;
-            named_bar_sync(1, kEw);
+            ctl->x1[grp][row] = ss;
+            ctl->x2[grp][row] = dyo;
+            named_bar_sync(1, kEwP);
             ok = __all_sync(0xffffffffu, ok);
-            const float ss_t = ctl->x1[0][row] + ctl->x1[1][row];
-            const float dyo_t = ctl->x2[0][row] + ctl->x2[1][row];
+            const float ss_t = (ctl->x1[0][row] + ctl->x1[1][row]) + (ctl->x1[2][row] + ctl->x1[3][row]);
+            const float dyo_t = (ctl->x2[0][row] + ctl->x2[1][row]) + (ctl->x2[2][row] + ctl->x2[3][row]);
             float a = 1.f, bc = 0.f;                    // do = a dy - bc o
             if (!p.no_norm) {
                 const float r2 = ss_t / static_cast<float>(kDV) + p.eps;
@@ -432,18 +441,18 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                 uint4 *dorow = reinterpret_cast<uint4 *>(p.dO + rowix * kDV + c0);
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t o1[32], o2[32];
-                    tmem_ld32(tmem + lane_off + c0 + cc * 32, o1);
-                    tmem_ld32(tmem + lane_off + tO2 + c0 + cc * 32, o2);
-                    tmem_ld_wait_regs(o1);
-                    reg_fence(o2);
-                    uint4 dq[4];
+                    uint32_t o1[16], o2[16];
+                    tmem_ld16(tmem + lane_off + c0 + cc * 16, o1);
+                    tmem_ld16(tmem + lane_off + tO2 + c0 + cc * 16, o2);
+                    tmem_ld_wait_regs16(o1);
+                    reg_fence16(o2);
+                    uint4 dq[2];
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) dq[v4] = in ? dyrow[cc * 4 + v4] : make_uint4(0, 0, 0, 0);
+                    for (int v4 = 0; v4 < 2; ++v4) dq[v4] = in ? dyrow[cc * 2 + v4] : make_uint4(0, 0, 0, 0);
                     const uint32_t *dw = reinterpret_cast<const uint32_t *>(dq);
-                    uint32_t pk[16];
+                    uint32_t pk[8];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
+                    for (int e = 0; e < 16; e += 2) {
                         const float O1a = __uint_as_float(o1[e]), O1b = __uint_as_float(o1[e + 1]);
                         const float O2a = __uint_as_float(o2[e]), O2b = __uint_as_float(o2[e + 1]);
                         const float oa = O1a - __fmul_rn(O2a, lam);
@@ -456,23 +465,23 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                     }
                     if (in) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            dorow[cc * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                        for (int v4 = 0; v4 < 2; ++v4)
+                            dorow[cc * 2 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
                     }
                 }
             }
-            ctl->y1[half][row] = d1;
-            ctl->y2[half][row] = d2;
-            named_bar_sync(1, kEw);
-            if (half == 0 && in && ok) {
+            ctl->y1[grp][row] = d1;
+            ctl->y2[grp][row] = d2;
+            named_bar_sync(1, kEwP);
+            if (grp == 0 && in && ok) {
                 const size_t vix = (static_cast<size_t>(b) * p.hs + h) * p.Lp + qrow;
-                p.D1[vix] = ctl->y1[0][row] + ctl->y1[1][row];
-                p.D2[vix] = ctl->y2[0][row] + ctl->y2[1][row];
+                p.D1[vix] = (ctl->y1[0][row] + ctl->y1[1][row]) + (ctl->y1[2][row] + ctl->y1[3][row]);
+                p.D2[vix] = (ctl->y2[0][row] + ctl->y2[1][row]) + (ctl->y2[2][row] + ctl->y2[3][row]);
             }
             tc_fence_before();
             mbar_arrive(&ctl->o_free);
             gt += nkv;
-            if (bar_red_or(1, kEw, !ok || *abort_flag)) break;
+            if (bar_red_or(1, kEwP, !ok || *abort_flag)) break;
         }
     }
 
@@ -891,7 +900,10 @@ __device__ __forceinline__ bool q_item(const BwdTcParams &p, int r, int G, int c
     return true;
 }
 
-__global__ void __launch_bounds__(kThr, 1)
+constexpr int kEwQ = 512;           // dQ elementwise threads: 16 warps, four 16-column groups
+constexpr int kThrQ = 64 + kEwQ;
+
+__global__ void __launch_bounds__(kThrQ, 1)
 gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CUtensorMap tmQ2,
                   const __grid_constant__ CUtensorMap tmdO, const __grid_constant__ CUtensorMap tmK1,
                   const __grid_constant__ CUtensorMap tmK2, const __grid_constant__ CUtensorMap tmV,
@@ -918,12 +930,12 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
         }
         for (int bb = 0; bb < 2; ++bb) {
             mbar_init(&ctl->s_full[bb], 1);
-            mbar_init(&ctl->p_full[bb], kEw);
+            mbar_init(&ctl->p_full[bb], kEwQ);
         }
         mbar_init(&ctl->acc_ready, 1);
-        mbar_init(&ctl->acc_free, kEw);
+        mbar_init(&ctl->acc_free, kEwQ);
         mbar_init(&ctl->q2_ready, 1);
-        mbar_init(&ctl->q2_free, kEw);
+        mbar_init(&ctl->q2_free, kEwQ);
         mbar_init(&ctl->mma_idle, 1);
         ctl->abort_flag = 0;
         fence_mbar_init();
@@ -1031,8 +1043,8 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                         tc_fence_after();
                         const uint32_t sk = k0a + st * LY::KST_BYTES;
                         const uint32_t sb = tmem + bb * kSB;
-                        issue_ts64<kD>(tmem + tdQ1, sb + tS1, sk, j > 0);                          // dQ1 += dS1 K1
-                        issue_ts64<kD>(tmem + tdQ2, sb + tS2, sk + LY::K_BYTES, j > 0 || hi > 0);  // dQ2 += dS2 K2
+                        issue_ts64q<kD>(tmem + tdQ1, sb + tS1, sk, j > 0);                          // dQ1 += dS1 K1
+                        issue_ts64q<kD>(tmem + tdQ2, sb + tS2, sk + LY::K_BYTES, j > 0 || hi > 0);  // dQ2 += dS2 K2
                         mma_commit(&ctl->k_empty[st]);
                         // the buffer just read by those products takes the logits of tile j + 2
                         if (j + 2 < nkv) ok = issue_s(j + 2);
@@ -1052,7 +1064,7 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
         }
         __syncwarp();
     } else {
-        const int half = (warp - 2) / 4;
+        const int grp = (warp - 2) / 4;             // key columns [16 grp, 16 grp + 16) of each tile
         const int quarter = warp % 4;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -1060,52 +1072,72 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
         uint32_t gk = 0, nh = 0;
         int b, g, q0, nkv;
         bool ok = true;
+        auto store16 = [&](float *dst, uint32_t taddr, bool in) {
+            uint32_t o[16];
+            tmem_ld16(taddr, o);
+            tmem_ld_wait_regs16(o);
+            if (in) {
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                    reinterpret_cast<float4 *>(dst)[v4] =
+                        make_float4(__uint_as_float(o[4 * v4]) * p.scale, __uint_as_float(o[4 * v4 + 1]) * p.scale,
+                                    __uint_as_float(o[4 * v4 + 2]) * p.scale, __uint_as_float(o[4 * v4 + 3]) * p.scale);
+            }
+        };
         for (int r = 0; ok && q_item(p, r, G, cid, b, g, q0, nkv); ++r) {
             const int qrow = q0 + row;
             const bool in = qrow < p.L;
             const int last_key = p.causal ? min(qrow, p.L - 1) : p.L - 1;
+            const int wrow_first = q0 + quarter * 32;   // this warp's first query row
             for (int hi = 0; ok && hi < r_grp; ++hi) {
                 const int h = g * r_grp + hi;
-                const float lam = p.lambda[h];
+                const float nlam = -p.lambda[h];
                 const float nlse1 = in ? -p.lse[(static_cast<size_t>(b) * heads + h) * p.Lp + qrow] : 0.f;
                 const float nlse2 = in ? -p.lse[(static_cast<size_t>(b) * heads + p.hs + g) * p.Lp + qrow] : 0.f;
                 const float D1 = in ? p.D1[(static_cast<size_t>(b) * p.hs + h) * p.Lp + qrow] : 0.f;
                 const float D2 = in ? p.D2[(static_cast<size_t>(b) * p.hs + h) * p.Lp + qrow] : 0.f;
                 for (int j = 0; j < nkv; ++j) {
-                    const uint32_t sb = tmem + lane_off + (gk & 1) * kSB;
+                    const uint32_t sb = tmem + lane_off + (gk & 1) * kSB + grp * 16;
                     if (!warp_wait(&ctl->s_full[gk & 1], (gk >> 1) & 1, p.err, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    uint32_t s1[32], s2[32], dp[32];
-                    tmem_ld32(sb + tS1 + half * 32, s1);
-                    tmem_ld32(sb + tS2 + half * 32, s2);
-                    tmem_ld32(sb + tdP + half * 32, dp);
-                    tmem_ld_wait_regs(s1);
-                    reg_fence(s2);
-                    reg_fence(dp);
-                    const int kc0 = j * kN + half * 32;
-                    uint32_t pd1[16], pd2[16];
+                    uint32_t s1[16], s2[16], dp[16];
+                    tmem_ld16(sb + tS1, s1);
+                    tmem_ld16(sb + tS2, s2);
+                    tmem_ld16(sb + tdP, dp);
+                    tmem_ld_wait_regs16(s1);
+                    reg_fence16(s2);
+                    reg_fence16(dp);
+                    const int kc0 = j * kN + grp * 16;
+                    // every (query, key) pair of this warp and group is visible: no per-element mask
+                    const bool clean = wrow_first + 31 < p.L && kc0 + 15 < p.L && (!p.causal || kc0 + 15 <= wrow_first);
+                    uint32_t pd1[8], pd2[8];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
+                    for (int e = 0; e < 16; e += 2) {
                         float a2[2], c2[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const bool vis = in && kc0 + e + u <= last_key;
                             const float p1 = fast_exp2(fmaf(__uint_as_float(s1[e + u]), sl2, nlse1));
-                            const float p2 = fast_exp2(fmaf(__uint_as_float(s2[e + u]), sl2, nlse2));
+                            const float np2 = nlam * fast_exp2(fmaf(__uint_as_float(s2[e + u]), sl2, nlse2));
                             const float dpv = __uint_as_float(dp[e + u]);
-                            const float ds1 = p1 * (dpv - D1);
-                            const float ds2 = -lam * p2 * (dpv - D2);
-                            a2[u] = vis ? ds1 : 0.f;
-                            c2[u] = vis ? ds2 : 0.f;
+                            a2[u] = p1 * (dpv - D1);
+                            c2[u] = np2 * (dpv - D2);
+                        }
+                        if (!clean) {
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const bool vis = in && kc0 + e + u <= last_key;
+                                a2[u] = vis ? a2[u] : 0.f;
+                                c2[u] = vis ? c2[u] : 0.f;
+                            }
                         }
                         pd1[e / 2] = pack_bf16x2(a2[0], a2[1]);
                         pd2[e / 2] = pack_bf16x2(c2[0], c2[1]);
                     }
-                    tmem_st16(sb + tS1 + half * 32, pd1);
-                    tmem_st16(sb + tS2 + half * 32, pd2);
+                    tmem_st8(sb + tS1, pd1);
+                    tmem_st8(sb + tS2, pd2);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(&ctl->p_full[gk & 1]);
@@ -1114,45 +1146,23 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                 ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
                 if (ok) ok = warp_wait(&ctl->acc_ready, nh & 1, p.err, abort_flag);
                 tc_fence_after();
-                if (ok) {
-                    float *dqrow = p.dq1 + ((static_cast<size_t>(b) * p.L + (in ? qrow : 0)) * p.hs + h) * kD + half * 32;
-                    uint32_t o[32];
-                    tmem_ld32(tmem + lane_off + tdQ1 + half * 32, o);
-                    tmem_ld_wait_regs(o);
-                    if (in) {
-#pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            reinterpret_cast<float4 *>(dqrow)[v4] =
-                                make_float4(__uint_as_float(o[4 * v4]) * p.scale, __uint_as_float(o[4 * v4 + 1]) * p.scale,
-                                            __uint_as_float(o[4 * v4 + 2]) * p.scale,
-                                            __uint_as_float(o[4 * v4 + 3]) * p.scale);
-                    }
-                }
+                if (ok)
+                    store16(p.dq1 + ((static_cast<size_t>(b) * p.L + (in ? qrow : 0)) * p.hs + h) * kD + grp * 16,
+                            tmem + lane_off + tdQ1 + grp * 16, in);
                 tc_fence_before();
                 mbar_arrive(&ctl->acc_free);
                 ++nh;
-                if (bar_red_or(1, kEw, !ok || *abort_flag)) ok = false;
+                if (bar_red_or(1, kEwQ, !ok || *abort_flag)) ok = false;
             }
             if (!ok) break;
             ok = warp_wait(&ctl->q2_ready, r & 1, p.err, abort_flag);
             tc_fence_after();
-            if (ok) {
-                float *dqrow = p.dq2 + ((static_cast<size_t>(b) * p.L + (in ? qrow : 0)) * p.hn + g) * kD + half * 32;
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + tdQ2 + half * 32, o);
-                tmem_ld_wait_regs(o);
-                if (in) {
-#pragma unroll
-                    for (int v4 = 0; v4 < 8; ++v4)
-                        reinterpret_cast<float4 *>(dqrow)[v4] =
-                            make_float4(__uint_as_float(o[4 * v4]) * p.scale, __uint_as_float(o[4 * v4 + 1]) * p.scale,
-                                        __uint_as_float(o[4 * v4 + 2]) * p.scale,
-                                        __uint_as_float(o[4 * v4 + 3]) * p.scale);
-                }
-            }
+            if (ok)
+                store16(p.dq2 + ((static_cast<size_t>(b) * p.L + (in ? qrow : 0)) * p.hn + g) * kD + grp * 16,
+                        tmem + lane_off + tdQ2 + grp * 16, in);
             tc_fence_before();
             mbar_arrive(&ctl->q2_free);
-            if (bar_red_or(1, kEw, !ok || *abort_flag)) break;
+            if (bar_red_or(1, kEwQ, !ok || *abort_flag)) break;
         }
         tmem_ld_wait();
     }
@@ -1278,12 +1288,12 @@ int launch_backward_tc(const BackwardTcArgs &a, cudaStream_t stream) {
 
     long long gp = nqt * a.B * a.hs;
     if (gp > sms) gp = sms;
-    gda_bwd_prep_kernel<<<static_cast<unsigned>(gp), kThr, smem_p, stream>>>(q1_128, k1_64, q2_128, k2_64, v_64, p);
+    gda_bwd_prep_kernel<<<static_cast<unsigned>(gp), kThrP, smem_p, stream>>>(q1_128, k1_64, q2_128, k2_64, v_64, p);
     long long gkv = nqt * a.B * a.hn;
     if (gkv > sms) gkv = sms;
     gda_bwd_dkdv_kernel<<<static_cast<unsigned>(gkv), kThrKv, smem_kv, stream>>>(k1_128, k2_128, v_128, q1_64, q2_64,
                                                                                do_64, p);
-    gda_bwd_dq_kernel<<<static_cast<unsigned>(gkv), kThr, smem_q, stream>>>(q1_128, q2_128, do_128, k1_64, k2_64,
+    gda_bwd_dq_kernel<<<static_cast<unsigned>(gkv), kThrQ, smem_q, stream>>>(q1_128, q2_128, do_128, k1_64, k2_64,
                                                                             v_64, p);
     gda_bwd_dlambda_kernel<<<a.hs, 256, 0, stream>>>(p);
     e = cudaGetLastError();
