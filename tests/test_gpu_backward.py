@@ -160,3 +160,19 @@ def test_backward_full_size_one_group():
     assert_grad_close(got[5][sig], dlam, "dlambda group 2")
     for t in got:
         assert torch.isfinite(t).all()
+
+
+def test_backward_lambda_zero_noise_gradients_vanish():
+    inp = list(W.make_backward_inputs(W.DIFF_F32_L128, B=1, L=90, h_s=4, h_n=2, d=64, dv=128, seed=48))
+    inp[5] = torch.zeros_like(inp[5])
+    got = run_bwd(inp, 0.8)
+    assert torch.count_nonzero(got[2]) == 0 and torch.count_nonzero(got[3]) == 0
+    check(got, gda_backward(*inp[:6], 0.8, inp[6]), "lambda 0")
+
+
+def test_backward_sharp_maps():
+    inp = list(W.make_backward_inputs(W.DIFF_F32_L128, B=1, L=120, h_s=4, h_n=2, d=64, dv=128, seed=49))
+    inp[0] = inp[0] * 4
+    inp[2] = inp[2] * 4
+    got = run_bwd(inp, 0.8)
+    check(got, gda_backward(*inp[:6], 0.8, inp[6]), "sharp maps")

@@ -149,3 +149,23 @@ def test_bf16_backward_full_size_one_group():
     assert_grad_bf16_close(got[5][sig], dlam, dmag, "dlambda group 1")
     for t in got:
         assert torch.isfinite(t).all()
+
+
+def test_bf16_backward_lambda_zero_noise_gradients_vanish():
+    """lambda = 0: the noise map does not reach the output, so the noise
+    projections' gradients are exactly 0; dlambda = -sum do . O2 is not."""
+    inp = list(W.make_backward_inputs(W.GDA3_PREFILL_L2048, B=1, L=150, h_s=6, h_n=2, seed=46))
+    inp[5] = torch.zeros_like(inp[5])
+    got = run_bwd(inp, 0.8)
+    assert torch.count_nonzero(got[2]) == 0 and torch.count_nonzero(got[3]) == 0
+    check(got, oracle_grads(inp, 0.8), "lambda 0")
+
+
+def test_bf16_backward_sharp_maps():
+    """Queries scaled by 4 (exact in bf16): logits up to ~30 / sqrt(d) units,
+    nearly one-hot rows, which exercises the saved statistics' range."""
+    inp = list(W.make_backward_inputs(W.GDA3_PREFILL_L2048, B=1, L=200, h_s=6, h_n=2, seed=47))
+    inp[0] = inp[0] * 4
+    inp[2] = inp[2] * 4
+    got = run_bwd(inp, 0.8)
+    check(got, oracle_grads(inp, 0.8), "sharp maps")
