@@ -160,7 +160,8 @@ int gda_attn_fwd_chunk(const void *q_sig, const void *k_sig, const void *q_noise
                        int Lk, int h_s, int h_n, int d, int dv, int causal, float eps, unsigned flags,
                        gda_stream_t stream) {
     int st = check_prefill_common(q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L,
-                                  h_s, h_n, d, dv, causal, eps, flags);
+                                  h_s, h_n, d, dv, causal, eps, flags,
+                                  GDA_FLAG_NO_NORM | GDA_FLAG_SINGLE_PASS);
     if (st != GDA_OK) return st;
     if (Lk < 1 || (causal && Lk < L)) return GDA_ERR_INVALID_ARG;
     if (static_cast<double>(B) * Lk * (h_s > h_n ? h_s : h_n) * (d > dv ? d : dv) > 9.0e15)
@@ -170,9 +171,21 @@ int gda_attn_fwd_chunk(const void *q_sig, const void *k_sig, const void *q_noise
     st = current_device(&err);
     if (st != GDA_OK) return st;
     PrefillArgs a{q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L, h_s, h_n,
-                  d, dv, causal, eps, flags, err};
+                  d, dv, causal, eps, flags & GDA_FLAG_NO_NORM, err};
     a.Lk = Lk;
-    return launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dv == 256 && !(flags & GDA_FLAG_SINGLE_PASS)) {
+        // as gda_attn_fwd: the two-pass kernels, statistics from the stream-ordered allocator
+        void *lse = nullptr;
+        if (cudaMallocAsync(&lse, prefill_2pass_workspace_bytes(B, L, h_s, h_n), s) == cudaSuccess) {
+            const int st2 = launch_prefill_2pass(a, lse, s);
+            const cudaError_t fe = cudaFreeAsync(lse, s);
+            if (st2 != GDA_OK) return st2;
+            return fe == cudaSuccess ? GDA_OK : record_cuda_error(fe);
+        }
+        cudaGetLastError();   // no statistics buffer: the single-pass kernel needs none
+    }
+    return launch_prefill_tc(a, s);
 }
 
 int gda_attn_fwd(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,

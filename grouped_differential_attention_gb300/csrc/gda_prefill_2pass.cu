@@ -1,5 +1,7 @@
 // Two-pass grouped differential attention prefill for sm_103a: the
-// difference map is formed before the value product.
+// difference map is formed before the value product.  Also serves chunked
+// prefill (L query rows continuing a sequence of Lk >= L keys: query row i
+// sits at key position Lk - L + i).
 //
 // Same result as the single-pass kernel (gda_prefill_tc.cu):
 //   o = softmax(Q1_h K1_h^T / sqrt d) V_h - lambda_h softmax(Q2_g K2_g^T / sqrt d) V_h
@@ -53,6 +55,7 @@ struct P2Params {
     float lambda_init, eps, scale_log2;
     int B, L, hs, hn, dv, causal, nqt, no_norm;
     int lse_ld;                     // row stride of lse (>= L)
+    int Lk, koff;                   // keys per sequence; query row i sits at key position koff + i
 };
 
 // ---------------------------------------------------------------- items --
@@ -76,7 +79,7 @@ __device__ __forceinline__ bool item2_of(const P2Params &p, int heads, int r, in
     it.b = rem / heads;
     it.head = rem % heads;
     it.q0 = qt * kBM;
-    const int kv_end = p.causal ? min(p.L, it.q0 + kBM) : p.L;
+    const int kv_end = p.causal ? min(p.Lk, p.koff + it.q0 + kBM) : p.Lk;
     it.nkv = (kv_end + kBN2 - 1) / kBN2;
     return true;
 }
@@ -235,7 +238,7 @@ gda_lse_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
         Item2 it;
         for (int r = 0; item2_of(p, heads, r, G, cid, it); ++r) {
             const int qrow = it.q0 + row;
-            const int last_key = p.causal ? min(qrow, p.L - 1) : p.L - 1;
+            const int last_key = p.causal ? min(p.koff + qrow, p.Lk - 1) : p.Lk - 1;
             float m = -INFINITY, l = 0.f;
             bool ok = true;
             for (int j = 0; j < it.nkv; ++j) {
@@ -560,7 +563,7 @@ gda_diffmap_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_con
             const int h = it.head, g = h / r_grp;
             const int qrow = it.q0 + row;
             const bool in = qrow < p.L;
-            const int last_key = p.causal ? min(qrow, p.L - 1) : p.L - 1;
+            const int last_key = p.causal ? min(p.koff + qrow, p.Lk - 1) : p.Lk - 1;
             const float lam = p.lambda[h];
             // rows past L get lse = +inf, so every P of theirs is 0
             const float neg1 = in ? -p.lse[(static_cast<size_t>(it.b) * heads + h) * p.lse_ld + qrow] : -INFINITY;
@@ -690,21 +693,24 @@ void fill_params(P2Params &p, const PrefillArgs &a, float *lse, int lse_ld) {
     p.nqt = (a.L + kBM - 1) / kBM;
     p.no_norm = (a.flags & GDA_FLAG_NO_NORM) ? 1 : 0;
     p.lse_ld = lse_ld;
+    p.Lk = a.Lk > 0 ? a.Lk : a.L;
+    p.koff = p.Lk - a.L;
 }
 
+// Queries: L rows per sequence; keys (and values): Lk rows.
 bool qk_maps(const PrefillArgs &a, CUtensorMap *mQ1, CUtensorMap *mK1, CUtensorMap *mQ2, CUtensorMap *mK2) {
-    const uint64_t B = a.B, L = a.L, hs = a.hs, hn = a.hn, d = a.d;
+    const uint64_t B = a.B, L = a.L, Lk = a.Lk > 0 ? a.Lk : a.L, hs = a.hs, hn = a.hn, d = a.d;
     const uint32_t boxq[4] = {64, 1, kBM, 1}, boxk[4] = {64, 1, kBN2, 1};
     {
-        const uint64_t dims[4] = {d, hs, L, B};
-        const uint64_t str[3] = {d * 2, hs * d * 2, L * hs * d * 2};
-        if (!encode_tmap_4d_bf16(mQ1, a.q1, dims, str, boxq)) return false;
-        if (!encode_tmap_4d_bf16(mK1, a.k1, dims, str, boxk)) return false;
+        const uint64_t dq[4] = {d, hs, L, B}, dk[4] = {d, hs, Lk, B};
+        const uint64_t sq[3] = {d * 2, hs * d * 2, L * hs * d * 2}, sk[3] = {d * 2, hs * d * 2, Lk * hs * d * 2};
+        if (!encode_tmap_4d_bf16(mQ1, a.q1, dq, sq, boxq)) return false;
+        if (!encode_tmap_4d_bf16(mK1, a.k1, dk, sk, boxk)) return false;
     }
-    const uint64_t dims[4] = {d, hn, L, B};
-    const uint64_t str[3] = {d * 2, hn * d * 2, L * hn * d * 2};
-    if (!encode_tmap_4d_bf16(mQ2, a.q2, dims, str, boxq)) return false;
-    return encode_tmap_4d_bf16(mK2, a.k2, dims, str, boxk);
+    const uint64_t dq[4] = {d, hn, L, B}, dk[4] = {d, hn, Lk, B};
+    const uint64_t sq[3] = {d * 2, hn * d * 2, L * hn * d * 2}, sk[3] = {d * 2, hn * d * 2, Lk * hn * d * 2};
+    if (!encode_tmap_4d_bf16(mQ2, a.q2, dq, sq, boxq)) return false;
+    return encode_tmap_4d_bf16(mK2, a.k2, dk, sk, boxk);
 }
 
 template <int D>
@@ -726,11 +732,11 @@ int launch_lse_impl(const PrefillArgs &a, const CUtensorMap &mQ1, const CUtensor
 template <int D, int DV>
 int launch_2pass_impl(const PrefillArgs &a, float *lse, cudaStream_t stream) {
     CUtensorMap mQ1, mK1, mQ2, mK2, mV;
-    const uint64_t B = a.B, L = a.L, hs = a.hs, dv = a.dv;
+    const uint64_t B = a.B, Lk = a.Lk > 0 ? a.Lk : a.L, hs = a.hs, dv = a.dv;
     if (!qk_maps(a, &mQ1, &mK1, &mQ2, &mK2)) return GDA_ERR_CUDA;
     {
-        const uint64_t dims[4] = {dv, hs, L, B};
-        const uint64_t str[3] = {dv * 2, hs * dv * 2, L * hs * dv * 2};
+        const uint64_t dims[4] = {dv, hs, Lk, B};
+        const uint64_t str[3] = {dv * 2, hs * dv * 2, Lk * hs * dv * 2};
         const uint32_t box[4] = {64, 1, kBN2, 1};
         if (!encode_tmap_4d_bf16(&mV, a.v, dims, str, box)) return GDA_ERR_CUDA;
     }

@@ -71,7 +71,7 @@ typedef enum {
 
 /* Flags for the *_ex entry points. */
 #define GDA_FLAG_NO_NORM 0x1u    /* return o_h (pre-norm, float32 difference) instead of y_h */
-#define GDA_FLAG_SINGLE_PASS 0x2u /* gda_attn_fwd_ex only: keep the single-pass kernel at dv = 256 */
+#define GDA_FLAG_SINGLE_PASS 0x2u /* gda_attn_fwd_ex, gda_attn_fwd_chunk: keep the single-pass kernel at dv = 256 */
 
 /*
  * Prefill / full-sequence forward, bf16 I/O, float32 accumulation.
@@ -104,7 +104,8 @@ int gda_attn_fwd(const void *q_sig, const void *k_sig, const void *q_noise,
  * and Serving Considerations".)
  *   q_sig [B, L, h_s, d], q_noise [B, L, h_n, d], out [B, L, h_s, dv];
  *   k_sig [B, Lk, h_s, d], k_noise [B, Lk, h_n, d], v [B, Lk, h_s, dv].
- * Other arguments, flags, support and errors as gda_attn_fwd_ex;
+ * Other arguments, flags (including GDA_FLAG_SINGLE_PASS), kernels (two-pass
+ * at dv = 256), support and errors as gda_attn_fwd_ex;
  * GDA_ERR_INVALID_ARG also for Lk < 1 or (causal and Lk < L).
  */
 int gda_attn_fwd_chunk(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,

@@ -97,7 +97,7 @@ def test_ex_rejects_unknown_flags(lib):
     assert rc == INVALID
 
 
-def test_single_pass_flag_only_on_the_forward_entry(lib):
+def test_single_pass_flag_only_on_the_forward_entries(lib):
     P = [ctypes.c_void_p(A)] * 5
     F, U = ctypes.c_float, ctypes.c_uint
     # accepted by gda_attn_fwd_ex (validation passes; without a GPU the call then reports a CUDA error)
@@ -108,7 +108,9 @@ def test_single_pass_flag_only_on_the_forward_entry(lib):
     assert lib.gda_attn_fwd_f32_ex(*P, ctypes.c_void_p(A), F(0.8), ctypes.c_void_p(A), 1, 128, 6, 2, 64, 128, 1,
                                    F(1e-5), U(0x2), None) == INVALID
     assert lib.gda_attn_fwd_chunk(*P, ctypes.c_void_p(A), F(0.8), ctypes.c_void_p(A), 1, 128, 128, 6, 2, 64, 256,
-                                  1, F(1e-5), U(0x2), None) == INVALID
+                                  1, F(1e-5), U(0x2), None) != INVALID
+    assert lib.gda_attn_fwd_chunk(*P, ctypes.c_void_p(A), F(0.8), ctypes.c_void_p(A), 1, 128, 128, 6, 2, 64, 256,
+                                  1, F(1e-5), U(0x4), None) == INVALID
     assert lib.gda_attn_fwd_2pass(*P, ctypes.c_void_p(A), F(0.8), ctypes.c_void_p(A), 1, 128, 6, 2, 64, 256, 1,
                                   F(1e-5), U(0x2), ctypes.c_void_p(A), 1 << 20, None) == INVALID
 
