@@ -32,6 +32,7 @@ __all__ = [
     "gda_attn_decode_noalloc",
     "gda_attn_bwd", "gda_attn_bwd_workspace_size", "gda_attn_fwd_2pass",
     "gda_attn_fwd_2pass_workspace_size", "gda_attn_bwd_bf16", "gda_attn_bwd_bf16_workspace_size",
+    "gda_attn_decode_paged_fp8",
 ]
 
 GDA_OK = 0
@@ -100,6 +101,9 @@ def _load():
             lib.gda_attn_fwd_chunk.restype = I
             lib.gda_lambda_reparam.argtypes = [P, P, P, P, F, P, I, I, P]
             lib.gda_lambda_reparam.restype = I
+            lib.gda_attn_decode_paged_fp8.argtypes = [P, P, P, P, P, P, P, P, P, P, P, F, P, I, I, I, I, I, I,
+                                                      I, I, F, P, Z, P]
+            lib.gda_attn_decode_paged_fp8.restype = I
             lib.gda_attn_fwd_2pass.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, F, U, P, Z, P]
             lib.gda_attn_fwd_2pass.restype = I
             lib.gda_attn_fwd_2pass_workspace_size.argtypes = [I, I, I, I]
@@ -312,6 +316,53 @@ def gda_attn_decode_paged(q_sig, q_noise, k_sig_pool, k_noise_pool, v_pool, bloc
             max_pages, page_size, num_pages, hs, hn, d, dv, float(eps), _ptr(workspace),
             workspace.numel() * workspace.element_size(), _stream(dev))
     _check(rc, "gda decode (paged caches)")
+    return out
+
+
+def gda_attn_decode_paged_fp8(q_sig, q_noise, k_sig_pool, k_noise_pool, v_pool, k_sig_scale, k_noise_scale,
+                              v_scale, block_table, cache_lens, lam, lambda_init: float, *, eps: float = 1e-5,
+                              out=None, workspace=None):
+    """bf16 decode over paged fp8 (e4m3) caches: pools [num_pages, page_size,
+    heads, dim] of float8_e4m3fn (or uint8 codes), per-head float32 scales,
+    block_table [B, max_pages] int32."""
+    dev = q_sig.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, hs, d = q_sig.shape
+    hn = q_noise.shape[1]
+    num_pages, page_size = k_sig_pool.shape[0], k_sig_pool.shape[1]
+    dv = v_pool.shape[3]
+    max_pages = block_table.shape[1]
+    bf = torch.bfloat16
+    pools = []
+    for t, name, shape in ((k_sig_pool, "k_sig_pool", (num_pages, page_size, hs, d)),
+                           (k_noise_pool, "k_noise_pool", (num_pages, page_size, hn, d)),
+                           (v_pool, "v_pool", (num_pages, page_size, hs, dv))):
+        if t.dtype == torch.float8_e4m3fn:
+            t = t.view(torch.uint8)
+        _expect(t, name, torch.uint8, shape, dev)
+        pools.append(t)
+    _expect(q_sig, "q_sig", bf, (B, hs, d), dev)
+    _expect(q_noise, "q_noise", bf, (B, hn, d), dev)
+    _expect(k_sig_scale, "k_sig_scale", torch.float32, (hs,), dev)
+    _expect(k_noise_scale, "k_noise_scale", torch.float32, (hn,), dev)
+    _expect(v_scale, "v_scale", torch.float32, (hs,), dev)
+    _expect(block_table, "block_table", torch.int32, (B, max_pages), dev)
+    _expect(cache_lens, "cache_lens", torch.int32, (B,), dev)
+    _expect(lam, "lam", torch.float32, (hs,), dev)
+    if out is None:
+        out = torch.empty((B, hs, dv), dtype=bf, device=dev)
+    _expect(out, "out", bf, (B, hs, dv), dev)
+    need = gda_attn_decode_workspace_size(B, max_pages * page_size, hs, hn, dv)
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = _load().gda_attn_decode_paged_fp8(
+            _ptr(q_sig), _ptr(q_noise), *[_ptr(t) for t in pools], _ptr(k_sig_scale), _ptr(k_noise_scale),
+            _ptr(v_scale), _ptr(block_table), _ptr(cache_lens), _ptr(lam), float(lambda_init), _ptr(out), B,
+            max_pages, page_size, num_pages, hs, hn, d, dv, float(eps), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(dev))
+    _check(rc, "gda decode (paged fp8 caches)")
     return out
 
 

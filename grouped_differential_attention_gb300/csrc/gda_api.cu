@@ -413,6 +413,50 @@ int gda_attn_decode_paged(const void *q_sig, const void *q_noise, const void *k_
     return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int gda_attn_decode_paged_fp8(const void *q_sig, const void *q_noise, const void *k_sig_pool,
+                              const void *k_noise_pool, const void *v_pool, const float *k_sig_scale,
+                              const float *k_noise_scale, const float *v_scale, const int *block_table,
+                              const int *cache_lens, const float *lambda, float lambda_init, void *out, int B,
+                              int max_pages, int page_size, int num_pages, int h_s, int h_n, int d, int dv,
+                              float eps, void *workspace, size_t workspace_bytes, gda_stream_t stream) {
+    if (!q_sig || !q_noise || !k_sig_pool || !k_noise_pool || !v_pool || !k_sig_scale || !k_noise_scale ||
+        !v_scale || !block_table || !cache_lens || !lambda || !out)
+        return GDA_ERR_INVALID_ARG;
+    if (B < 1 || max_pages < 1 || page_size < 1 || num_pages < 1 || h_s < 1 || h_n < 1 || d < 1 || dv < 1 ||
+        h_s % h_n != 0)
+        return GDA_ERR_INVALID_ARG;
+    const long long Lcap = static_cast<long long>(max_pages) * page_size;
+    if (Lcap > 0x7fffffffLL) return GDA_ERR_INVALID_ARG;
+    if (!std::isfinite(eps) || eps < 0.f || !std::isfinite(lambda_init)) return GDA_ERR_INVALID_ARG;
+    if (static_cast<double>(num_pages) * page_size * h_s * (d > dv ? d : dv) > 9.0e15) return GDA_ERR_INVALID_ARG;
+    if (!(d == 64 || d == 128) || !(dv == 64 || dv == 128 || dv == 256)) return GDA_ERR_UNSUPPORTED;
+    if (h_s + h_n > 128 || B > 65535) return GDA_ERR_UNSUPPORTED;
+    if (!aligned16(q_sig) || !aligned16(q_noise) || !aligned16(k_sig_pool) || !aligned16(k_noise_pool) ||
+        !aligned16(v_pool) || !aligned16(cache_lens) || !aligned16(lambda) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(block_table) & 3u))
+        return GDA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(k_sig_scale) | reinterpret_cast<uintptr_t>(k_noise_scale) |
+         reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+        return GDA_ERR_MISALIGNED;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < gda_attn_decode_workspace_size(B, static_cast<int>(Lcap), h_s, h_n, dv))
+        return GDA_ERR_WORKSPACE;
+    unsigned *err = nullptr;
+    const int st = current_device(&err);
+    if (st != GDA_OK) return st;
+    DecodeArgs a{q_sig, q_noise, k_sig_pool, k_noise_pool, v_pool, cache_lens, lambda, lambda_init,
+                 out, B, static_cast<int>(Lcap), h_s, h_n, d, dv, eps, workspace, workspace_bytes, err};
+    a.fp8 = 1;
+    a.k1_scale = k_sig_scale;
+    a.k2_scale = k_noise_scale;
+    a.v_scale = v_scale;
+    a.block_table = block_table;
+    a.page_size = page_size;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int gda_lambda_reparam(const float *lambda_q1, const float *lambda_k1, const float *lambda_q2,
                        const float *lambda_k2, float lambda_init, float *lambda_out, int h_s, int d,
                        gda_stream_t stream) {

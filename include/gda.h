@@ -305,6 +305,21 @@ int gda_attn_decode_paged(const void *q_sig, const void *q_noise, const void *k_
                           float eps, void *workspace, size_t workspace_bytes, gda_stream_t stream);
 
 /*
+ * Decode over paged fp8 (e4m3) caches: the page pools and block table of
+ * gda_attn_decode_paged holding the e4m3 codes and per-head scales of
+ * gda_attn_decode_fp8 (cached value = code x scale of its head).  Arguments,
+ * layouts, ownership and errors as those two entries; both serving variants
+ * ("Hardware Implementations and Serving Considerations": paged KV caches
+ * and low-bit KV quantisation) at once.
+ */
+int gda_attn_decode_paged_fp8(const void *q_sig, const void *q_noise, const void *k_sig_pool,
+                              const void *k_noise_pool, const void *v_pool, const float *k_sig_scale,
+                              const float *k_noise_scale, const float *v_scale, const int *block_table,
+                              const int *cache_lens, const float *lambda, float lambda_init, void *out, int B,
+                              int max_pages, int page_size, int num_pages, int h_s, int h_n, int d, int dv,
+                              float eps, void *workspace, size_t workspace_bytes, gda_stream_t stream);
+
+/*
  * Decode that allocates nothing and takes no workspace.  No counterpart on
  * the pages: it exists for callers that cannot allocate device memory, such
  * as a plugin or serving loop whose host framework owns all device memory in

@@ -289,3 +289,23 @@ def test_two_pass_prefill_rejects_bad_arguments(lib):
     assert call(ws=None) == WORKSPACE
     assert call(ws_bytes=4 * 2 * 128 * 8 - 4) == WORKSPACE
     assert call(ws=ctypes.c_void_p(A + 4)) == WORKSPACE
+
+
+def test_decode_paged_fp8_rejects_bad_arguments(lib):
+    # every call below fails validation before any device work
+    F = ctypes.c_float
+
+    def call(first=None, B=2, max_pages=4, page_size=16, num_pages=9, hs=6, hn=2, d=64, dv=128, scale_off=0,
+             ws=ctypes.c_void_p(A), ws_bytes=1 << 30):
+        ptrs = first if first is not None else [ctypes.c_void_p(A)] * 5
+        scales = [ctypes.c_void_p(A + scale_off)] * 3
+        return lib.gda_attn_decode_paged_fp8(*ptrs, *scales, ctypes.c_void_p(A), ctypes.c_void_p(A),
+                                             ctypes.c_void_p(A), F(0.8), ctypes.c_void_p(A), B, max_pages, page_size,
+                                             num_pages, hs, hn, d, dv, F(1e-5), ws, ws_bytes, None)
+    assert call(first=[None] + [ctypes.c_void_p(A)] * 4) == INVALID
+    assert call(page_size=0) == INVALID
+    assert call(hs=6, hn=4) == INVALID
+    assert call(d=96) == UNSUPPORTED
+    assert call(scale_off=2) == MISALIGNED
+    assert call(ws=None) == WORKSPACE
+    assert call(ws_bytes=16) == WORKSPACE

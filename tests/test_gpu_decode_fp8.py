@@ -73,3 +73,38 @@ def test_fp8_cache_of_representable_values_matches_bf16_decode():
     ref = gda.gda_attn_decode(*(t.cuda() for t in (q1, q2, *bf, lens, lam)), 0.8)
     torch.cuda.synchronize()
     assert_bf16_close(got, ref.cpu().double().numpy(), "fp8 vs bf16 decode")
+
+
+def run_paged_fp8(inp, page_size, seed, lam_init=0.8):
+    q1, q2, k1q, k2q, vq, k1s, k2s, vs, lens, lam = inp
+    k1p, k2p, vp, table = W.page_caches(k1q, k2q, vq, page_size, seed=seed)
+    out = gda.gda_attn_decode_paged_fp8(*(t.cuda() for t in (q1, q2, k1p, k2p, vp, k1s, k2s, vs, table, lens, lam)),
+                                        lam_init)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+@pytest.mark.parametrize("shape", [  # B, Lcap, h_s, h_n, d, dv, page_size
+    (3, 64, 12, 4, 64, 128, 16),
+    (5, 1000, 6, 2, 128, 256, 8),
+    (2, 777, 4, 4, 64, 64, 7),
+    (70, 64, 3, 1, 64, 128, 1),
+])
+def test_paged_fp8_decode_matches_oracle(shape):
+    """Paged pools of e4m3 codes (seeded random page order) with per-head
+    scales: both serving variants at once, against the float64 dense decode
+    of the same codes and scales."""
+    B, Lcap, hs, hn, d, dv, ps = shape
+    Lcap = (Lcap + ps - 1) // ps * ps
+    inp = W.make_decode_inputs_fp8(W.GDA3_DECODE_B64, B=B, Lcap=Lcap, h_s=hs, h_n=hn, d=d, dv=dv,
+                                   seed=B * 41 + Lcap + ps, len_range=(1, Lcap))
+    inp[8][0] = 1
+    inp[8][-1] = Lcap
+    assert_bf16_close(run_paged_fp8(inp, ps, seed=ps), oracle_fp8(inp, 0.8), str(shape))
+
+
+def test_paged_fp8_decode_equals_contiguous_fp8_decode():
+    """Same positions, same partition over the CTAs, same arithmetic: the
+    paged result equals the contiguous one bit for bit."""
+    inp = W.make_decode_inputs_fp8(W.GDA3_DECODE_B64, B=8, Lcap=4096, seed=93, len_range=(1, 4096))
+    assert torch.equal(run_paged_fp8(inp, 64, seed=7), run_fp8(inp, 0.8))
