@@ -375,6 +375,27 @@ def run_gda(args, world, rank, local):
     dp_ms_step = ev8.elapsed_time(ev9) / dec_steps
     del dpg
 
+    # ---- the same decode over paged fp8 caches
+    cpu_d8 = W.make_decode_inputs_fp8(dw, seed=rank)
+    k1p8, k2p8, vp8, table8 = W.page_caches(cpu_d8[2], cpu_d8[3], cpu_d8[4], page_size, seed=rank)
+    dpg8 = [t.to(dev) for t in (cpu_d8[0], cpu_d8[1], k1p8, k2p8, vp8, cpu_d8[5], cpu_d8[6], cpu_d8[7], table8,
+                                cpu_d8[8], cpu_d8[9])]
+    del cpu_d8, k1p8, k2p8, vp8
+
+    def dp8step():
+        gda.gda_attn_decode_paged_fp8(*dpg8, dw.lambda_init, eps=dw.eps, out=dout, workspace=ws)
+
+    for _ in range(max(3, args.warmup // 4)):
+        dp8step()
+    torch.cuda.synchronize(dev)
+    ev8.record(stream)
+    for _ in range(dec_steps):
+        dp8step()
+    ev9.record(stream)
+    torch.cuda.synchronize(dev)
+    dp8_ms_step = ev8.elapsed_time(ev9) / dec_steps
+    del dpg8
+
     # ---- chunked prefill: 512 new rows continuing a 7680-row cached prefix
     ck_L, ck_Lk = 512, 8192
     g = torch.Generator().manual_seed(rank + 21)
@@ -680,6 +701,13 @@ def run_gda(args, world, rank, local):
                          "roofline": {"bound": "hbm", "achieved": dec_bytes / (dp_ms_step * 1e-3) / 1e9,
                                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": dec_bytes / (dp_ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"]}},
+        "decode_paged_fp8": {"workload": dw.name + f" with fp8 e4m3 caches in {page_size}-position pages, random "
+                                                   "pool order",
+                             "value": d8_bytes / (dp8_ms_step * 1e-3) / 1e9, "unit": "GB/s",
+                             "ms_per_step": dp8_ms_step, "steps": dec_steps, "bytes_per_step": d8_bytes,
+                             "roofline": {"bound": "hbm", "achieved": d8_bytes / (dp8_ms_step * 1e-3) / 1e9,
+                                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                          "frac": d8_bytes / (dp8_ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"]}},
         "prefill_chunk": {"workload": f"B={w.B}, {ck_L} new rows after a {ck_Lk - ck_L}-row cached prefix, "
                                       f"{w.h_s}+{w.h_n} heads, d={w.d}, dv={w.dv}",
                           "value": ck_flops / (ck_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ck_ms,
