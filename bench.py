@@ -420,6 +420,35 @@ def run_gda(args, world, rank, local):
     ck_ms = eva.elapsed_time(evb) / ck_steps
     del ck
 
+    # ---- per-launch distribution of the headline kernel: 50 launches, each timed alone
+    # (10 warm-up launches first), rotating input sets
+    for i in range(10):
+        step(i)
+    torch.cuda.synchronize(dev)
+    lat_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for i, (a, b) in enumerate(lat_ev):
+        a.record(stream)
+        step(i)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    lat_us = sorted(a.elapsed_time(b) * 1e3 for a, b in lat_ev)
+
+    # ---- the float32 CUDA-core prefill at its own workload (B=1, L=128, 2+2 heads): latency only
+    wf = W.DIFF_F32_L128
+    f32_in = [t.to(dev) for t in W.make_prefill_inputs(wf)]
+    f32_out = torch.empty((wf.B, wf.L, wf.h_s, wf.dv), dtype=torch.float32, device=dev)
+    for _ in range(10):
+        gda.gda_attn_fwd_f32(*f32_in, wf.lambda_init, causal=wf.causal, eps=wf.eps, out=f32_out)
+    torch.cuda.synchronize(dev)
+    f32_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for a, b in f32_ev:
+        a.record(stream)
+        gda.gda_attn_fwd_f32(*f32_in, wf.lambda_init, causal=wf.causal, eps=wf.eps, out=f32_out)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    f32_us = sorted(a.elapsed_time(b) * 1e3 for a, b in f32_ev)
+    del f32_in, f32_out
+
     # ---- two-pass prefill (difference map before the value product) on the same inputs
     tp_ws = torch.empty(gda.gda_attn_fwd_2pass_workspace_size(w.B, w.L, w.h_s, w.h_n), dtype=torch.uint8,
                         device=dev)
@@ -701,6 +730,18 @@ def run_gda(args, world, rank, local):
                          "roofline": {"bound": "hbm", "achieved": dec_bytes / (dp_ms_step * 1e-3) / 1e9,
                                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": dec_bytes / (dp_ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"]}},
+        "launch_stats": {"kernel": "gda_prefill_tc_kernel<64>", "launches": len(lat_us), "warmup": 10,
+                         "us_min": lat_us[0], "us_median": lat_us[len(lat_us) // 2],
+                         "us_p90": lat_us[int(0.9 * (len(lat_us) - 1))],
+                         "tflops_at_median": flops / (lat_us[len(lat_us) // 2] * 1e-6) / 1e12,
+                         "tflops_min_count_at_median": prefill_min_flops(w.B, w.L, w.h_s, w.h_n, w.d, w.dv)
+                         / (lat_us[len(lat_us) // 2] * 1e-6) / 1e12,
+                         "min_count": "causal pairs x (2d(h_s+h_n) + 2 dv h_s): one product of the difference "
+                                      "map with V"},
+        "prefill_f32": {"workload": wf.name, "us_median": f32_us[len(f32_us) // 2], "us_min": f32_us[0],
+                        "us_p90": f32_us[int(0.9 * (len(f32_us) - 1))], "launches": len(f32_us),
+                        "bound": "latency: 64 CTAs of 4 rows walk up to 4 key tiles each (precision path; no "
+                                 "roofline claim)"},
         "decode_paged_fp8": {"workload": dw.name + f" with fp8 e4m3 caches in {page_size}-position pages, random "
                                                    "pool order",
                              "value": d8_bytes / (dp8_ms_step * 1e-3) / 1e9, "unit": "GB/s",
@@ -771,6 +812,14 @@ def run_gda(args, world, rank, local):
             "value": cpu_value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{nrows} query rows (all {w.B} sequences x {w.h_s} heads) of the same "
                       f"workload, {spent:.1f} s of float64 oracle time"}
+        # the same oracle on one core, a shorter sample
+        import oracle
+        oracle.set_threads(1)
+        one_value, one_rows, one_spent, _ = oracle_rows_throughput(w, rows_per_sample=2,
+                                                                   target_s=max(0.5, args.cpu_seconds / 5))
+        oracle.set_threads(cores)
+        line["cpu_baseline"]["one_core"] = {"value": one_value, "unit": "TFLOP/s", "cores": 1,
+                                            "sample": f"{one_rows} query rows, {one_spent:.1f} s"}
     print(json.dumps(line), flush=True)
 
 

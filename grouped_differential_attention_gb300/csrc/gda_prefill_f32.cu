@@ -7,10 +7,12 @@
 // Architecture" and "Headwise Normalization"; noise heads shared by groups of
 // signal heads per the "Grouped Differential Attention" abstract).
 //
-// CTA = (16 query rows, signal head h, batch b), 4 warps with 4 rows each.
-// Keys stream through shared memory 32 at a time; lane j scores key j of the
-// tile for both maps, the warp keeps both online softmax states of its rows,
-// and lane l owns output columns l, l+32, ... of both accumulators.
+// CTA = (4 RPW query rows, signal head h, batch b), 4 warps with RPW rows
+// each (RPW = 4; 1 for dv > 160 or when 16-row CTAs would not fill the GPU).  Keys stream
+// through shared memory 32 at a time; lane j scores key j of the tile for
+// both maps, the warp keeps both online softmax states of its rows, and lane
+// l owns output columns l, l+32, ... of both accumulators.  With one row per
+// warp the head width d is a compile-time constant for d = 64 and 128.
 #include <cuda_runtime.h>
 #include <cstdint>
 #include <cmath>
@@ -21,7 +23,6 @@
 namespace gda {
 namespace {
 
-constexpr int kRows = 16;
 constexpr int kKeys = 32;
 constexpr int kThreadsF32 = 128;
 
@@ -61,11 +62,12 @@ __device__ __forceinline__ float online_step(float s, float &m, float &l, float 
     return p;
 }
 
-template <int NV>   // dv = 32 * NV
+template <int NV, int RPW, int DT>   // dv = 32 * NV; RPW rows per warp; DT = d (0: runtime d)
 __global__ void __launch_bounds__(kThreadsF32)
 gda_prefill_f32_kernel(const F32Params p) {
     extern __shared__ float sm[];
-    const int d = p.d, dp = p.d + 1;
+    constexpr int kRows = 4 * RPW;
+    const int d = DT ? DT : p.d, dp = d + 1;
     float *q1s = sm;                       // [kRows][d]
     float *q2s = q1s + kRows * d;          // [kRows][d]
     float *k1s = q2s + kRows * d;          // [kKeys][d+1]
@@ -85,10 +87,10 @@ gda_prefill_f32_kernel(const F32Params p) {
         q2s[i] = in ? p.q2[((static_cast<size_t>(b) * p.L + qi) * p.hn + g) * d + e] : 0.f;
     }
 
-    float m1[4], l1[4], m2[4], l2[4];
-    float o1[4][NV], o2[4][NV];
+    float m1[RPW], l1[RPW], m2[RPW], l2[RPW];
+    float o1[RPW][NV], o2[RPW][NV];
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
+    for (int rr = 0; rr < RPW; ++rr) {
         m1[rr] = m2[rr] = -INFINITY;
         l1[rr] = l2[rr] = 0.f;
 #pragma unroll
@@ -98,27 +100,50 @@ gda_prefill_f32_kernel(const F32Params p) {
     const int kv_end = p.causal ? min(p.L, q0 + kRows) : p.L;
     for (int k0 = 0; k0 < kv_end; k0 += kKeys) {
         __syncthreads();
-        for (int i = threadIdx.x; i < kKeys * d; i += blockDim.x) {
-            const int j = i / d, e = i % d, kj = k0 + j;
-            const bool in = kj < p.L;
-            k1s[j * dp + e] = in ? p.k1[((static_cast<size_t>(b) * p.L + kj) * p.hs + h) * d + e] : 0.f;
-            k2s[j * dp + e] = in ? p.k2[((static_cast<size_t>(b) * p.L + kj) * p.hn + g) * d + e] : 0.f;
+        // 16-byte loads, several in flight per thread (d = 64 / 128 and every dv are multiples of 4)
+        if constexpr (DT != 0) {
+            constexpr int d4 = DT / 4;
+#pragma unroll 4
+            for (int i = threadIdx.x; i < kKeys * d4; i += blockDim.x) {
+                const int j = i / d4, e = (i % d4) * 4, kj = k0 + j;
+                float4 x1 = make_float4(0.f, 0.f, 0.f, 0.f), x2 = x1;
+                if (kj < p.L) {
+                    x1 = *reinterpret_cast<const float4 *>(p.k1 + ((static_cast<size_t>(b) * p.L + kj) * p.hs + h) * d + e);
+                    x2 = *reinterpret_cast<const float4 *>(p.k2 + ((static_cast<size_t>(b) * p.L + kj) * p.hn + g) * d + e);
+                }
+                float *r1 = k1s + j * dp + e, *r2 = k2s + j * dp + e;
+                r1[0] = x1.x; r1[1] = x1.y; r1[2] = x1.z; r1[3] = x1.w;
+                r2[0] = x2.x; r2[1] = x2.y; r2[2] = x2.z; r2[3] = x2.w;
+            }
+        } else {
+#pragma unroll 4
+            for (int i = threadIdx.x; i < kKeys * d; i += blockDim.x) {
+                const int j = i / d, e = i % d, kj = k0 + j;
+                const bool in = kj < p.L;
+                k1s[j * dp + e] = in ? p.k1[((static_cast<size_t>(b) * p.L + kj) * p.hs + h) * d + e] : 0.f;
+                k2s[j * dp + e] = in ? p.k2[((static_cast<size_t>(b) * p.L + kj) * p.hn + g) * d + e] : 0.f;
+            }
         }
-        for (int i = threadIdx.x; i < kKeys * dv; i += blockDim.x) {
-            const int j = i / dv, c = i % dv, kj = k0 + j;
-            vs[i] = kj < p.L ? p.v[((static_cast<size_t>(b) * p.L + kj) * p.hs + h) * dv + c] : 0.f;
+        const int dv4 = dv / 4;
+#pragma unroll 4
+        for (int i = threadIdx.x; i < kKeys * dv4; i += blockDim.x) {
+            const int j = i / dv4, c = (i % dv4) * 4, kj = k0 + j;
+            *reinterpret_cast<float4 *>(vs + j * dv + c) =
+                kj < p.L ? *reinterpret_cast<const float4 *>(p.v + ((static_cast<size_t>(b) * p.L + kj) * p.hs + h) * dv + c)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         __syncthreads();
 
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            const int row = warp * 4 + rr;
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int row = warp * RPW + rr;
             const int qi = q0 + row;
             const int kj = k0 + lane;
             const bool visible = kj < p.L && (!p.causal || kj <= qi);
             float a1 = 0.f, a2 = 0.f;
             const float *q1r = q1s + row * d, *q2r = q2s + row * d;
             const float *k1r = k1s + lane * dp, *k2r = k2s + lane * dp;
+#pragma unroll 4
             for (int e = 0; e < d; ++e) {
                 a1 = fmaf(q1r[e], k1r[e], a1);
                 a2 = fmaf(q2r[e], k2r[e], a2);
@@ -148,8 +173,8 @@ gda_prefill_f32_kernel(const F32Params p) {
 
     const float lam = p.lambda[h];
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-        const int qi = q0 + warp * 4 + rr;
+    for (int rr = 0; rr < RPW; ++rr) {
+        const int qi = q0 + warp * RPW + rr;
         float o[NV];
         float ss = 0.f;
 #pragma unroll
@@ -167,10 +192,11 @@ gda_prefill_f32_kernel(const F32Params p) {
     }
 }
 
-template <int NV>
+template <int NV, int RPW, int DT>
 int launch_nv(const F32Params &p, cudaStream_t stream) {
+    constexpr int kRows = 4 * RPW;
     const size_t smem = sizeof(float) * (2 * kRows * p.d + 2 * kKeys * (p.d + 1) + kKeys * p.dv);
-    auto kern = gda_prefill_f32_kernel<NV>;
+    auto kern = gda_prefill_f32_kernel<NV, RPW, DT>;
     if (smem > 48 * 1024) {
         const cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -181,6 +207,18 @@ int launch_nv(const F32Params &p, cudaStream_t stream) {
     kern<<<grid, kThreadsF32, smem, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GDA_OK : record_cuda_error(e);
+}
+
+template <int NV>
+int launch_rows(const F32Params &p, bool one_row_per_warp, cudaStream_t stream) {
+    if (one_row_per_warp) {
+        if (p.d == 64) return launch_nv<NV, 1, 64>(p, stream);
+        if (p.d == 128) return launch_nv<NV, 1, 128>(p, stream);
+        return launch_nv<NV, 1, 0>(p, stream);
+    }
+    // four rows per warp; one for dv > 160 (more rows' accumulators would spill)
+    if constexpr (NV > 5) return launch_nv<NV, 1, 0>(p, stream);
+    else return launch_nv<NV, 4, 0>(p, stream);
 }
 
 }  // namespace
@@ -205,15 +243,21 @@ int launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream) {
     p.dv = a.dv;
     p.causal = a.causal;
     p.no_norm = (a.flags & GDA_FLAG_NO_NORM) ? 1 : 0;
+    // 16-row CTAs unless they would not fill the GPU's SMs: then one row per warp
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    const bool one = static_cast<long long>((a.L + 15) / 16) * a.hs * a.B < sms;
     switch (a.dv / 32) {
-        case 1: return launch_nv<1>(p, stream);
-        case 2: return launch_nv<2>(p, stream);
-        case 3: return launch_nv<3>(p, stream);
-        case 4: return launch_nv<4>(p, stream);
-        case 5: return launch_nv<5>(p, stream);
-        case 6: return launch_nv<6>(p, stream);
-        case 7: return launch_nv<7>(p, stream);
-        case 8: return launch_nv<8>(p, stream);
+        case 1: return launch_rows<1>(p, one, stream);
+        case 2: return launch_rows<2>(p, one, stream);
+        case 3: return launch_rows<3>(p, one, stream);
+        case 4: return launch_rows<4>(p, one, stream);
+        case 5: return launch_rows<5>(p, one, stream);
+        case 6: return launch_rows<6>(p, one, stream);
+        case 7: return launch_rows<7>(p, one, stream);
+        case 8: return launch_rows<8>(p, one, stream);
         default: return GDA_ERR_UNSUPPORTED;
     }
 }
