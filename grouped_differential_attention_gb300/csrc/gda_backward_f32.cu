@@ -35,7 +35,7 @@
 namespace gda {
 namespace {
 
-constexpr int kBRows = 16;       // query rows (row pass) or keys (column pass) per CTA
+constexpr int kBRows = 32;       // query rows (row pass) or keys (column pass) per CTA
 constexpr int kBTile = 32;       // keys (row pass) or query rows (column pass) per shared-memory tile
 constexpr int kBThreads = 256;   // 8 warps
 constexpr int kRPW = kBRows / (kBThreads / 32);   // rows (keys) per warp
@@ -69,18 +69,32 @@ __device__ __forceinline__ size_t rix(const BwdParams &p, int b, int i, int h) {
     return (static_cast<size_t>(b) * p.L + i) * p.hs + h;
 }
 
+// Shared-memory rows read one per lane are padded by 4 floats (16-byte
+// aligned float4 reads, at most the 4 wavefronts 512 bytes need); rows read
+// by the whole warp at once (broadcast) are not padded.  Each warp's rows
+// (keys) share every load: the row loops sit inside the load loops.
+
+template <int D>
+__device__ __forceinline__ float4 ld4(const float *base, int i) {
+    return reinterpret_cast<const float4 *>(base)[i];
+}
+
+__device__ __forceinline__ float dot4(const float4 &a, const float4 &b, float acc) {
+    return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
+}
+
 // -------------------------------------------------------------- row pass --
 template <int ND, int NV>   // d = 32 ND, dv = 32 NV
 __global__ void __launch_bounds__(kBThreads)
 gda_bwd_row_kernel(const BwdParams p) {
     extern __shared__ float sm[];
-    constexpr int d = 32 * ND, dv = 32 * NV, dp = d + 1, dvp = dv + 1;
-    float *q1s = sm;                       // [kBRows][d]
+    constexpr int d = 32 * ND, dv = 32 * NV, dk = d + 4, dvk = dv + 4;
+    float *q1s = sm;                       // [kBRows][d]      broadcast rows
     float *q2s = q1s + kBRows * d;         // [kBRows][d]
-    float *k1s = q2s + kBRows * d;         // [kBTile][d+1]   (+1: a lane per key row, no bank conflicts)
-    float *k2s = k1s + kBTile * dp;        // [kBTile][d+1]
-    float *vs = k2s + kBTile * dp;         // [kBTile][dv+1]
-    float *dos = vs + kBTile * dvp;        // [kBRows][dv]
+    float *k1s = q2s + kBRows * d;         // [kBTile][d+4]    one row per lane
+    float *k2s = k1s + kBTile * dk;        // [kBTile][d+4]
+    float *vs = k2s + kBTile * dk;         // [kBTile][dv+4]
+    float *dos = vs + kBTile * dvk;        // [kBRows][dv]     broadcast rows
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int q0 = blockIdx.x * kBRows;
@@ -88,41 +102,64 @@ gda_bwd_row_kernel(const BwdParams p) {
     const int g = h / (p.hs / p.hn);
     const float lam = p.lambda[h];
 
-    for (int t = threadIdx.x; t < kBRows * d; t += blockDim.x) {
-        const int r = t / d, e = t % d, qi = q0 + r;
-        const bool in = qi < p.L;
-        q1s[t] = in ? p.q1[rix(p, b, qi, h) * d + e] : 0.f;
-        q2s[t] = in ? p.q2[((static_cast<size_t>(b) * p.L + qi) * p.hn + g) * d + e] : 0.f;
+    for (int t = threadIdx.x; t < kBRows * d / 4; t += blockDim.x) {
+        const int r = t / (d / 4), e = (t % (d / 4)) * 4, qi = q0 + r;
+        float4 x1 = make_float4(0.f, 0.f, 0.f, 0.f), x2 = x1;
+        if (qi < p.L) {
+            x1 = *reinterpret_cast<const float4 *>(p.q1 + rix(p, b, qi, h) * d + e);
+            x2 = *reinterpret_cast<const float4 *>(p.q2 + ((static_cast<size_t>(b) * p.L + qi) * p.hn + g) * d + e);
+        }
+        *reinterpret_cast<float4 *>(q1s + r * d + e) = x1;
+        *reinterpret_cast<float4 *>(q2s + r * d + e) = x2;
     }
 
     auto load_keys = [&](int k0) {
         __syncthreads();
-        for (int t = threadIdx.x; t < kBTile * d; t += blockDim.x) {
-            const int j = t / d, e = t % d, kj = k0 + j;
-            const bool in = kj < p.L;
-            k1s[j * dp + e] = in ? p.k1[rix(p, b, kj, h) * d + e] : 0.f;
-            k2s[j * dp + e] = in ? p.k2[((static_cast<size_t>(b) * p.L + kj) * p.hn + g) * d + e] : 0.f;
+#pragma unroll 2
+        for (int t = threadIdx.x; t < kBTile * d / 4; t += blockDim.x) {
+            const int j = t / (d / 4), e = (t % (d / 4)) * 4, kj = k0 + j;
+            float4 x1 = make_float4(0.f, 0.f, 0.f, 0.f), x2 = x1;
+            if (kj < p.L) {
+                x1 = *reinterpret_cast<const float4 *>(p.k1 + rix(p, b, kj, h) * d + e);
+                x2 = *reinterpret_cast<const float4 *>(p.k2 + ((static_cast<size_t>(b) * p.L + kj) * p.hn + g) * d + e);
+            }
+            *reinterpret_cast<float4 *>(k1s + j * dk + e) = x1;
+            *reinterpret_cast<float4 *>(k2s + j * dk + e) = x2;
         }
-        for (int t = threadIdx.x; t < kBTile * dv; t += blockDim.x) {
-            const int j = t / dv, c = t % dv, kj = k0 + j;
-            vs[j * dvp + c] = kj < p.L ? p.v[rix(p, b, kj, h) * dv + c] : 0.f;
+#pragma unroll 2
+        for (int t = threadIdx.x; t < kBTile * dv / 4; t += blockDim.x) {
+            const int j = t / (dv / 4), c = (t % (dv / 4)) * 4, kj = k0 + j;
+            *reinterpret_cast<float4 *>(vs + j * dvk + c) =
+                kj < p.L ? *reinterpret_cast<const float4 *>(p.v + rix(p, b, kj, h) * dv + c)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         __syncthreads();
     };
-    auto logits = [&](int row, int k0, float &s1, float &s2) -> bool {
-        const int qi = q0 + row, kj = k0 + lane;
-        const bool visible = qi < p.L && kj < p.L && (!p.causal || kj <= qi);
-        float a1 = 0.f, a2 = 0.f;
-        const float *q1r = q1s + row * d, *q2r = q2s + row * d;
-        const float *k1r = k1s + lane * dp, *k2r = k2s + lane * dp;
-        #pragma unroll 4
-        for (int e = 0; e < d; ++e) {
-            a1 = fmaf(q1r[e], k1r[e], a1);
-            a2 = fmaf(q2r[e], k2r[e], a2);
+    // scaled logits of key k0 + lane against the warp's rows, both maps
+    auto logits = [&](float (&s1)[kRPW], float (&s2)[kRPW]) {
+        float a1[kRPW], a2[kRPW];
+#pragma unroll
+        for (int rr = 0; rr < kRPW; ++rr) a1[rr] = a2[rr] = 0.f;
+        const float *k1r = k1s + lane * dk, *k2r = k2s + lane * dk;
+#pragma unroll 4
+        for (int e4 = 0; e4 < d / 4; ++e4) {
+            const float4 x1 = ld4<d>(k1r, e4), x2 = ld4<d>(k2r, e4);
+#pragma unroll
+            for (int rr = 0; rr < kRPW; ++rr) {
+                const int row = warp * kRPW + rr;
+                a1[rr] = dot4(ld4<d>(q1s + row * d, e4), x1, a1[rr]);
+                a2[rr] = dot4(ld4<d>(q2s + row * d, e4), x2, a2[rr]);
+            }
         }
-        s1 = a1 * p.scale;
-        s2 = a2 * p.scale;
-        return visible;
+#pragma unroll
+        for (int rr = 0; rr < kRPW; ++rr) {
+            s1[rr] = a1[rr] * p.scale;
+            s2[rr] = a2[rr] * p.scale;
+        }
+    };
+    auto visible = [&](int rr, int k0) {
+        const int qi = q0 + warp * kRPW + rr, kj = k0 + lane;
+        return qi < p.L && kj < p.L && (!p.causal || kj <= qi);
     };
 
     // ---- sweep 1: the forward's online softmax (row statistics, O1, O2)
@@ -137,28 +174,28 @@ gda_bwd_row_kernel(const BwdParams p) {
     const int kv_end = p.causal ? min(p.L, q0 + kBRows) : p.L;
     for (int k0 = 0; k0 < kv_end; k0 += kBTile) {
         load_keys(k0);
+        float s1[kRPW], s2[kRPW], w1[kRPW], w2[kRPW];
+        logits(s1, s2);
 #pragma unroll
         for (int rr = 0; rr < kRPW; ++rr) {
-            const int row = warp * kRPW + rr;
-            float s1, s2;
-            const bool vis = logits(row, k0, s1, s2);
-            if (!vis) s1 = s2 = -INFINITY;
-            float w1 = 0.f, w2 = 0.f, al1 = 1.f, al2 = 1.f;
+            if (!visible(rr, k0)) s1[rr] = s2[rr] = -INFINITY;
+            float al1 = 1.f, al2 = 1.f;
+            w1[rr] = w2[rr] = 0.f;
             {
-                const float mn = fmaxf(m1[rr], warp_max_b(s1));
+                const float mn = fmaxf(m1[rr], warp_max_b(s1[rr]));
                 if (mn != -INFINITY) {
                     al1 = m1[rr] == -INFINITY ? 0.f : expf(m1[rr] - mn);
-                    w1 = s1 == -INFINITY ? 0.f : expf(s1 - mn);
-                    l1[rr] = l1[rr] * al1 + warp_sum_b(w1);
+                    w1[rr] = s1[rr] == -INFINITY ? 0.f : expf(s1[rr] - mn);
+                    l1[rr] = l1[rr] * al1 + warp_sum_b(w1[rr]);
                     m1[rr] = mn;
                 }
             }
             {
-                const float mn = fmaxf(m2[rr], warp_max_b(s2));
+                const float mn = fmaxf(m2[rr], warp_max_b(s2[rr]));
                 if (mn != -INFINITY) {
                     al2 = m2[rr] == -INFINITY ? 0.f : expf(m2[rr] - mn);
-                    w2 = s2 == -INFINITY ? 0.f : expf(s2 - mn);
-                    l2[rr] = l2[rr] * al2 + warp_sum_b(w2);
+                    w2[rr] = s2[rr] == -INFINITY ? 0.f : expf(s2[rr] - mn);
+                    l2[rr] = l2[rr] * al2 + warp_sum_b(w2[rr]);
                     m2[rr] = mn;
                 }
             }
@@ -167,15 +204,22 @@ gda_bwd_row_kernel(const BwdParams p) {
                 o1[rr][c] *= al1;
                 o2[rr][c] *= al2;
             }
-            #pragma unroll 4
-            for (int j = 0; j < kBTile; ++j) {
-                const float pj1 = __shfl_sync(0xffffffffu, w1, j);
-                const float pj2 = __shfl_sync(0xffffffffu, w2, j);
+        }
+#pragma unroll 4
+        for (int j = 0; j < kBTile; ++j) {
+            float pj1[kRPW], pj2[kRPW];
 #pragma unroll
-                for (int c = 0; c < NV; ++c) {
-                    const float vv = vs[j * dvp + lane + 32 * c];
-                    o1[rr][c] = fmaf(pj1, vv, o1[rr][c]);
-                    o2[rr][c] = fmaf(pj2, vv, o2[rr][c]);
+            for (int rr = 0; rr < kRPW; ++rr) {
+                pj1[rr] = __shfl_sync(0xffffffffu, w1[rr], j);
+                pj2[rr] = __shfl_sync(0xffffffffu, w2[rr], j);
+            }
+#pragma unroll
+            for (int c = 0; c < NV; ++c) {
+                const float vv = vs[j * dvk + lane + 32 * c];
+#pragma unroll
+                for (int rr = 0; rr < kRPW; ++rr) {
+                    o1[rr][c] = fmaf(pj1[rr], vv, o1[rr][c]);
+                    o2[rr][c] = fmaf(pj2[rr], vv, o2[rr][c]);
                 }
             }
         }
@@ -239,30 +283,42 @@ gda_bwd_row_kernel(const BwdParams p) {
         for (int e = 0; e < ND; ++e) dq1a[rr][e] = dq2a[rr][e] = 0.f;
     for (int k0 = 0; k0 < kv_end; k0 += kBTile) {
         load_keys(k0);
+        float s1[kRPW], s2[kRPW], dA[kRPW], ds1[kRPW], ds2[kRPW];
+        logits(s1, s2);
+#pragma unroll
+        for (int rr = 0; rr < kRPW; ++rr) dA[rr] = 0.f;
+        const float *vj = vs + lane * dvk;
+#pragma unroll 4
+        for (int c4 = 0; c4 < dv / 4; ++c4) {
+            const float4 x = ld4<dv>(vj, c4);
+#pragma unroll
+            for (int rr = 0; rr < kRPW; ++rr) dA[rr] = dot4(ld4<dv>(dos + (warp * kRPW + rr) * dv, c4), x, dA[rr]);
+        }
 #pragma unroll
         for (int rr = 0; rr < kRPW; ++rr) {
-            const int row = warp * kRPW + rr;
-            float s1, s2;
-            const bool vis = logits(row, k0, s1, s2);
-            float ds1 = 0.f, ds2 = 0.f;
-            if (vis) {
-                const float a1 = expf(s1 - m1[rr]) / l1[rr];
-                const float a2 = expf(s2 - m2[rr]) / l2[rr];
-                float dA = 0.f;
-                const float *dor = dos + row * dv, *vj = vs + lane * dvp;
-                #pragma unroll 4
-                for (int c = 0; c < dv; ++c) dA = fmaf(dor[c], vj[c], dA);
-                ds1 = a1 * (dA - D1[rr]);
-                ds2 = -lam * a2 * (dA - D2[rr]);
+            ds1[rr] = ds2[rr] = 0.f;
+            if (visible(rr, k0)) {
+                const float a1 = expf(s1[rr] - m1[rr]) / l1[rr];
+                const float a2 = expf(s2[rr] - m2[rr]) / l2[rr];
+                ds1[rr] = a1 * (dA[rr] - D1[rr]);
+                ds2[rr] = -lam * a2 * (dA[rr] - D2[rr]);
             }
-            #pragma unroll 4
-            for (int j = 0; j < kBTile; ++j) {
-                const float x1 = __shfl_sync(0xffffffffu, ds1, j);
-                const float x2 = __shfl_sync(0xffffffffu, ds2, j);
+        }
+#pragma unroll 4
+        for (int j = 0; j < kBTile; ++j) {
+            float x1[kRPW], x2[kRPW];
 #pragma unroll
-                for (int e = 0; e < ND; ++e) {
-                    dq1a[rr][e] = fmaf(x1, k1s[j * dp + lane + 32 * e], dq1a[rr][e]);
-                    dq2a[rr][e] = fmaf(x2, k2s[j * dp + lane + 32 * e], dq2a[rr][e]);
+            for (int rr = 0; rr < kRPW; ++rr) {
+                x1[rr] = __shfl_sync(0xffffffffu, ds1[rr], j);
+                x2[rr] = __shfl_sync(0xffffffffu, ds2[rr], j);
+            }
+#pragma unroll
+            for (int e = 0; e < ND; ++e) {
+                const float kk1 = k1s[j * dk + lane + 32 * e], kk2 = k2s[j * dk + lane + 32 * e];
+#pragma unroll
+                for (int rr = 0; rr < kRPW; ++rr) {
+                    dq1a[rr][e] = fmaf(x1[rr], kk1, dq1a[rr][e]);
+                    dq2a[rr][e] = fmaf(x2[rr], kk2, dq2a[rr][e]);
                 }
             }
         }
@@ -284,14 +340,14 @@ template <int ND, int NV>
 __global__ void __launch_bounds__(kBThreads)
 gda_bwd_col_kernel(const BwdParams p) {
     extern __shared__ float sm[];
-    constexpr int d = 32 * ND, dv = 32 * NV, dp = d + 1, dvp = dv + 1;
-    float *k1s = sm;                       // [kBRows][d]   this CTA's keys
+    constexpr int d = 32 * ND, dv = 32 * NV, dk = d + 4, dvk = dv + 4;
+    float *k1s = sm;                       // [kBRows][d]   this CTA's keys (broadcast rows)
     float *k2s = k1s + kBRows * d;         // [kBRows][d]
     float *vks = k2s + kBRows * d;         // [kBRows][dv]
-    float *q1s = vks + kBRows * dv;        // [kBTile][d+1] a tile of query rows
-    float *q2s = q1s + kBTile * dp;        // [kBTile][d+1]
-    float *dos = q2s + kBTile * dp;        // [kBTile][dv+1]
-    float *sts = dos + kBTile * dvp;       // [kBTile][6]
+    float *q1s = vks + kBRows * dv;        // [kBTile][d+4]  a tile of query rows (one per lane)
+    float *q2s = q1s + kBTile * dk;        // [kBTile][d+4]
+    float *dos = q2s + kBTile * dk;        // [kBTile][dv+4]
+    float *sts = dos + kBTile * dvk;       // [kBTile][6]
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int j0 = blockIdx.x * kBRows;
@@ -299,15 +355,21 @@ gda_bwd_col_kernel(const BwdParams p) {
     const int g = h / (p.hs / p.hn);
     const float lam = p.lambda[h];
 
-    for (int t = threadIdx.x; t < kBRows * d; t += blockDim.x) {
-        const int r = t / d, e = t % d, kj = j0 + r;
-        const bool in = kj < p.L;
-        k1s[t] = in ? p.k1[rix(p, b, kj, h) * d + e] : 0.f;
-        k2s[t] = in ? p.k2[((static_cast<size_t>(b) * p.L + kj) * p.hn + g) * d + e] : 0.f;
+    for (int t = threadIdx.x; t < kBRows * d / 4; t += blockDim.x) {
+        const int r = t / (d / 4), e = (t % (d / 4)) * 4, kj = j0 + r;
+        float4 x1 = make_float4(0.f, 0.f, 0.f, 0.f), x2 = x1;
+        if (kj < p.L) {
+            x1 = *reinterpret_cast<const float4 *>(p.k1 + rix(p, b, kj, h) * d + e);
+            x2 = *reinterpret_cast<const float4 *>(p.k2 + ((static_cast<size_t>(b) * p.L + kj) * p.hn + g) * d + e);
+        }
+        *reinterpret_cast<float4 *>(k1s + r * d + e) = x1;
+        *reinterpret_cast<float4 *>(k2s + r * d + e) = x2;
     }
-    for (int t = threadIdx.x; t < kBRows * dv; t += blockDim.x) {
-        const int r = t / dv, c = t % dv, kj = j0 + r;
-        vks[t] = kj < p.L ? p.v[rix(p, b, kj, h) * dv + c] : 0.f;
+    for (int t = threadIdx.x; t < kBRows * dv / 4; t += blockDim.x) {
+        const int r = t / (dv / 4), c = (t % (dv / 4)) * 4, kj = j0 + r;
+        *reinterpret_cast<float4 *>(vks + r * dv + c) =
+            kj < p.L ? *reinterpret_cast<const float4 *>(p.v + rix(p, b, kj, h) * dv + c)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
     float dva[kRPW][NV], dk1a[kRPW][ND], dk2a[kRPW][ND];
@@ -322,57 +384,92 @@ gda_bwd_col_kernel(const BwdParams p) {
     const int i_begin = p.causal ? (j0 / kBTile) * kBTile : 0;
     for (int i0 = i_begin; i0 < p.L; i0 += kBTile) {
         __syncthreads();
-        for (int t = threadIdx.x; t < kBTile * d; t += blockDim.x) {
-            const int i = t / d, e = t % d, qi = i0 + i;
-            const bool in = qi < p.L;
-            q1s[i * dp + e] = in ? p.q1[rix(p, b, qi, h) * d + e] : 0.f;
-            q2s[i * dp + e] = in ? p.q2[((static_cast<size_t>(b) * p.L + qi) * p.hn + g) * d + e] : 0.f;
+#pragma unroll 2
+        for (int t = threadIdx.x; t < kBTile * d / 4; t += blockDim.x) {
+            const int i = t / (d / 4), e = (t % (d / 4)) * 4, qi = i0 + i;
+            float4 x1 = make_float4(0.f, 0.f, 0.f, 0.f), x2 = x1;
+            if (qi < p.L) {
+                x1 = *reinterpret_cast<const float4 *>(p.q1 + rix(p, b, qi, h) * d + e);
+                x2 = *reinterpret_cast<const float4 *>(p.q2 + ((static_cast<size_t>(b) * p.L + qi) * p.hn + g) * d + e);
+            }
+            *reinterpret_cast<float4 *>(q1s + i * dk + e) = x1;
+            *reinterpret_cast<float4 *>(q2s + i * dk + e) = x2;
         }
-        for (int t = threadIdx.x; t < kBTile * dv; t += blockDim.x) {
-            const int i = t / dv, c = t % dv, qi = i0 + i;
-            dos[i * dvp + c] = qi < p.L ? p.dO[rix(p, b, qi, h) * dv + c] : 0.f;
+#pragma unroll 2
+        for (int t = threadIdx.x; t < kBTile * dv / 4; t += blockDim.x) {
+            const int i = t / (dv / 4), c = (t % (dv / 4)) * 4, qi = i0 + i;
+            *reinterpret_cast<float4 *>(dos + i * dvk + c) =
+                qi < p.L ? *reinterpret_cast<const float4 *>(p.dO + rix(p, b, qi, h) * dv + c)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         for (int t = threadIdx.x; t < kBTile * 6; t += blockDim.x) {
             const int i = t / 6, qi = i0 + i;
             sts[t] = qi < p.L ? p.stats[rix(p, b, qi, h) * 6 + t % 6] : (t % 6 == 1 || t % 6 == 3 ? 1.f : 0.f);
         }
         __syncthreads();
+
+        // query row i0 + lane against the warp's keys, both maps, and dA
+        float a1[kRPW], a2[kRPW], dA[kRPW];
+#pragma unroll
+        for (int kk = 0; kk < kRPW; ++kk) a1[kk] = a2[kk] = dA[kk] = 0.f;
+        {
+            const float *q1r = q1s + lane * dk, *q2r = q2s + lane * dk;
+#pragma unroll 4
+            for (int e4 = 0; e4 < d / 4; ++e4) {
+                const float4 y1 = ld4<d>(q1r, e4), y2 = ld4<d>(q2r, e4);
+#pragma unroll
+                for (int kk = 0; kk < kRPW; ++kk) {
+                    const int key = warp * kRPW + kk;
+                    a1[kk] = dot4(y1, ld4<d>(k1s + key * d, e4), a1[kk]);
+                    a2[kk] = dot4(y2, ld4<d>(k2s + key * d, e4), a2[kk]);
+                }
+            }
+            const float *dor = dos + lane * dvk;
+#pragma unroll 4
+            for (int c4 = 0; c4 < dv / 4; ++c4) {
+                const float4 y = ld4<dv>(dor, c4);
+#pragma unroll
+                for (int kk = 0; kk < kRPW; ++kk) dA[kk] = dot4(y, ld4<dv>(vks + (warp * kRPW + kk) * dv, c4), dA[kk]);
+            }
+        }
+        const int qi = i0 + lane;
+        const float *st = sts + lane * 6;
+        float w[kRPW], ds1[kRPW], ds2[kRPW];
 #pragma unroll
         for (int kk = 0; kk < kRPW; ++kk) {
-            const int key = warp * kRPW + kk, kj = j0 + key;
-            const int qi = i0 + lane;
+            const int kj = j0 + warp * kRPW + kk;
             const bool vis = qi < p.L && kj < p.L && (!p.causal || kj <= qi);
-            float w = 0.f, ds1 = 0.f, ds2 = 0.f;
+            w[kk] = ds1[kk] = ds2[kk] = 0.f;
             if (vis) {
-                float a1 = 0.f, a2 = 0.f, dA = 0.f;
-                const float *q1r = q1s + lane * dp, *q2r = q2s + lane * dp;
-                const float *k1r = k1s + key * d, *k2r = k2s + key * d;
-                #pragma unroll 4
-                for (int e = 0; e < d; ++e) {
-                    a1 = fmaf(q1r[e], k1r[e], a1);
-                    a2 = fmaf(q2r[e], k2r[e], a2);
-                }
-                const float *st = sts + lane * 6;
-                const float p1 = expf(a1 * p.scale - st[0]) / st[1];
-                const float p2 = expf(a2 * p.scale - st[2]) / st[3];
-                const float *dor = dos + lane * dvp, *vr = vks + key * dv;
-                #pragma unroll 4
-                for (int c = 0; c < dv; ++c) dA = fmaf(dor[c], vr[c], dA);
-                w = p1 - lam * p2;
-                ds1 = p1 * (dA - st[4]);
-                ds2 = -lam * p2 * (dA - st[5]);
+                const float p1 = expf(a1[kk] * p.scale - st[0]) / st[1];
+                const float p2 = expf(a2[kk] * p.scale - st[2]) / st[3];
+                w[kk] = p1 - lam * p2;
+                ds1[kk] = p1 * (dA[kk] - st[4]);
+                ds2[kk] = -lam * p2 * (dA[kk] - st[5]);
             }
-            #pragma unroll 4
-            for (int i = 0; i < kBTile; ++i) {
-                const float wi = __shfl_sync(0xffffffffu, w, i);
-                const float x1 = __shfl_sync(0xffffffffu, ds1, i);
-                const float x2 = __shfl_sync(0xffffffffu, ds2, i);
+        }
+#pragma unroll 4
+        for (int i = 0; i < kBTile; ++i) {
+            float wi[kRPW], x1[kRPW], x2[kRPW];
 #pragma unroll
-                for (int c = 0; c < NV; ++c) dva[kk][c] = fmaf(wi, dos[i * dvp + lane + 32 * c], dva[kk][c]);
+            for (int kk = 0; kk < kRPW; ++kk) {
+                wi[kk] = __shfl_sync(0xffffffffu, w[kk], i);
+                x1[kk] = __shfl_sync(0xffffffffu, ds1[kk], i);
+                x2[kk] = __shfl_sync(0xffffffffu, ds2[kk], i);
+            }
 #pragma unroll
-                for (int e = 0; e < ND; ++e) {
-                    dk1a[kk][e] = fmaf(x1, q1s[i * dp + lane + 32 * e], dk1a[kk][e]);
-                    dk2a[kk][e] = fmaf(x2, q2s[i * dp + lane + 32 * e], dk2a[kk][e]);
+            for (int c = 0; c < NV; ++c) {
+                const float dd = dos[i * dvk + lane + 32 * c];
+#pragma unroll
+                for (int kk = 0; kk < kRPW; ++kk) dva[kk][c] = fmaf(wi[kk], dd, dva[kk][c]);
+            }
+#pragma unroll
+            for (int e = 0; e < ND; ++e) {
+                const float qq1 = q1s[i * dk + lane + 32 * e], qq2 = q2s[i * dk + lane + 32 * e];
+#pragma unroll
+                for (int kk = 0; kk < kRPW; ++kk) {
+                    dk1a[kk][e] = fmaf(x1[kk], qq1, dk1a[kk][e]);
+                    dk2a[kk][e] = fmaf(x2[kk], qq2, dk2a[kk][e]);
                 }
             }
         }
@@ -432,9 +529,9 @@ gda_bwd_reduce_kernel(const BwdParams p, int n_sum_blocks) {
 template <int ND, int NV>
 int launch_bwd(const BwdParams &p, cudaStream_t stream) {
     constexpr int d = 32 * ND, dv = 32 * NV;
-    const size_t smem_row = sizeof(float) * (2 * kBRows * d + 2 * kBTile * (d + 1) + kBTile * (dv + 1) + kBRows * dv);
+    const size_t smem_row = sizeof(float) * (2 * kBRows * d + 2 * kBTile * (d + 4) + kBTile * (dv + 4) + kBRows * dv);
     const size_t smem_col =
-        sizeof(float) * (2 * kBRows * d + kBRows * dv + 2 * kBTile * (d + 1) + kBTile * (dv + 1) + kBTile * 6);
+        sizeof(float) * (2 * kBRows * d + kBRows * dv + 2 * kBTile * (d + 4) + kBTile * (dv + 4) + kBTile * 6);
     auto rk = gda_bwd_row_kernel<ND, NV>;
     auto ck = gda_bwd_col_kernel<ND, NV>;
     cudaError_t e = cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_row));
@@ -455,7 +552,9 @@ int launch_bwd(const BwdParams &p, cudaStream_t stream) {
 
 size_t backward_f32_workspace_bytes(int B, int L, int hs, int d, int dv) {
     const size_t rows = static_cast<size_t>(B) * L * hs;
-    return sizeof(float) * rows * (6 + static_cast<size_t>(dv) + 2 * static_cast<size_t>(d) + 1) + 256;
+    // stats (6 per row, padded to a multiple of 4) | dO | dq2 shares | dk2 shares | dlambda terms
+    return sizeof(float) * ((rows * 6 + 3) / 4 * 4 + rows * (static_cast<size_t>(dv) + 2 * static_cast<size_t>(d) + 1)) +
+           256;
 }
 
 int launch_backward_f32(const BackwardArgs &a, cudaStream_t stream) {
@@ -476,7 +575,7 @@ int launch_backward_f32(const BackwardArgs &a, cudaStream_t stream) {
     const size_t rows = static_cast<size_t>(a.B) * a.L * a.hs;
     float *w = static_cast<float *>(a.workspace);
     p.stats = w;
-    p.dO = p.stats + rows * 6;
+    p.dO = p.stats + (rows * 6 + 3) / 4 * 4;     // 16-byte aligned: read as float4
     p.dq2h = p.dO + rows * a.dv;
     p.dk2h = p.dq2h + rows * a.d;
     p.dlam_row = p.dk2h + rows * a.d;

@@ -54,6 +54,7 @@ SMALL = [
     (1, 129, 8, 2, 128, 128, False),
     (1, 200, 6, 3, 64, 256, True),
     (2, 33, 4, 2, 128, 64, True),
+    (1, 77, 3, 1, 64, 128, True),      # odd B * L * h_s: workspace segments stay 16-byte aligned
 ]
 
 
