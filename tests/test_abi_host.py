@@ -309,3 +309,34 @@ def test_decode_paged_fp8_rejects_bad_arguments(lib):
     assert call(scale_off=2) == MISALIGNED
     assert call(ws=None) == WORKSPACE
     assert call(ws_bytes=16) == WORKSPACE
+
+
+def test_binding_refuses_host_tensors_for_every_entry():
+    """Every binding refuses CPU tensors before calling the library (there is
+    no CPU fallback)."""
+    import grouped_differential_attention_gb300 as gda
+    bf, f32 = torch.bfloat16, torch.float32
+    q = torch.zeros(1, 4, 2, 64, dtype=bf)
+    v = torch.zeros(1, 4, 2, 128, dtype=bf)
+    lam = torch.zeros(2)
+    qf, vf = q.float(), v.float()
+    calls = [
+        lambda: gda.gda_attn_fwd_2pass(q, q, q, q, v, lam, 0.8),
+        lambda: gda.gda_attn_fwd_chunk(q, q, q, q, v, lam, 0.8),
+        lambda: gda.gda_attn_fwd_f32(qf, qf, qf, qf, vf, lam, 0.8),
+        lambda: gda.gda_attn_bwd(qf, qf, qf, qf, vf, lam, 0.8, vf),
+        lambda: gda.gda_attn_bwd_bf16(q, q, q, q, v, lam, 0.8, v),
+    ]
+    qd = torch.zeros(1, 2, 64, dtype=bf)
+    cache = torch.zeros(1, 16, 2, 64, dtype=torch.uint8)
+    vcache = torch.zeros(1, 16, 2, 128, dtype=torch.uint8)
+    lens = torch.ones(1, dtype=torch.int32)
+    sc = torch.ones(2, dtype=f32)
+    table = torch.zeros(1, 1, dtype=torch.int32)
+    calls += [
+        lambda: gda.gda_attn_decode_fp8(qd, qd, cache, cache, vcache, sc, sc, sc, lens, lam, 0.8),
+        lambda: gda.gda_attn_decode_paged_fp8(qd, qd, cache, cache, vcache, sc, sc, sc, table, lens, lam, 0.8),
+    ]
+    for call in calls:
+        with pytest.raises((ValueError, TypeError)):
+            call()
