@@ -351,6 +351,15 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
             const float lam = p.lambda[h];
             const float neg1 = in ? -p.lse[(static_cast<size_t>(b) * heads + h) * p.Lp + qrow] : -INFINITY;
             const float neg2 = in ? -p.lse[(static_cast<size_t>(b) * heads + p.hs + g) * p.Lp + qrow] : -INFINITY;
+            // this thread's 32 dy values, requested now so the loads complete during the tile loop
+            const int c0 = grp * 32;
+            const size_t rowix = (static_cast<size_t>(b) * p.L + (in ? qrow : 0)) * p.hs + h;
+            uint4 dyv[4];
+            {
+                const uint4 *dyrow = reinterpret_cast<const uint4 *>(p.dy + rowix * kDV + c0);
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4) dyv[v4] = in ? dyrow[v4] : make_uint4(0, 0, 0, 0);
+            }
             bool ok = true;
             for (int j = 0; j < nkv; ++j) {
                 const uint32_t gs = gt + j;
@@ -399,9 +408,6 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
             ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
             if (ok) ok = warp_wait(&ctl->o_final, r & 1, p.err, abort_flag);
             tc_fence_after();
-            const int c0 = grp * 32;
-            const size_t rowix = (static_cast<size_t>(b) * p.L + (in ? qrow : 0)) * p.hs + h;
-            const uint4 *dyrow = reinterpret_cast<const uint4 *>(p.dy + rowix * kDV + c0);
             float ss = 0.f, dyo = 0.f;
             if (ok) {
 #pragma unroll
@@ -411,10 +417,7 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                     tmem_ld16(tmem + lane_off + tO2 + c0 + cc * 16, o2);
                     tmem_ld_wait_regs16(o1);
                     reg_fence16(o2);
-                    uint4 dq[2];
-#pragma unroll
-                    for (int v4 = 0; v4 < 2; ++v4) dq[v4] = in ? dyrow[cc * 2 + v4] : make_uint4(0, 0, 0, 0);
-                    const uint32_t *dw = reinterpret_cast<const uint32_t *>(dq);
+                    const uint32_t *dw = reinterpret_cast<const uint32_t *>(&dyv[cc * 2]);
 #pragma unroll
                     for (int e = 0; e < 16; e += 2) {
                         const float oa = __uint_as_float(o1[e]) - __fmul_rn(__uint_as_float(o2[e]), lam);
@@ -446,10 +449,7 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                     tmem_ld16(tmem + lane_off + tO2 + c0 + cc * 16, o2);
                     tmem_ld_wait_regs16(o1);
                     reg_fence16(o2);
-                    uint4 dq[2];
-#pragma unroll
-                    for (int v4 = 0; v4 < 2; ++v4) dq[v4] = in ? dyrow[cc * 2 + v4] : make_uint4(0, 0, 0, 0);
-                    const uint32_t *dw = reinterpret_cast<const uint32_t *>(dq);
+                    const uint32_t *dw = reinterpret_cast<const uint32_t *>(&dyv[cc * 2]);
                     uint32_t pk[8];
 #pragma unroll
                     for (int e = 0; e < 16; e += 2) {
