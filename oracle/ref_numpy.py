@@ -112,3 +112,36 @@ def row_logsumexp(q, k, causal=True):
         s = np.where(np.triu(np.ones((L, L), dtype=bool), k=1), -np.inf, s)
     m = np.max(s, axis=-1)
     return m + np.log(np.sum(np.exp(s - m[..., None]), axis=-1))
+
+
+def gda_magnitudes(q1, k1, q2, k2, v, lam, lambda_init, causal=True, eps=1e-5, norm=True):
+    """Size of the terms that make up each output element, float64, [B,L,hs,dv].
+
+    The output is a sum over keys of (a1_ij - lambda_h a2_ij) v_jc with a1, a2
+    the two softmax maps ("Differential Attention in Large Language Models
+    ...", section "Differential Attention Architecture"; noise map of head
+    h // (h_s / h_n) per the "Grouped Differential Attention" abstract).  This
+    returns the same sum with every term replaced by its absolute value,
+    sum_j (a1_ij + |lambda_h| a2_ij) |v_jc|, and with ``norm`` that sum scaled
+    like the output, by |1 - lambda_init| / sqrt(mean_c(o_c^2) + eps)
+    (section "Headwise Normalization").  It bounds |output| and measures how
+    much a relative rounding of every map weight can move the output when
+    the two maps nearly cancel (lambda near 1).
+    """
+    q1, k1, q2, k2, v = (np.asarray(t, dtype=np.float64) for t in (q1, k1, q2, k2, v))
+    lam = np.asarray(lam, dtype=np.float64).reshape(-1)
+    B, L, hs, d = q1.shape
+    hn = q2.shape[2]
+    s1 = np.einsum("bihd,bjhd->bhij", q1, k1) / np.sqrt(d)
+    s2 = np.einsum("bigd,bjgd->bgij", q2, k2) / np.sqrt(d)
+    if causal:
+        hidden = np.triu(np.ones((L, L), dtype=bool), k=1)
+        s1 = np.where(hidden, -np.inf, s1)
+        s2 = np.where(hidden, -np.inf, s2)
+    a1 = _softmax_last(s1)
+    a2 = _softmax_last(s2)[:, contiguous_groups(hs, hn)]
+    mag = np.einsum("bhij,bjhe->bihe", a1 + np.abs(lam)[None, :, None, None] * a2, np.abs(v))
+    if norm:
+        o = np.einsum("bhij,bjhe->bihe", a1 - lam[None, :, None, None] * a2, v)
+        mag = abs(1.0 - lambda_init) * mag / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    return mag

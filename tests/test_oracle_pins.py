@@ -121,6 +121,64 @@ def test_rows_of_each_map_sum_to_one(oracle_mod, causal):
                                rtol=1e-14, atol=1e-14)
 
 
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_lambda_outside_unit_interval(oracle_mod, causal):
+    """lambda = -1 ... 2 (0 and 1 included): nothing in the definition clamps it.
+
+    Pre-norm output = SDPA(Q1,K1,V) - lambda_h SDPA(Q2_rep,K2_rep,V) as above,
+    and with V = 1 the norm's closed form holds for these lambda too.  At
+    lambda = 1 the closed form is 0 while the pre-norm value is the float64
+    residue of 1 - sum(p2) (a few ulp times L), which the norm scales by up
+    to (1 - lambda_init) / sqrt(eps) ~ 63: hence the 1e-12 absolute slack."""
+    hs, hn = 7, 1
+    q1, k1, q2, k2, v, _ = case(2, 23, hs, hn, 16, 32, seed=19)
+    lam = torch.linspace(-1.0, 2.0, hs)
+    lam64 = lam.double().numpy()
+    a = sdpa64(q1, k1, v, causal)
+    b = sdpa64(q2.repeat_interleave(hs // hn, dim=2), k2.repeat_interleave(hs // hn, dim=2), v, causal)
+    got = oracle_mod.prefill(q1, k1, q2, k2, v, lam, 0.8, causal=causal, norm=False)
+    np.testing.assert_allclose(got, a - lam64[None, None, :, None] * b, rtol=0, atol=1e-12)
+    post = oracle_mod.prefill(q1, k1, q2, k2, torch.ones_like(v), lam, 0.8, causal=causal)
+    closed = 0.2 * (1 - lam64) / np.sqrt((1 - lam64) ** 2 + 1e-5)
+    np.testing.assert_allclose(post, np.broadcast_to(closed[None, None, :, None], post.shape),
+                               rtol=1e-14, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_magnitudes_are_library_attention_of_absolute_values(causal):
+    """Pre-norm magnitudes = SDPA(Q1, K1, |V|) + |lambda_h| SDPA(Q2_rep, K2_rep, |V|):
+    pins the maps, the group map and the absolute values of lambda and V."""
+    hs, hn = 6, 2
+    q1, k1, q2, k2, v, _ = case(2, 19, hs, hn, 16, 32, seed=25)
+    lam = torch.linspace(-1.0, 2.0, hs)
+    r = hs // hn
+    want = (sdpa64(q1, k1, v.abs(), causal) + np.abs(lam.double().numpy())[None, None, :, None]
+            * sdpa64(q2.repeat_interleave(r, dim=2), k2.repeat_interleave(r, dim=2), v.abs(), causal))
+    got = ref_numpy.gda_magnitudes(q1, k1, q2, k2, v, lam, 0.8, causal=causal, norm=False)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def test_magnitudes_equal_the_output_when_terms_share_a_sign(oracle_mod):
+    """lambda <= 0 and V >= 0: every term (a1 - lambda a2) v is >= 0, so the
+    sum of absolute terms is the output itself, with and without the norm."""
+    q1, k1, q2, k2, v, _ = case(1, 23, 4, 2, 16, 32, seed=27)
+    v = v.abs()
+    lam = torch.tensor([0.0, -0.3, -1.0, -2.5])
+    for norm in (False, True):
+        out = oracle_mod.prefill(q1, k1, q2, k2, v, lam, 0.8, norm=norm)
+        mag = ref_numpy.gda_magnitudes(q1, k1, q2, k2, v, lam, 0.8, norm=norm)
+        np.testing.assert_allclose(mag, out, rtol=1e-12, atol=1e-14)
+
+
+def test_magnitudes_bound_the_output(oracle_mod):
+    q1, k1, q2, k2, v, _ = case(2, 31, 7, 1, 16, 32, seed=29)
+    lam = torch.linspace(-1.0, 2.0, 7)
+    for norm in (False, True):
+        out = oracle_mod.prefill(q1, k1, q2, k2, v, lam, 0.8, norm=norm)
+        mag = ref_numpy.gda_magnitudes(q1, k1, q2, k2, v, lam, 0.8, norm=norm)
+        assert np.all(np.abs(out) <= mag + 1e-12)
+
 def test_first_row_under_causal_mask(oracle_mod):
     """Row 0 sees only key 0: y0 = (1-li)(1-lam) v0 / sqrt(mean(((1-lam) v0)^2) + eps)."""
     q1, k1, q2, k2, v, lam = case(2, 17, 6, 3, 16, 32, seed=11)
