@@ -504,8 +504,14 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
             tmem_ld_wait();
 
             // ------------------------------------------------ epilogue of the item
+            // A row's two halves (map 0's warp: columns 0-63 of O1 and O2, map
+            // 1's warp: columns 64-127) sit in the two warps of one lane
+            // quarter; only those two warps exchange the row sums and the sums
+            // of squares, on a named barrier of their own, so a pair never
+            // waits for the other quarters.
+            const uint32_t pair_bar = 2 + quarter;
             ctl->l_row[m][row] = l;
-            named_bar_sync(1, 32 * kSoftmaxWarps);
+            named_bar_sync(pair_bar, 64);
             const float l1 = ctl->l_row[0][row];
             const float l2 = ctl->l_row[1][row];
             ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
@@ -534,7 +540,7 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                 }
             }
             ctl->ss_part[m][row] = ss;
-            named_bar_sync(1, 32 * kSoftmaxWarps);
+            named_bar_sync(pair_bar, 64);
             float ss_tot = ctl->ss_part[0][row] + ctl->ss_part[1][row];
             if (p.nslices == 2) {
                 const int pb = r & 1;
@@ -617,8 +623,10 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
             tc_fence_before();
             mbar_arrive(&ctl->o_free);
             gt += nkv;
-            // every softmax thread agrees on whether to go on
-            if (bar_red_or(1, 32 * kSoftmaxWarps, !ok || *abort_flag)) break;
+            // both warps of the pair agree on whether to go on; pairs share no
+            // named barrier, so one that stops early cannot block another
+            // (every mbarrier wait is bounded and sees the abort flag)
+            if (bar_red_or(pair_bar, 64, !ok || *abort_flag)) break;
         }
     }
 
