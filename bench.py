@@ -1,11 +1,14 @@
 """Benchmark of the grouped differential attention hot path on GB300.
 
-One JSON line on rank 0.  A step is one causal prefill of the 3:1 workload
-(B=4, L=2048, 12 signal + 4 noise heads, d=64, dv=128, bf16 I/O) through
+One JSON line on rank 0.  A step is one causal prefill of the long-context
+3:1 workload (B=1, L=32768, 24 signal + 8 noise heads, d=64, dv=128, 1% of
+key positions boosted x4, bf16 I/O; the largest prefill workload) through
 gda_attn_fwd; `value` is its throughput in TFLOP/s (causal-pair flop count
-below) with the inputs already in HBM; `decode` reports the 64-sequence
-split-KV decode in GB/s of KV cache read.  Inputs are synthetic (seeded
-normal tensors at the workloads' shapes).
+below) with the inputs already in HBM.  Side measurements in the same line:
+the 3:1 B=4 L=2048 and 4:1 d=128 dv=256 prefills, the 64-sequence split-KV
+decode in GB/s of KV cache read (and its fp8 / paged variants), chunked
+prefill, the backward passes.  Inputs are synthetic (seeded normal tensors
+at the workloads' shapes).
 
 Flop count per causal (query, key) pair: 2 d (h_s + h_n) for the logits of
 every signal head and, once per noise head, of the shared noise map, plus
@@ -101,14 +104,17 @@ def kernel_hash(kind="prefill"):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kind="prefill"):
-    """DRAM bytes per launch from the committed ncu summary, if it matches the kernel."""
+def profiled_traffic(kind="prefill", workload=None):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the
+    kernel's sources and (when given) the workload."""
     try:
         with open(PROFILES[kind][0]) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None, None
     if rec.get("kernel_hash") != kernel_hash(kind):
+        return None, None
+    if workload is not None and rec.get("workload") != workload:
         return None, None
     return rec.get("dram_bytes_per_launch"), rec.get("workload")
 
@@ -396,7 +402,41 @@ def run_gda(args, world, rank, local):
     dp8_ms_step = ev8.elapsed_time(ev9) / dec_steps
     del dpg8
 
+    # ---- the 3:1 B=4 L=2048 workload through gda_attn_fwd (rotating input sets, > L2)
+    w2 = W.GDA3_PREFILL_L2048
+    sets2 = []
+    for s_ in range(N_INPUT_SETS):
+        if s_ == 0:
+            base2 = [t.to(dev) for t in W.make_prefill_inputs(w2, seed=rank * 100 + 7)]
+            sets2.append(base2)
+        else:
+            sets2.append([t.clone() for t in base2])
+    out2 = torch.empty((w2.B, w2.L, w2.h_s, w2.dv), dtype=torch.bfloat16, device=dev)
+
+    def step2(i, flags=0):
+        q1, k1, q2, k2, v, lam = sets2[i % N_INPUT_SETS]
+        gda.gda_attn_fwd(q1, k1, q2, k2, v, lam, w2.lambda_init, causal=w2.causal, eps=w2.eps, out=out2,
+                         flags=flags)
+
+    ms2 = {}
+    for tag, fl in (("default", 0), ("single_pass", gda.GDA_FLAG_SINGLE_PASS)):
+        for i in range(10):
+            step2(i, fl)
+        torch.cuda.synchronize(dev)
+        n2 = 200
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(n2):
+            step2(i, fl)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms2[tag] = ev0.elapsed_time(ev1) / n2
+    fl2 = prefill_flops(w2.B, w2.L, w2.h_s, w2.h_n, w2.d, w2.dv, w2.causal)
+    fl2_min = prefill_min_flops(w2.B, w2.L, w2.h_s, w2.h_n, w2.d, w2.dv)
+    tf2 = fl2 / (ms2["default"] * 1e-3) / 1e12
+
     # ---- chunked prefill: 512 new rows continuing a 7680-row cached prefix
+    w = w2
     ck_L, ck_Lk = 512, 8192
     g = torch.Generator().manual_seed(rank + 21)
     ck = [torch.randn(w.B, ck_L, w.h_s, w.d, generator=g).to(torch.bfloat16),
@@ -404,7 +444,7 @@ def run_gda(args, world, rank, local):
           torch.randn(w.B, ck_L, w.h_n, w.d, generator=g).to(torch.bfloat16),
           torch.randn(w.B, ck_Lk, w.h_n, w.d, generator=g).to(torch.bfloat16),
           torch.randn(w.B, ck_Lk, w.h_s, w.dv, generator=g).to(torch.bfloat16)]
-    ck = [t.to(dev) for t in ck] + [sets[0][5]]
+    ck = [t.to(dev) for t in ck] + [sets2[0][5]]
     ck_out = torch.empty(w.B, ck_L, w.h_s, w.dv, dtype=torch.bfloat16, device=dev)
     ck_flops = row_flops(w.B, range(ck_Lk - ck_L, ck_Lk), w.h_s, w.h_n, w.d, w.dv)
     for _ in range(5):
@@ -422,6 +462,7 @@ def run_gda(args, world, rank, local):
 
     # ---- per-launch distribution of the headline kernel: 50 launches, each timed alone
     # (10 warm-up launches first), rotating input sets
+    w = W.PREFILL_WORKLOADS[args.workload]
     for i in range(10):
         step(i)
     torch.cuda.synchronize(dev)
@@ -449,13 +490,14 @@ def run_gda(args, world, rank, local):
     f32_us = sorted(a.elapsed_time(b) * 1e3 for a, b in f32_ev)
     del f32_in, f32_out
 
-    # ---- two-pass prefill (difference map before the value product) on the same inputs
+    # ---- two-pass prefill (difference map before the value product) on the 3:1 L=2048 inputs
+    w = w2
     tp_ws = torch.empty(gda.gda_attn_fwd_2pass_workspace_size(w.B, w.L, w.h_s, w.h_n), dtype=torch.uint8,
                         device=dev)
-    tp_out = torch.empty_like(out)
+    tp_out = torch.empty_like(out2)
 
     def tpstep(i):
-        q1, k1, q2, k2, v, lam = sets[i % N_INPUT_SETS]
+        q1, k1, q2, k2, v, lam = sets2[i % N_INPUT_SETS]
         gda.gda_attn_fwd_2pass(q1, k1, q2, k2, v, lam, w.lambda_init, causal=w.causal, eps=w.eps, out=tp_out,
                                workspace=tp_ws)
 
@@ -473,16 +515,22 @@ def run_gda(args, world, rank, local):
     tp_tflops = prefill_flops(w.B, w.L, w.h_s, w.h_n, w.d, w.dv, w.causal) / (tp_ms * 1e-3) / 1e12
     del tp_ws, tp_out
 
-    # ---- the 4:1 d=128 dv=256 prefill through gda_attn_fwd (two-pass kernels at dv = 256), and
-    # the same call held to the single-pass kernel; one input set of 302 MB (larger than L2)
+    # ---- the 4:1 d=128 dv=256 prefill through gda_attn_fwd_2pass (caller workspace) and through
+    # gda_attn_fwd (single pass, no workspace); one input set of 302 MB (larger than L2)
     w4 = W.GDA4_PREFILL_L8192
     in4 = [t.to(dev) for t in W.make_prefill_inputs(w4, seed=rank + 41)]
     out4 = torch.empty((w4.B, w4.L, w4.h_s, w4.dv), dtype=torch.bfloat16, device=dev)
+    ws4 = torch.empty(gda.gda_attn_fwd_2pass_workspace_size(w4.B, w4.L, w4.h_s, w4.h_n), dtype=torch.uint8,
+                      device=dev)
     fl4 = prefill_flops(w4.B, w4.L, w4.h_s, w4.h_n, w4.d, w4.dv, w4.causal)
     ms4 = {}
-    for tag, fl in (("default", 0), ("single_pass", gda.GDA_FLAG_SINGLE_PASS)):
+    for tag in ("two_pass", "single_pass"):
         def step4():
-            gda.gda_attn_fwd(*in4, w4.lambda_init, causal=w4.causal, eps=w4.eps, out=out4, flags=fl)
+            if tag == "two_pass":
+                gda.gda_attn_fwd_2pass(*in4, w4.lambda_init, causal=w4.causal, eps=w4.eps, out=out4,
+                                       workspace=ws4)
+            else:
+                gda.gda_attn_fwd(*in4, w4.lambda_init, causal=w4.causal, eps=w4.eps, out=out4)
         for _ in range(3):
             step4()
         torch.cuda.synchronize(dev)
@@ -494,9 +542,10 @@ def run_gda(args, world, rank, local):
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         ms4[tag] = ev0.elapsed_time(ev1) / n4
-    del in4, out4
+    del in4, out4, ws4
 
     # ---- one attention training step: forward, then the tensor-core backward of its inputs
+    w = w2
     tr_in = [t.to(dev) for t in W.make_backward_inputs(w, seed=rank + 61)]
     tr_out = torch.empty((w.B, w.L, w.h_s, w.dv), dtype=torch.bfloat16, device=dev)
     tr_ws = torch.empty(gda.gda_attn_bwd_bf16_workspace_size(w.B, w.L, w.h_s, w.h_n, w.dv), dtype=torch.uint8,
@@ -590,6 +639,8 @@ def run_gda(args, world, rank, local):
     lam_us = ev4.elapsed_time(ev5) / lam_steps * 1e3
     clocks = sampler.stop()
     dev_err = gda.gda_device_error(clear=True)
+    w = W.PREFILL_WORKLOADS[args.workload]
+    del sets2, out2
 
     # ---- end to end through the public API with pinned host buffers: every step copies its
     # inputs host -> device, runs gda_attn_fwd and copies its output device -> host.  Copies
@@ -663,8 +714,8 @@ def run_gda(args, world, rank, local):
     value = world * flops * args.steps / (prefill_ms * 1e-3) / 1e12
     per_launch_s = ms_per_step * 1e-3
     achieved = flops / per_launch_s / 1e12
-    traffic, traffic_wl = profiled_traffic("prefill")
-    dec_traffic, dec_traffic_wl = profiled_traffic("decode")
+    traffic, traffic_wl = profiled_traffic("prefill", w.name)
+    dec_traffic, dec_traffic_wl = profiled_traffic("decode", dw.name)
     dec_bytes = decode_bytes(lens_host, dw.h_s, dw.h_n, dw.d, dw.dv)
     dec_ms_step = decode_ms / dec_steps
     dec_gbs = dec_bytes / (dec_ms_step * 1e-3) / 1e9
@@ -760,19 +811,28 @@ def run_gda(args, world, rank, local):
                                             "pass 2 one P V product per head with P = A1 - lambda A2",
                           "value": tp_tflops, "unit": "TFLOP/s", "ms_per_step": tp_ms, "steps": tp_steps,
                           "gpu_launches": 2 * tp_steps,
-                          "speed_vs_single_pass": tp_tflops / achieved,
+                          "speed_vs_gda_attn_fwd": tp_tflops / tf2,
                           "flops_counted": "the single-pass kernel's algorithmic count, so value ratios are "
                                            "time ratios",
                           "roofline": {"bound": "tensor", "achieved": tp_tflops, "peak": peaks["bf16_tflops"],
                                        "unit": "TFLOP/s", "frac": tp_tflops / peaks["bf16_tflops"]}},
-        "prefill_4to1": {"workload": w4.name + " through gda_attn_fwd (two-pass kernels at dv = 256)",
-                         "value": fl4 / (ms4["default"] * 1e-3) / 1e12, "unit": "TFLOP/s",
-                         "ms_per_step": ms4["default"], "steps": 20, "gpu_launches": 2 * 20,
-                         "single_pass_kernel_tflops": fl4 / (ms4["single_pass"] * 1e-3) / 1e12,
-                         "single_pass_kernel_ms": ms4["single_pass"],
-                         "roofline": {"bound": "tensor", "achieved": fl4 / (ms4["default"] * 1e-3) / 1e12,
+        "prefill_4to1": {"workload": w4.name + " through gda_attn_fwd_2pass (two-pass kernels, caller workspace)",
+                         "value": fl4 / (ms4["two_pass"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                         "ms_per_step": ms4["two_pass"], "steps": 20, "gpu_launches": 2 * 20,
+                         "gda_attn_fwd_tflops": fl4 / (ms4["single_pass"] * 1e-3) / 1e12,
+                         "gda_attn_fwd_ms": ms4["single_pass"],
+                         "gda_attn_fwd_kernel": "single pass, dv split over a CTA pair (no workspace)",
+                         "roofline": {"bound": "tensor", "achieved": fl4 / (ms4["two_pass"] * 1e-3) / 1e12,
                                       "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                                      "frac": fl4 / (ms4["default"] * 1e-3) / 1e12 / peaks["bf16_tflops"]}},
+                                      "frac": fl4 / (ms4["two_pass"] * 1e-3) / 1e12 / peaks["bf16_tflops"]}},
+        "prefill_3to1_L2048": {"workload": w2.name + " through gda_attn_fwd",
+                               "value": tf2, "unit": "TFLOP/s", "ms_per_step": ms2["default"], "steps": 200,
+                               "tflops_min_count": fl2_min / (ms2["default"] * 1e-3) / 1e12,
+                               "single_pass_kernel_ms": ms2["single_pass"],
+                               "single_pass_kernel_tflops": fl2 / (ms2["single_pass"] * 1e-3) / 1e12,
+                               "l2": f"{N_INPUT_SETS} rotating input sets",
+                               "roofline": {"bound": "tensor", "achieved": tf2, "peak": peaks["bf16_tflops"],
+                                            "unit": "TFLOP/s", "frac": tf2 / peaks["bf16_tflops"]}},
         "backward_bf16": {"workload": f"tensor-core gradients of q_sig, k_sig, q_noise, k_noise, v, lambda from bf16 "
                                       f"inputs at B={w.B}, L={w.L}, {w.h_s}+{w.h_n} heads, d={w.d}, dv={w.dv}, causal",
                           "value": bb_tflops, "unit": "TFLOP/s", "ms_per_step": bb_ms, "steps": bb_steps,
@@ -827,10 +887,10 @@ def main():
     from grouped_differential_attention_gb300 import workloads as W
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["gda", "reference"], default="gda")
-    ap.add_argument("--workload", default=W.GDA3_PREFILL_L2048.name,
+    ap.add_argument("--workload", default=W.GDA3_PREFILL_L32768.name,
                     choices=sorted(n for n, x in W.PREFILL_WORKLOADS.items() if x.dtype == "bf16"))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()

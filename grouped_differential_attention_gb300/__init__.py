@@ -19,7 +19,6 @@ v and the output [B, L, h_s, dv]; lambda [h_s] float32.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import threading
 
@@ -28,11 +27,11 @@ import torch
 __all__ = [
     "GDAError", "gda_attn_fwd", "gda_attn_fwd_f32", "gda_attn_decode",
     "gda_attn_decode_workspace_size", "gda_status_string", "gda_device_error",
-    "lambda_init_schedule", "library_path", "GDA_FLAG_NO_NORM", "GDA_FLAG_SINGLE_PASS",
+    "library_path", "GDA_FLAG_NO_NORM", "GDA_FLAG_SINGLE_PASS",
     "gda_attn_decode_noalloc",
     "gda_attn_bwd", "gda_attn_bwd_workspace_size", "gda_attn_fwd_2pass",
     "gda_attn_fwd_2pass_workspace_size", "gda_attn_bwd_bf16", "gda_attn_bwd_bf16_workspace_size",
-    "gda_attn_decode_paged_fp8",
+    "gda_attn_decode_paged_fp8", "gda_attn_fwd_chunk", "gda_attn_fwd_chunk_2pass",
 ]
 
 GDA_OK = 0
@@ -99,6 +98,9 @@ def _load():
             lib.gda_attn_decode_paged.restype = I
             lib.gda_attn_fwd_chunk.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, F, U, P]
             lib.gda_attn_fwd_chunk.restype = I
+            lib.gda_attn_fwd_chunk_2pass.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, I, F, U,
+                                                     P, Z, P]
+            lib.gda_attn_fwd_chunk_2pass.restype = I
             lib.gda_lambda_reparam.argtypes = [P, P, P, P, F, P, I, I, P]
             lib.gda_lambda_reparam.restype = I
             lib.gda_attn_decode_paged_fp8.argtypes = [P, P, P, P, P, P, P, P, P, P, P, F, P, I, I, I, I, I, I,
@@ -193,11 +195,15 @@ def gda_attn_fwd(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float, *,
 
 
 def gda_attn_fwd_chunk(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: float, *,
-                       causal: bool = True, eps: float = 1e-5, out=None, flags: int = 0):
+                       causal: bool = True, eps: float = 1e-5, out=None, flags: int = 0, workspace=None,
+                       two_pass: bool = False):
     """Chunked bf16 prefill: L query rows at key positions Lk - L .. Lk - 1.
 
     q_sig [B, L, h_s, d], q_noise [B, L, h_n, d]; k_sig [B, Lk, h_s, d],
     k_noise [B, Lk, h_n, d], v [B, Lk, h_s, dv]; returns out [B, L, h_s, dv].
+    ``two_pass`` calls gda_attn_fwd_chunk_2pass, whose statistics workspace
+    (uint8 CUDA tensor of gda_attn_fwd_2pass_workspace_size(B, L, h_s, h_n)
+    bytes) is ``workspace`` or allocated here.
     """
     dev = q_sig.device
     if dev.type != "cuda":
@@ -216,10 +222,17 @@ def gda_attn_fwd_chunk(q_sig, k_sig, q_noise, k_noise, v, lam, lambda_init: floa
     if out is None:
         out = torch.empty((B, L, hs, dv), dtype=bf, device=dev)
     _expect(out, "out", bf, (B, L, hs, dv), dev)
+    args = (_ptr(q_sig), _ptr(k_sig), _ptr(q_noise), _ptr(k_noise), _ptr(v), _ptr(lam), float(lambda_init),
+            _ptr(out), B, L, Lk, hs, hn, d, dv, int(bool(causal)), float(eps), int(flags))
     with torch.cuda.device(dev):
-        rc = _load().gda_attn_fwd_chunk(_ptr(q_sig), _ptr(k_sig), _ptr(q_noise), _ptr(k_noise), _ptr(v),
-                                        _ptr(lam), float(lambda_init), _ptr(out), B, L, Lk, hs, hn, d, dv,
-                                        int(bool(causal)), float(eps), int(flags), _stream(dev))
+        if two_pass:
+            need = gda_attn_fwd_2pass_workspace_size(B, L, hs, hn)
+            if workspace is None:
+                workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+            _expect(workspace, "workspace", torch.uint8, (workspace.numel(),), dev)
+            rc = _load().gda_attn_fwd_chunk_2pass(*args, _ptr(workspace), workspace.numel(), _stream(dev))
+        else:
+            rc = _load().gda_attn_fwd_chunk(*args, _stream(dev))
     _check(rc, "gda chunked prefill")
     return out
 
@@ -585,12 +598,3 @@ def gda_device_error(clear: bool = True) -> int:
         raise GDAError(rc, "gda_device_error")
     return rc
 
-
-def lambda_init_schedule(layer: int) -> float:
-    """lambda_init of 1-based layer ``layer``: 0.8 - 0.6 exp(-0.3 (layer - 1)).
-
-    The depth schedule of "Differential Attention in Large Language Models
-    ...", section "Learnable Lambda Re-parameterization" (0.2 in the first
-    layer, rising toward 0.8).  A host-side constant for a layer's call.
-    """
-    return 0.8 - 0.6 * math.exp(-0.3 * (layer - 1))

@@ -140,19 +140,7 @@ int gda_attn_fwd_ex(const void *q_sig, const void *k_sig, const void *q_noise, c
     if (st != GDA_OK) return st;
     PrefillArgs a{q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L, h_s, h_n,
                   d, dv, causal, eps, flags & GDA_FLAG_NO_NORM, err};
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (dv == 256 && !(flags & GDA_FLAG_SINGLE_PASS)) {
-        // one accumulator per CTA beats the CTA pair of the single-pass kernel here
-        void *lse = nullptr;
-        if (cudaMallocAsync(&lse, prefill_2pass_workspace_bytes(B, L, h_s, h_n), s) == cudaSuccess) {
-            const int st2 = launch_prefill_2pass(a, lse, s);
-            const cudaError_t fe = cudaFreeAsync(lse, s);
-            if (st2 != GDA_OK) return st2;
-            return fe == cudaSuccess ? GDA_OK : record_cuda_error(fe);
-        }
-        cudaGetLastError();   // no statistics buffer: the single-pass kernel needs none
-    }
-    return launch_prefill_tc(a, s);
+    return launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gda_attn_fwd_chunk(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,
@@ -173,19 +161,30 @@ int gda_attn_fwd_chunk(const void *q_sig, const void *k_sig, const void *q_noise
     PrefillArgs a{q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L, h_s, h_n,
                   d, dv, causal, eps, flags & GDA_FLAG_NO_NORM, err};
     a.Lk = Lk;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (dv == 256 && !(flags & GDA_FLAG_SINGLE_PASS)) {
-        // as gda_attn_fwd: the two-pass kernels, statistics from the stream-ordered allocator
-        void *lse = nullptr;
-        if (cudaMallocAsync(&lse, prefill_2pass_workspace_bytes(B, L, h_s, h_n), s) == cudaSuccess) {
-            const int st2 = launch_prefill_2pass(a, lse, s);
-            const cudaError_t fe = cudaFreeAsync(lse, s);
-            if (st2 != GDA_OK) return st2;
-            return fe == cudaSuccess ? GDA_OK : record_cuda_error(fe);
-        }
-        cudaGetLastError();   // no statistics buffer: the single-pass kernel needs none
-    }
-    return launch_prefill_tc(a, s);
+    return launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gda_attn_fwd_chunk_2pass(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,
+                             const void *v, const float *lambda, float lambda_init, void *out, int B, int L,
+                             int Lk, int h_s, int h_n, int d, int dv, int causal, float eps, unsigned flags,
+                             void *workspace, size_t workspace_bytes, gda_stream_t stream) {
+    int st = check_prefill_common(q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L,
+                                  h_s, h_n, d, dv, causal, eps, flags);
+    if (st != GDA_OK) return st;
+    if (Lk < 1 || (causal && Lk < L)) return GDA_ERR_INVALID_ARG;
+    if (static_cast<double>(B) * Lk * (h_s > h_n ? h_s : h_n) * (d > dv ? d : dv) > 9.0e15)
+        return GDA_ERR_INVALID_ARG;
+    if (!(d == 64 || d == 128) || !(dv == 128 || dv == 256)) return GDA_ERR_UNSUPPORTED;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < prefill_2pass_workspace_bytes(B, L, h_s, h_n))
+        return GDA_ERR_WORKSPACE;
+    unsigned *err = nullptr;
+    st = current_device(&err);
+    if (st != GDA_OK) return st;
+    PrefillArgs a{q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L, h_s, h_n,
+                  d, dv, causal, eps, flags, err};
+    a.Lk = Lk;
+    return launch_prefill_2pass(a, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gda_attn_fwd(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,

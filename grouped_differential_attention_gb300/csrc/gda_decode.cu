@@ -727,15 +727,17 @@ static __device__ __align__(256) unsigned char g_decode_scratch[GDA_DECODE_SCRAT
 namespace gda {
 namespace {
 constexpr int kScratchDevices = 64;
+// Per device: the scratch array's device address once a lookup succeeded.
+// A failed lookup (for instance one made during a stream capture) is not
+// remembered, so a later call on that device tries again.
 struct ScratchState {
-    std::once_flag once;
+    std::mutex mu;
     void *ptr = nullptr;
-    int status = GDA_ERR_CUDA;
 };
 ScratchState g_scratch[kScratchDevices];
 
-// Device address of the scratch array on the current device (set up on the
-// first call for that device, with the device current).
+// Device address of the scratch array on the current device (looked up with
+// the device current, on the first successful call for that device).
 int scratch_address(void **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kScratchDevices) {
@@ -743,18 +745,15 @@ int scratch_address(void **out) {
         return GDA_ERR_CUDA;
     }
     ScratchState &s = g_scratch[dev];
-    std::call_once(s.once, [&s]() {
+    std::lock_guard<std::mutex> lock(s.mu);
+    if (s.ptr == nullptr) {
         void *ptr = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
-        if (e != cudaSuccess) {
-            s.status = record_cuda_error(e);
-            return;
-        }
+        if (e != cudaSuccess) return record_cuda_error(e);
         s.ptr = ptr;
-        s.status = GDA_OK;
-    });
+    }
     *out = s.ptr;
-    return s.status;
+    return GDA_OK;
 }
 }  // namespace
 

@@ -98,6 +98,16 @@ def make_prefill_inputs(w: PrefillWorkload, **overrides):
     ``overrides`` may replace B, L, h_s, h_n, d, dv, seed, dtype (small parity
     cases reuse a workload's recipe at other sizes).
     """
+    return make_prefill_inputs_and_boosted(w, **overrides)[0]
+
+
+def make_prefill_inputs_and_boosted(w: PrefillWorkload, **overrides):
+    """``make_prefill_inputs`` plus the boosted key positions of each sequence.
+
+    Returns ((q1, k1, q2, k2, v, lam), positions): positions[b] is the sorted
+    list of key positions of sequence b whose K1 and K2 rows were scaled (an
+    empty list for every b when the workload boosts none).
+    """
     p = dataclasses.replace(w, **overrides) if overrides else w
     g = torch.Generator().manual_seed(p.seed)
     q1 = torch.randn(p.B, p.L, p.h_s, p.d, generator=g)
@@ -107,6 +117,7 @@ def make_prefill_inputs(w: PrefillWorkload, **overrides):
     v = torch.randn(p.B, p.L, p.h_s, p.dv, generator=g)
     lo, hi = p.lam_range
     lam = torch.empty(p.h_s).uniform_(lo, hi, generator=g)
+    positions = [[] for _ in range(p.B)]
     if p.key_boost is not None:
         frac, factor = p.key_boost
         n = int(math.floor(frac * p.L))
@@ -114,8 +125,9 @@ def make_prefill_inputs(w: PrefillWorkload, **overrides):
             idx = torch.randperm(p.L, generator=g)[:n]
             k1[b, idx] *= factor
             k2[b, idx] *= factor
+            positions[b] = sorted(int(i) for i in idx)
     dt = _io_dtype(p.dtype)
-    return (q1.to(dt), k1.to(dt), q2.to(dt), k2.to(dt), v.to(dt), lam.to(torch.float32))
+    return (q1.to(dt), k1.to(dt), q2.to(dt), k2.to(dt), v.to(dt), lam.to(torch.float32)), positions
 
 
 def make_backward_inputs(w: PrefillWorkload, **overrides):

@@ -71,7 +71,7 @@ typedef enum {
 
 /* Flags for the *_ex entry points. */
 #define GDA_FLAG_NO_NORM 0x1u    /* return o_h (pre-norm, float32 difference) instead of y_h */
-#define GDA_FLAG_SINGLE_PASS 0x2u /* gda_attn_fwd_ex, gda_attn_fwd_chunk: keep the single-pass kernel at dv = 256 */
+#define GDA_FLAG_SINGLE_PASS 0x2u /* gda_attn_fwd_ex, gda_attn_fwd_chunk: run the per-signal-head single-pass kernel */
 
 /*
  * Prefill / full-sequence forward, bf16 I/O, float32 accumulation.
@@ -80,14 +80,11 @@ typedef enum {
  *   Supported: d in {64, 128}; dv in {128, 256}; B, L >= 1; h_s % h_n == 0;
  *   every pointer 16-byte aligned; device sm_103 (GB300).  causal in {0, 1}.
  *   Output is rounded once to bf16 (round to nearest even).
- * Computed by hand-written tcgen05/TMA kernels.  dv = 128: one pass with two
- * running softmax states per row, no workspace.  dv = 256: the two-pass
- * kernels of gda_attn_fwd_2pass (measured 1.2-1.4x faster there, one
- * accumulator per CTA instead of a CTA pair), with the pass-1 statistics
- * (4 B x B x (h_s + h_n) x L) taken from the stream-ordered allocator
- * (cudaMallocAsync / cudaFreeAsync on `stream`); if that allocation fails,
- * or with GDA_FLAG_SINGLE_PASS (gda_attn_fwd_ex), the single-pass kernel
- * runs instead (same result within the bf16 bound, no allocation).
+ * Computed by hand-written tcgen05/TMA kernels in one pass with two running
+ * softmax states per row; no workspace and no allocation (at dv = 256 the
+ * 256 accumulator columns are split over a CTA pair).  Callers that can
+ * provide a workspace get the faster two-pass kernels at dv = 256 from
+ * gda_attn_fwd_2pass.
  */
 int gda_attn_fwd(const void *q_sig, const void *k_sig, const void *q_noise,
                  const void *k_noise, const void *v, const float *lambda,
@@ -104,14 +101,28 @@ int gda_attn_fwd(const void *q_sig, const void *k_sig, const void *q_noise,
  * and Serving Considerations".)
  *   q_sig [B, L, h_s, d], q_noise [B, L, h_n, d], out [B, L, h_s, dv];
  *   k_sig [B, Lk, h_s, d], k_noise [B, Lk, h_n, d], v [B, Lk, h_s, dv].
- * Other arguments, flags (including GDA_FLAG_SINGLE_PASS), kernels (two-pass
- * at dv = 256), support and errors as gda_attn_fwd_ex;
- * GDA_ERR_INVALID_ARG also for Lk < 1 or (causal and Lk < L).
+ * Other arguments, flags, kernels (no workspace, no allocation), support and
+ * errors as gda_attn_fwd_ex; GDA_ERR_INVALID_ARG also for Lk < 1 or (causal
+ * and Lk < L).
  */
 int gda_attn_fwd_chunk(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,
                        const void *v, const float *lambda, float lambda_init, void *out, int B, int L,
                        int Lk, int h_s, int h_n, int d, int dv, int causal, float eps, unsigned flags,
                        gda_stream_t stream);
+
+/*
+ * Chunked prefill through the two-pass kernels of gda_attn_fwd_2pass (the
+ * faster choice at dv = 256).  Arguments as gda_attn_fwd_chunk plus a
+ * caller-owned device workspace of at least
+ * gda_attn_fwd_2pass_workspace_size(B, L, h_s, h_n) bytes (L = the chunk's
+ * query rows; 16-byte aligned), which receives the chunk rows' base-2
+ * log-sum-exp values.  Flags: GDA_FLAG_NO_NORM.  GDA_ERR_WORKSPACE if the
+ * workspace is null, misaligned or too small.
+ */
+int gda_attn_fwd_chunk_2pass(const void *q_sig, const void *k_sig, const void *q_noise, const void *k_noise,
+                             const void *v, const float *lambda, float lambda_init, void *out, int B, int L,
+                             int Lk, int h_s, int h_n, int d, int dv, int causal, float eps, unsigned flags,
+                             void *workspace, size_t workspace_bytes, gda_stream_t stream);
 
 /* gda_attn_fwd with flags (GDA_FLAG_NO_NORM, GDA_FLAG_SINGLE_PASS). */
 int gda_attn_fwd_ex(const void *q_sig, const void *k_sig, const void *q_noise,
@@ -335,7 +346,8 @@ int gda_attn_decode_paged_fp8(const void *q_sig, const void *q_noise, const void
  *   more than about 2200 such sequences do not fit).
  *   The first call on a device looks up the scratch array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   before any stream capture.  If the lookup fails the call returns
+ *   GDA_ERR_CUDA and the next call on that device looks it up again.
  *   Every call shares the one array and it keeps the last call's contents
  *   (the kernels write every value they later read, so nothing needs
  *   clearing).  Calls whose work overlaps on the GPU, on any streams, race

@@ -233,6 +233,28 @@ def test_chunked_prefill_rejects_bad_arguments(lib):
     assert call(dv=64) == UNSUPPORTED
 
 
+def test_chunked_two_pass_prefill_checks_arguments_and_workspace(lib):
+    # every call below fails validation before any device work
+    F, U, Z = ctypes.c_float, ctypes.c_uint, ctypes.c_size_t
+    P = [ctypes.c_void_p(A)] * 6
+    lib.gda_attn_fwd_chunk_2pass.argtypes = [ctypes.c_void_p] * 6 + [F, ctypes.c_void_p] + [ctypes.c_int] * 8 + [
+        F, U, ctypes.c_void_p, Z, ctypes.c_void_p]
+
+    def call(L=128, Lk=512, causal=1, hs=6, hn=2, d=64, dv=256, ws=A, ws_bytes=None, flags=0):
+        need = lib.gda_attn_fwd_2pass_workspace_size(2, L, hs, hn)
+        return lib.gda_attn_fwd_chunk_2pass(*P, F(0.8), ctypes.c_void_p(A), 2, L, Lk, hs, hn, d, dv, causal,
+                                            F(1e-5), U(flags), ctypes.c_void_p(ws) if ws else None,
+                                            need if ws_bytes is None else ws_bytes, None)
+    assert call(Lk=0) == INVALID
+    assert call(L=128, Lk=100) == INVALID
+    assert call(hs=6, hn=4) == INVALID
+    assert call(d=96) == UNSUPPORTED
+    assert call(flags=0x2) == INVALID                 # the single-pass flag does not apply here
+    assert call(ws=None) == WORKSPACE
+    assert call(ws=A + 8) == WORKSPACE
+    assert call(ws_bytes=lib.gda_attn_fwd_2pass_workspace_size(2, 128, 6, 2) - 4) == WORKSPACE
+
+
 def test_backward_workspace_size(lib):
     assert lib.gda_attn_bwd_workspace_size(0, 128, 6, 64, 128) == 0
     assert lib.gda_attn_bwd_workspace_size(2, 128, 6, 64, -1) == 0

@@ -62,19 +62,20 @@ def test_prefill_in_chunks_equals_whole_prefill():
     assert_bf16_close(torch.cat(parts, dim=1).cpu(), whole.cpu().double().numpy(), "chunks vs whole")
 
 
-@pytest.mark.parametrize("flags", [0, gda.GDA_FLAG_SINGLE_PASS], ids=["two_pass", "single_pass"])
+@pytest.mark.parametrize("two_pass", [True, False], ids=["two_pass", "single_pass"])
 @pytest.mark.parametrize("shape", [  # B, L, Lk, h_s, h_n, d, dv, causal
     (1, 100, 700, 4, 1, 64, 256, True),
     (1, 130, 500, 4, 2, 128, 256, False),
     (2, 1, 257, 4, 2, 128, 256, True),
+    (2, 77, 300, 6, 2, 64, 128, True),
 ])
-def test_chunked_prefill_dv256_both_kernels(oracle_mod, shape, flags):
-    """At dv = 256 the chunk runs the two-pass kernels unless
-    GDA_FLAG_SINGLE_PASS keeps the single-pass CTA pair; both match the oracle."""
+def test_chunked_prefill_both_kernels(oracle_mod, shape, two_pass):
+    """gda_attn_fwd_chunk_2pass (two-pass kernels, caller workspace) and
+    gda_attn_fwd_chunk (single pass, no workspace) both match the oracle."""
     B, L, Lk, hs, hn, d, dv, causal = shape
     q1, k1, q2, k2, v, lam = chunk_case(B, L, Lk, hs, hn, d, dv, seed=L * 5 + Lk)
     chunk = (q1[:, Lk - L:], k1, q2[:, Lk - L:], k2, v, lam)
-    got = gda.gda_attn_fwd_chunk(*(t.contiguous().cuda() for t in chunk), 0.8, causal=causal, flags=flags)
+    got = gda.gda_attn_fwd_chunk(*(t.contiguous().cuda() for t in chunk), 0.8, causal=causal, two_pass=two_pass)
     torch.cuda.synchronize()
     ref = oracle_mod.prefill_rows(q1, k1, q2, k2, v, lam, 0.8, list(range(Lk - L, Lk)), causal=causal)
     assert_bf16_close(got.cpu(), ref, str(shape))

@@ -285,17 +285,14 @@ def _golden_lambda_init():
 
 
 def test_lambda_init_schedule_matches_page(oracle_mod):
-    import grouped_differential_attention_gb300 as gda
     for layer, value in _golden_lambda_init():
         if layer == "inf":
             assert abs(oracle_mod.lambda_init_schedule(10_000) - value) < 1e-12
-            assert abs(gda.lambda_init_schedule(10_000) - value) < 1e-12
         else:
             assert abs(oracle_mod.lambda_init_schedule(int(layer)) - value) < 1e-15
-            assert abs(gda.lambda_init_schedule(int(layer)) - value) < 1e-15
     # the layer-8 constant used by the 3:1 prefill workload
     assert abs(oracle_mod.lambda_init_schedule(8) - workloads.LAMBDA_INIT_LAYER8) < 1e-15
-    assert abs(gda.lambda_init_schedule(8) - 0.8 + 0.6 * math.exp(-2.1)) < 1e-15
+    assert abs(workloads.LAMBDA_INIT_LAYER8 - 0.8 + 0.6 * math.exp(-2.1)) < 1e-15
 
 
 def test_oracle_rejects_bad_shapes(oracle_mod):
@@ -507,3 +504,99 @@ def test_gradient_magnitudes_equal_gradients_when_terms_share_a_sign():
     mags = gda_grad_magnitudes(q1, k1, q2, k2, v, lam, 0.5, dy, causal=True, norm=False)
     np.testing.assert_allclose(mags[4].numpy(), grads[4].numpy(), rtol=0, atol=1e-12)
     np.testing.assert_allclose(mags[5].numpy(), -grads[5].numpy(), rtol=0, atol=1e-12)
+
+
+def _loop_grad_magnitudes(q1, k1, q2, k2, v, lam, lambda_init, dy, causal, norm, eps=1e-5):
+    """The gradient magnitudes written out term by term with scalar loops.
+
+    Independent of ``gda_grad_magnitudes``: both maps come from scalar
+    max-shifted softmax loops, the accumulators O1, O2 from loops over keys,
+    and the norm's input gradient from PyTorch autograd of the library
+    ``rms_norm`` ("Headwise Normalization").  Every term of every gradient
+    (the score gradients expanded down to the dot products over dv) enters as
+    the product of the absolute values of its factors.
+    """
+    q1, k1, q2, k2, v, dy = (t.double().numpy() for t in (q1, k1, q2, k2, v, dy))
+    lam = lam.double().numpy()
+    B, L, hs, d = q1.shape
+    hn = q2.shape[2]
+    r = hs // hn
+    dv = v.shape[3]
+    sc = 1.0 / math.sqrt(d)
+
+    def softmax_rows(q, k, hq, hk, b):
+        a = np.zeros((L, L))
+        for i in range(L):
+            keys = range(i + 1) if causal else range(L)
+            s = {j: sum(q[b, i, hq, c] * k[b, j, hk, c] for c in range(d)) * sc for j in keys}
+            m = max(s.values())
+            z = sum(math.exp(x - m) for x in s.values())
+            for j, x in s.items():
+                a[i, j] = math.exp(x - m) / z
+        return a
+
+    A1 = np.zeros((B, hs, L, L))
+    A2 = np.zeros((B, hs, L, L))
+    for b in range(B):
+        for h in range(hs):
+            A1[b, h] = softmax_rows(q1, k1, h, h, b)
+            A2[b, h] = softmax_rows(q2, k2, h // r, h // r, b)
+    O1 = np.zeros((B, L, hs, dv))
+    O2 = np.zeros((B, L, hs, dv))
+    for b in range(B):
+        for h in range(hs):
+            for i in range(L):
+                for j in range(L):
+                    O1[b, i, h] += A1[b, h, i, j] * v[b, j, h]
+                    O2[b, i, h] += A2[b, h, i, j] * v[b, j, h]
+    o = torch.tensor(O1 - lam[None, None, :, None] * O2, requires_grad=True)
+    if norm:
+        y = (1.0 - lambda_init) * F.rms_norm(o, (dv,), eps=eps)
+        (do,) = torch.autograd.grad(y, o, grad_outputs=torch.tensor(dy))
+        do = do.numpy()
+    else:
+        do = dy
+    m = [np.zeros_like(q1), np.zeros_like(k1), np.zeros_like(q2), np.zeros_like(k2),
+         np.zeros_like(v), np.zeros(hs)]
+    for b in range(B):
+        for h in range(hs):
+            g = h // r
+            for i in range(L):
+                m[5][h] += abs(sum(do[b, i, h, e] * O2[b, i, h, e] for e in range(dv)))
+                for j in range(L):
+                    a1, a2 = A1[b, h, i, j], abs(lam[h]) * A2[b, h, i, j]
+                    if a1 == 0.0 and a2 == 0.0:
+                        continue
+                    t1 = t2 = 0.0
+                    for e in range(dv):
+                        t1 += abs(do[b, i, h, e]) * abs(v[b, j, h, e]) + abs(do[b, i, h, e]) * abs(O1[b, i, h, e])
+                        t2 += abs(do[b, i, h, e]) * abs(v[b, j, h, e]) + abs(do[b, i, h, e]) * abs(O2[b, i, h, e])
+                        m[4][b, j, h, e] += (a1 + a2) * abs(do[b, i, h, e])
+                    for c in range(d):
+                        m[0][b, i, h, c] += a1 * t1 * abs(k1[b, j, h, c]) * sc
+                        m[1][b, j, h, c] += a1 * t1 * abs(q1[b, i, h, c]) * sc
+                        m[2][b, i, g, c] += a2 * t2 * abs(k2[b, j, g, c]) * sc
+                        m[3][b, j, g, c] += a2 * t2 * abs(q2[b, i, g, c]) * sc
+    return m
+
+
+@pytest.mark.parametrize("r,hn,causal,norm", [(2, 1, True, True), (3, 1, False, True),
+                                              (2, 2, False, False), (3, 2, True, False)])
+def test_gradient_magnitudes_equal_the_term_by_term_sums(r, hn, causal, norm):
+    """Pins gda_grad_magnitudes from above and below: each of its six outputs
+    equals the same sums of absolute terms evaluated by scalar loops (a
+    wrong factor, such as a dropped 1/sqrt(d) or terms scaled by a constant,
+    fails here; the triangle-inequality pin only bounds them from below)."""
+    from oracle.ref_torch_grad import gda_grad_magnitudes
+    g = torch.Generator().manual_seed(90 + 10 * r + hn)
+    B, L, d, dv = 1, 6, 4, 3
+    hs = r * hn
+    q1, k1 = (torch.randn(B, L, hs, d, generator=g, dtype=torch.float64) for _ in range(2))
+    q2, k2 = (torch.randn(B, L, hn, d, generator=g, dtype=torch.float64) for _ in range(2))
+    v = torch.randn(B, L, hs, dv, generator=g, dtype=torch.float64)
+    lam = torch.rand(hs, generator=g, dtype=torch.float64) * 3.0 - 1.0   # includes negative lambda
+    dy = torch.randn(B, L, hs, dv, generator=g, dtype=torch.float64)
+    got = gda_grad_magnitudes(q1, k1, q2, k2, v, lam, 0.6, dy, causal=causal, norm=norm)
+    want = _loop_grad_magnitudes(q1, k1, q2, k2, v, lam, 0.6, dy, causal, norm)
+    for name, a, b in zip(("dq1", "dk1", "dq2", "dk2", "dv", "dlambda"), got, want):
+        np.testing.assert_allclose(a.numpy(), b, rtol=1e-12, atol=1e-13, err_msg=name)
