@@ -140,6 +140,8 @@ int gda_attn_fwd_ex(const void *q_sig, const void *k_sig, const void *q_noise, c
     if (st != GDA_OK) return st;
     PrefillArgs a{q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L, h_s, h_n,
                   d, dv, causal, eps, flags & GDA_FLAG_NO_NORM, err};
+    if (!(flags & GDA_FLAG_SINGLE_PASS) && prefill_group_supported(a))
+        return launch_prefill_group(a, reinterpret_cast<cudaStream_t>(stream));
     return launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -161,6 +163,8 @@ int gda_attn_fwd_chunk(const void *q_sig, const void *k_sig, const void *q_noise
     PrefillArgs a{q_sig, k_sig, q_noise, k_noise, v, lambda, lambda_init, out, B, L, h_s, h_n,
                   d, dv, causal, eps, flags & GDA_FLAG_NO_NORM, err};
     a.Lk = Lk;
+    if (!(flags & GDA_FLAG_SINGLE_PASS) && prefill_group_supported(a))
+        return launch_prefill_group(a, reinterpret_cast<cudaStream_t>(stream));
     return launch_prefill_tc(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

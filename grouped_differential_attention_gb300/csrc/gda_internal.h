@@ -75,6 +75,9 @@ int device_state(unsigned **err_word);
 // Each launcher validates nothing (the ABI layer did) and returns a
 // gda_status value.
 int launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
+// The grouped kernel (noise map once per noise head and query tile): d = 64, dv = 128.
+bool prefill_group_supported(const PrefillArgs &a);
+int launch_prefill_group(const PrefillArgs &a, cudaStream_t stream);
 int launch_prefill_f32(const PrefillArgs &a, cudaStream_t stream);
 int launch_decode(const DecodeArgs &a, cudaStream_t stream);
 int launch_prefill_2pass(const PrefillArgs &a, void *workspace, cudaStream_t stream);

@@ -28,6 +28,7 @@ def main(argv=None):
     ap.add_argument("kind", choices=["prefill", "prefill2pass", "decode", "decode_fp8", "backward", "backward_bf16"])
     ap.add_argument("workload", nargs="?", default=None)
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--flags", type=int, default=0, help="gda_attn_fwd_ex flags for the prefill kind")
     args = ap.parse_args(argv)
     dev = torch.device("cuda:0")
     if args.kind == "prefill":
@@ -37,7 +38,7 @@ def main(argv=None):
         out = torch.empty((w.B, w.L, w.h_s, w.dv), dtype=inp[0].dtype, device=dev)
 
         def launch():
-            fn(*inp, w.lambda_init, causal=w.causal, eps=w.eps, out=out)
+            fn(*inp, w.lambda_init, causal=w.causal, eps=w.eps, out=out, flags=args.flags)
     elif args.kind == "prefill2pass":
         w = W.PREFILL_WORKLOADS[args.workload or W.GDA3_PREFILL_L2048.name]
         inp = [t.to(dev) for t in W.make_prefill_inputs(w)]
@@ -87,6 +88,7 @@ def main(argv=None):
         def launch():
             gda.gda_attn_decode(*inp, w.lambda_init, eps=w.eps, out=out, workspace=ws)
 
+    launch()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()

@@ -55,6 +55,10 @@ SMALL_BF16 = [  # B, L, h_s, h_n, d, dv, causal
     (1, 131, 8, 2, 128, 128, False),
     (2, 64, 2, 1, 128, 256, False),
     (1, 390, 4, 2, 128, 128, True),
+    (1, 200, 8, 2, 64, 128, True),       # groups of 4: two items of 2 signal heads per noise head
+    (2, 150, 6, 1, 64, 128, False),      # groups of 6: two items of 3
+    (1, 333, 4, 2, 64, 128, True),       # groups of 2
+    (3, 70, 5, 1, 64, 128, True),        # groups of 5: items of one signal head
 ]
 
 
