@@ -11,7 +11,7 @@
 //
 // Work item = (128-row query tile, batch b, noise head g, S signal heads
 // h0 .. h0+S-1 of g's group); S <= 3 divides the group size r.  Each item
-// runs two sweeps over its visible keys (64-key tiles), both in one CTA:
+// runs two sweeps over its visible keys (128-key tiles), both in one CTA:
 //   phase A  every map's row statistics: for the noise map of g and for each
 //            of the S signal maps, a running (max, sum) in base-2 units,
 //            combined into lse = max + log2(sum).  The noise map is one map
@@ -24,24 +24,31 @@
 //            head's float32 accumulator.  No online rescaling.
 // Both maps are normalised before the subtraction (the statistics are exact
 // by the end of phase A), so the accumulator holds o_h directly and the
-// epilogue only applies the headwise norm.  No statistics leave the SM: no
-// workspace.
+// epilogue only applies the headwise norm.  Forming P_h in float32 before its
+// one rounding keeps the rounding error relative to the difference map, not
+// to its two terms.  No statistics leave the SM: no workspace.
+//
+// Throughput facts this layout follows (tcgen05.mma with M = 128, K = 64,
+// measured on GB300): an N = 64 logit product takes as long as an N = 128
+// one (about 367 cycles), and a value product reading P from shared memory
+// (313 cycles at N = 128) is faster than one reading it from TMEM (439).
 //
 // TMEM (512 columns): accumulators O_h at [128 h, 128 h + 128) for h < S,
-// then NSLOT slots of 64 columns for logit tiles (two at S = 3).  A slot is
-// released as soon as the compute warps have loaded its tile into registers
-// (P goes to shared memory), so the next logit tile's MMA never waits for a
-// value product.
+// then NSLOT slots of 128 columns for 128-key logit tiles (one at S = 3).
+// A slot is released as soon as the compute warps have loaded its tile into
+// registers (P goes to shared memory).
 // Warp roles (persistent CTA, one per SM):
 //   warp 0      TMA producer: Q2 and the S Q1 tiles once per item, a ring of
-//               K tiles (one head each) and a ring of V tiles (one head each)
-//               in exactly the order the MMAs consume them;
-//   warp 1      TMEM allocator and MMA issuer: logit MMAs (SS, K-major) into
-//               the slot ring, value MMAs (SS: P from shared memory, V as an
-//               MN-major operand) NSLOT uses behind;
-//   warps 2-9   compute (thread = query row = TMEM lane; warps 2-5 take key
-//               columns 0-31 of each tile, warps 6-9 columns 32-63): running
-//               statistics, P, and the epilogue of the item.
+//               128-key K tiles (one head each) and a ring of 64-key V tiles
+//               (one head each) in exactly the order the MMAs consume them;
+//   warp 1      TMEM allocator and MMA issuer: logit MMAs (SS, K-major, N =
+//               128) into the slot ring, value MMAs (SS: P from shared
+//               memory, V as an MN-major operand) NSLOT uses behind;
+//   warps 2-17  compute (thread = query row = TMEM lane; warps 2-5 take keys
+//               0-31 of each 128-key tile, warps 6-9 keys 32-63, 10-13 keys
+//               64-95, 14-17 keys 96-127: four compute warps per SM
+//               sub-partition, so one warp's exponential latency hides behind
+//               the others): running statistics, P, and the item's epilogue.
 // Every mbarrier wait is bounded (1 s) and sets GDA_DEVERR_PREFILL_TIMEOUT.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -57,38 +64,72 @@
 namespace gda {
 namespace {
 
-constexpr int kGBN = 64;               // keys per tile
-constexpr int kGThreads = 320;         // 10 warps
-constexpr int kGComputeWarps = 8;
+constexpr int kGBN = 128;              // keys per logit tile
+constexpr int kPH = 64;                // keys per P half / V tile
+#ifndef GDA_GROUP_KEYS_PER_THREAD
+#define GDA_GROUP_KEYS_PER_THREAD 32
+#endif
+constexpr int kKQ = GDA_GROUP_KEYS_PER_THREAD;   // keys of a 128-key tile per compute thread
+constexpr int kNQ = kGBN / kKQ;                  // compute threads per query row
+constexpr int kGComputeWarps = 4 * kNQ;
+constexpr int kGThreads = 32 * (2 + kGComputeWarps);
+static_assert(kKQ == 32 || kKQ == 64, "a thread takes 32 or 64 keys of each tile");
 
 template <int S> struct GLayout {
-    static constexpr int NSLOT = (512 - 128 * S) / 64;   // logit slots of 64 TMEM columns
-    static constexpr int LAG = NSLOT;                    // value MMA of use u issued after logit MMA of u + LAG
-    static constexpr int KS = 6, VS = 4, NP = 2;         // K, V, P ring depths
+    // TMEM: four 128-column slots; slot h < S holds O_h.  Phase A (statistics)
+    // uses all four slots for logit tiles (the accumulators are free until the
+    // item's first value MMA), phase B the NB slots above the accumulators.
+    static constexpr int NB = 4 - S;                     // phase-B logit slots
+    static constexpr int LAG = NB + 1;                   // value MMA of use u issued after logit MMA of u + LAG
+    static constexpr int NR = 6;                         // ring of 16 KB K / V tiles
     static constexpr int Q_BYTES = kBM * 64 * 2;         // one head's 128 x 64 query tile
-    static constexpr int K_BYTES = kGBN * 64 * 2;        // one head's 64 x 64 key tile
-    static constexpr int V_BYTES = kGBN * 128 * 2;       // one head's 64 x 128 value tile
-    static constexpr int P_BYTES = kBM * kGBN * 2;       // one head's 128 x 64 bf16 P tile
+    static constexpr int R_BYTES = 16384;                // ring slot: a 128 x 64 K tile or a 64 x 128 V tile
+    static constexpr int PH_BYTES = kBM * kPH * 2;       // one 128 x 64 bf16 half of a P tile
     static constexpr int OFF_Q = 0;                      // Q2, then Q1 of heads h0 .. h0+S-1
-    static constexpr int OFF_K = OFF_Q + (S + 1) * Q_BYTES;
-    static constexpr int OFF_V = OFF_K + KS * K_BYTES;
-    static constexpr int OFF_P = OFF_V + VS * V_BYTES;
-    static constexpr int TILES = OFF_P + NP * P_BYTES;
-    static_assert(128 * S + 64 * NSLOT <= 512 && NSLOT >= 2, "TMEM budget");
+    static constexpr int OFF_R = OFF_Q + (S + 1) * Q_BYTES;
+    static constexpr int OFF_P = OFF_R + NR * R_BYTES;   // P tiles [buffer][half: keys 0-63, 64-127]
+    static constexpr int TILES = OFF_P + 4 * PH_BYTES;
+    static_assert(NB >= 1, "TMEM budget");
+    static_assert(kGBN * 64 * 2 == R_BYTES && kPH * 128 * 2 == R_BYTES, "ring slot size");
+};
+
+// Physical TMEM slot of phase-A use a of an item: the phase-B slots first (no
+// wait for the previous item's epilogue), then the accumulator slots.
+template <int S>
+__device__ __forceinline__ uint32_t slot_a(uint32_t a) {
+    const uint32_t k = a % 4;
+    return k < static_cast<uint32_t>(4 - S) ? S + k : k - (4 - S);
+}
+
+// Post-increment of counter number `slot` of four (kept in registers).
+__device__ __forceinline__ uint32_t bump(uint32_t (&cnt)[4], uint32_t slot) {
+    uint32_t k = 0;
+#pragma unroll
+    for (uint32_t q = 0; q < 4; ++q)
+        if (q == slot) {
+            k = cnt[q];
+            cnt[q] = k + 1;
+        }
+    return k;
+}
+
+// Per-item exchange between the warps that hold a row's key parts.  It
+// lives in the P buffers, which no MMA reads at the times it is used (after
+// the item's last value MMA, or before its first P tile is written).
+struct GExchange {
+    float xm[kNQ][4][kBM];     // [key part][map][row]: phase-A reference maximum
+    float xl[kNQ][4][kBM];     // [key part][map][row]: phase-A sum against it
+    float ss[kNQ][3][kBM];     // [column part][head][row]: epilogue sums of squares
 };
 
 struct GCtrl {
     uint64_t q_full, q_empty;
-    uint64_t k_full[8], k_empty[8];
-    uint64_t v_full[8], v_empty[8];
-    uint64_t s_full[6], s_free[6];
-    uint64_t p_full[4], p_empty[4];
+    uint64_t r_full[6], r_empty[6];      // K / V ring
+    uint64_t s_full[4], s_free[4];       // TMEM logit slots
+    uint64_t p_full[2][2], p_empty[2][2];   // [P buffer][half]
     uint64_t o_final, o_free, mma_idle;
     uint32_t tmem_base;
     int abort_flag;
-    float xm[2][4][kBM];       // [column half][map][row]: phase-A running max
-    float xl[2][4][kBM];       // [column half][map][row]: phase-A running sum
-    float ss[2][3][kBM];       // [column half][head][row]: epilogue sums of squares
 };
 
 template <int S>
@@ -131,10 +172,31 @@ __device__ __forceinline__ bool gitem_of(const GParams &p, int S, int rr, int G,
     return true;
 }
 
-// Per-warp arrival on a barrier that counts the 8 compute warps.
+// Per-warp arrival on a barrier that counts warps.
 __device__ __forceinline__ void warp_arrive(uint64_t *bar, uint32_t lane) {
     __syncwarp();
     if (lane == 0) mbar_arrive(bar);
+}
+
+// Bounded wait without the suspend-time hint: a wait whose phase has already
+// completed costs about a third as much as the hinted form, which matters on
+// the single MMA-issuing thread.
+__device__ __forceinline__ bool wait_fast(uint64_t *bar, uint32_t parity, unsigned *err, volatile int *abort) {
+    const uint32_t a = smem_u32(bar);
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    return mbar_wait(bar, parity, err, GDA_DEVERR_PREFILL_TIMEOUT, abort);
+}
+
+__device__ __forceinline__ bool warp_wait_fast(uint64_t *bar, uint32_t parity, unsigned *err, volatile int *abort) {
+    return __all_sync(0xffffffffu, wait_fast(bar, parity, err, abort));
 }
 
 template <int S>
@@ -143,12 +205,14 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                          const __grid_constant__ CUtensorMap tmQ2, const __grid_constant__ CUtensorMap tmK2,
                          const __grid_constant__ CUtensorMap tmV, const GParams p) {
     using LY = GLayout<S>;
-    constexpr int NSLOT = LY::NSLOT, LAG = LY::LAG, KS = LY::KS, VS = LY::VS, NP = LY::NP;
+    constexpr int NB = LY::NB, LAG = LY::LAG, NR = LY::NR;
     constexpr int M = S + 1;                 // maps per item: noise map (0), signal heads (1..S)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     GCtrl *ctl = reinterpret_cast<GCtrl *>(smem + LY::TILES);
+    GExchange *xch = reinterpret_cast<GExchange *>(smem + LY::OFF_P);
+    static_assert(sizeof(GExchange) <= 2 * LY::PH_BYTES, "exchange fits the P buffers");
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int cid = blockIdx.x;
@@ -157,22 +221,19 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
     if (threadIdx.x == 0) {
         mbar_init(&ctl->q_full, 1);
         mbar_init(&ctl->q_empty, 1);
-        for (int s = 0; s < KS; ++s) {
-            mbar_init(&ctl->k_full[s], 1);
-            mbar_init(&ctl->k_empty[s], 1);
+        for (int s = 0; s < NR; ++s) {
+            mbar_init(&ctl->r_full[s], 1);
+            mbar_init(&ctl->r_empty[s], 1);
         }
-        for (int s = 0; s < VS; ++s) {
-            mbar_init(&ctl->v_full[s], 1);
-            mbar_init(&ctl->v_empty[s], 1);
-        }
-        for (int s = 0; s < NSLOT; ++s) {
+        for (int s = 0; s < 4; ++s) {
             mbar_init(&ctl->s_full[s], 1);
             mbar_init(&ctl->s_free[s], kGComputeWarps);
         }
-        for (int s = 0; s < NP; ++s) {
-            mbar_init(&ctl->p_full[s], kGComputeWarps);
-            mbar_init(&ctl->p_empty[s], 1);
-        }
+        for (int s = 0; s < 2; ++s)
+            for (int hf = 0; hf < 2; ++hf) {
+                mbar_init(&ctl->p_full[s][hf], kGComputeWarps / 2);      // the warps writing the half
+                mbar_init(&ctl->p_empty[s][hf], 1);
+            }
         mbar_init(&ctl->o_final, 1);
         mbar_init(&ctl->o_free, kGComputeWarps);
         mbar_init(&ctl->mma_idle, 1);
@@ -187,7 +248,6 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    const uint32_t tSlot0 = 128 * S;          // first logit slot column
     volatile int *abort_flag = &ctl->abort_flag;
 
     if (warp == 0) {
@@ -198,7 +258,7 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             tma_prefetch_desc(&tmQ2);
             tma_prefetch_desc(&tmK2);
             tma_prefetch_desc(&tmV);
-            uint32_t kt = 0, vt = 0;
+            uint32_t ct = 0;
             int nq = 0;
             bool ok = true;
             GItem it;
@@ -211,114 +271,124 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                     tma_load_4d(smem + LY::OFF_Q + (1 + h) * LY::Q_BYTES, &tmQ1, &ctl->q_full, 0, it.h0 + h, it.q0,
                                 it.b);
                 ++nq;
-                // K tile of map m (0: noise head g, 1..S: signal head h0 + m - 1) at key tile j
+                // next ring slot (K and V tiles share one ring, filled in consumption order)
+                auto ring = [&](uint32_t bytes) -> uint8_t * {
+                    const int st = ct % NR;
+                    if (ct >= NR && !wait_bar(&ctl->r_empty[st], ((ct / NR) - 1) & 1, p.err, abort_flag))
+                        return nullptr;
+                    mbar_arrive_expect_tx(&ctl->r_full[st], bytes);
+                    return smem + LY::OFF_R + st * LY::R_BYTES;
+                };
+                // 128-key K tile of map m (0: noise head g, 1..S: signal head h0 + m - 1) at key tile j
                 auto load_k = [&](int m, int j) -> bool {
-                    const int st = kt % KS;
-                    if (kt >= KS && !wait_bar(&ctl->k_empty[st], ((kt / KS) - 1) & 1, p.err, abort_flag))
-                        return false;
-                    mbar_arrive_expect_tx(&ctl->k_full[st], LY::K_BYTES);
+                    uint8_t *dst = ring(LY::R_BYTES);
+                    if (!dst) return false;
+                    uint64_t *bar = &ctl->r_full[ct % NR];
                     if (m == 0)
-                        tma_load_4d(smem + LY::OFF_K + st * LY::K_BYTES, &tmK2, &ctl->k_full[st], 0, it.g, j * kGBN,
-                                    it.b);
+                        tma_load_4d(dst, &tmK2, bar, 0, it.g, j * kGBN, it.b);
                     else
-                        tma_load_4d(smem + LY::OFF_K + st * LY::K_BYTES, &tmK1, &ctl->k_full[st], 0, it.h0 + m - 1,
-                                    j * kGBN, it.b);
-                    ++kt;
+                        tma_load_4d(dst, &tmK1, bar, 0, it.h0 + m - 1, j * kGBN, it.b);
+                    ++ct;
                     return true;
                 };
-                auto load_v = [&](int h, int j) -> bool {
-                    const int st = vt % VS;
-                    if (vt >= VS && !wait_bar(&ctl->v_empty[st], ((vt / VS) - 1) & 1, p.err, abort_flag))
-                        return false;
-                    mbar_arrive_expect_tx(&ctl->v_full[st], LY::V_BYTES);
-                    uint8_t *dst = smem + LY::OFF_V + st * LY::V_BYTES;
-                    tma_load_4d(dst, &tmV, &ctl->v_full[st], 0, it.h0 + h, j * kGBN, it.b);
-                    tma_load_4d(dst + kGBN * 128, &tmV, &ctl->v_full[st], 64, it.h0 + h, j * kGBN, it.b);
-                    ++vt;
+                // 64-key V tile of signal head h0 + h, keys j * 128 + half * 64 ..
+                auto load_v = [&](int h, int j, int half) -> bool {
+                    uint8_t *dst = ring(LY::R_BYTES);
+                    if (!dst) return false;
+                    uint64_t *bar = &ctl->r_full[ct % NR];
+                    const int key0 = j * kGBN + half * kPH;
+                    tma_load_4d(dst, &tmV, bar, 0, it.h0 + h, key0, it.b);
+                    tma_load_4d(dst + kPH * 128, &tmV, bar, 64, it.h0 + h, key0, it.b);
+                    ++ct;
                     return true;
                 };
                 // phase A: every map's K tiles, key tile by key tile
                 for (int j = 0; ok && j < it.nkv; ++j)
                     for (int m = 0; ok && m < M; ++m) ok = load_k(m, j);
-                // phase B: the same K tiles again, with each P-use's V tile LAG uses later
+                // phase B: the same K tiles again, with each P-use's two V tiles LAG uses later
                 const int nB = it.nkv * M;
                 for (int i = 0; ok && i < nB; ++i) {
                     ok = load_k(i % M, i / M);
-                    if (ok && i >= LAG && (i - LAG) % M != 0) ok = load_v((i - LAG) % M - 1, (i - LAG) / M);
+                    if (ok && i >= LAG && (i - LAG) % M != 0) {
+                        const int v = i - LAG;
+                        ok = load_v(v % M - 1, v / M, 0) && load_v(v % M - 1, v / M, 1);
+                    }
                 }
                 for (int v = (nB > LAG ? nB - LAG : 0); ok && v < nB; ++v)
-                    if (v % M != 0) ok = load_v(v % M - 1, v / M);
+                    if (v % M != 0) ok = load_v(v % M - 1, v / M, 0) && load_v(v % M - 1, v / M, 1);
             }
             // our own copies must land before the CTA may exit
             if (nq > 0) drain_wait(&ctl->q_full, (nq - 1) & 1, p.err);
-            for (uint32_t j = (kt > KS ? kt - KS : 0); j < kt; ++j)
-                drain_wait(&ctl->k_full[j % KS], (j / KS) & 1, p.err);
-            for (uint32_t j = (vt > VS ? vt - VS : 0); j < vt; ++j)
-                drain_wait(&ctl->v_full[j % VS], (j / VS) & 1, p.err);
+            for (uint32_t j = (ct > NR ? ct - NR : 0); j < ct; ++j)
+                drain_wait(&ctl->r_full[j % NR], (j / NR) & 1, p.err);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ================================================= MMA issuer
         if (elect_one()) {
             const uint32_t qa0 = smem_u32(smem + LY::OFF_Q);
-            const uint32_t ka0 = smem_u32(smem + LY::OFF_K);
-            const uint32_t va0 = smem_u32(smem + LY::OFF_V);
+            const uint32_t ra0 = smem_u32(smem + LY::OFF_R);
             const uint32_t pa0 = smem_u32(smem + LY::OFF_P);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, 128, 1);
-            uint32_t u = 0, kt = 0, vt = 0, pk = 0;
+            uint32_t cnt[4] = {0, 0, 0, 0};    // uses of each TMEM slot so far
+            uint32_t ct = 0, pk = 0;
             bool ok = true;
             GItem it;
             int nitem = 0;
-            // logit MMA of use u, map m, into slot u % NSLOT
-            auto qk = [&](int m) -> bool {
-                const uint32_t slot = u % NSLOT;
-                if (u >= NSLOT && !wait_bar(&ctl->s_free[slot], ((u / NSLOT) - 1) & 1, p.err, abort_flag))
-                    return false;
-                const uint32_t st = kt % KS;
-                if (!wait_bar(&ctl->k_full[st], (kt / KS) & 1, p.err, abort_flag)) return false;
+            bool o_ready = true;
+            // the accumulator slots are free once the previous item's epilogue has read them
+            auto need_o = [&]() -> bool {
+                if (o_ready) return true;
+                o_ready = true;
+                return nitem == 0 || wait_fast(&ctl->o_free, (nitem - 1) & 1, p.err, abort_flag);
+            };
+            // logit MMA of map m into TMEM slot `slot`
+            auto qk = [&](int m, uint32_t slot) -> bool {
+                const uint32_t k = bump(cnt, slot);
+                if (slot < static_cast<uint32_t>(S) && !need_o()) return false;
+                if (k >= 1 && !wait_fast(&ctl->s_free[slot], (k - 1) & 1, p.err, abort_flag)) return false;
+                const uint32_t st = ct % NR;
+                if (!wait_fast(&ctl->r_full[st], (ct / NR) & 1, p.err, abort_flag)) return false;
                 tc_fence_after();
-                issue_qk<64, kGBN>(tmem + tSlot0 + slot * kGBN, qa0 + m * LY::Q_BYTES, ka0 + st * LY::K_BYTES);
+                issue_qk<64, kGBN>(tmem + slot * 128, qa0 + m * LY::Q_BYTES, ra0 + st * LY::R_BYTES);
                 mma_commit(&ctl->s_full[slot]);
-                mma_commit(&ctl->k_empty[st]);
-                ++u;
-                ++kt;
+                mma_commit(&ctl->r_empty[st]);
+                ++ct;
                 return true;
             };
-            bool first_pv = true;
-            // value MMA of P-use v (phase-B index) of the current item: O_h += P_h V_h
+            // value MMAs of P-use v (phase-B index) of the current item: O_h += P_h V_h, one
+            // MMA group per 64-key half
             auto pv = [&](int v) -> bool {
                 const int h = v % (S + 1) - 1, j = v / (S + 1);
-                const uint32_t buf = pk % NP;
-                if (!wait_bar(&ctl->p_full[buf], (pk / NP) & 1, p.err, abort_flag)) return false;
-                const uint32_t st = vt % VS;
-                if (!wait_bar(&ctl->v_full[st], (vt / VS) & 1, p.err, abort_flag)) return false;
-                if (first_pv) {
-                    // the accumulators are free once the previous item's epilogue has read them
-                    if (nitem > 0 && !wait_bar(&ctl->o_free, (nitem - 1) & 1, p.err, abort_flag)) return false;
-                    first_pv = false;
-                }
-                tc_fence_after();
-                const uint32_t pa = pa0 + buf * LY::P_BYTES, va = va0 + st * LY::V_BYTES;
+                const uint32_t pb = pk & 1;
+                if (!need_o()) return false;
+                for (int half = 0; half < 2; ++half) {
+                    if (!wait_fast(&ctl->p_full[pb][half], (pk >> 1) & 1, p.err, abort_flag)) return false;
+                    const uint32_t st = ct % NR;
+                    if (!wait_fast(&ctl->r_full[st], (ct / NR) & 1, p.err, abort_flag)) return false;
+                    tc_fence_after();
+                    const uint32_t pa = pa0 + (pb * 2 + half) * LY::PH_BYTES, va = ra0 + st * LY::R_BYTES;
 #pragma unroll
-                for (int k = 0; k < kGBN / 16; ++k) {
-                    const uint64_t a = smem_desc_sw128(pa + k * 32, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(va + k * 2048, kGBN * 128, 1024);
-                    mma_ss(tmem + 128 * h, a, b, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < kPH / 16; ++k) {
+                        const uint64_t a = smem_desc_sw128(pa + k * 32, 16, 1024);
+                        const uint64_t b = smem_desc_sw128(va + k * 2048, kPH * 128, 1024);
+                        mma_ss(tmem + 128 * h, a, b, idesc_pv, (j > 0 || half > 0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&ctl->p_empty[pb][half]);
+                    mma_commit(&ctl->r_empty[st]);
+                    ++ct;
                 }
-                mma_commit(&ctl->p_empty[buf]);
-                mma_commit(&ctl->v_empty[st]);
                 ++pk;
-                ++vt;
                 return true;
             };
             for (int rr = 0; ok && gitem_of(p, S, rr, G, cid, it); ++rr) {
-                if (!wait_bar(&ctl->q_full, rr & 1, p.err, abort_flag)) break;
-                for (int j = 0; ok && j < it.nkv; ++j)
-                    for (int m = 0; ok && m < M; ++m) ok = qk(m);
+                if (!wait_fast(&ctl->q_full, rr & 1, p.err, abort_flag)) break;
+                o_ready = false;
+                const int nA = it.nkv * M;
+                for (int a = 0; ok && a < nA; ++a) ok = qk(a % M, slot_a<S>(a));
                 const int nB = it.nkv * M;
-                first_pv = true;
                 for (int i = 0; ok && i < nB; ++i) {
-                    ok = qk(i % M);
+                    ok = qk(i % M, S + i % NB);
                     if (ok && i == nB - 1) mma_commit(&ctl->q_empty);     // the item's last logit MMA
                     if (ok && i >= LAG && (i - LAG) % M != 0) ok = pv(i - LAG);
                 }
@@ -335,14 +405,19 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
         __syncwarp();
     } else {
         // ================================================= compute warps
-        const int half = (warp - 2) / 4;          // key columns [32 half, 32 half + 32) of every tile
+        const int kq = (warp - 2) / 4;            // keys [kKQ kq, kKQ kq + kKQ) of every 128-key tile
+        const int half = (kq * kKQ) / kPH;        // the P half (value MMA) those keys belong to
         const int quarter = warp % 4;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t pair_bar = 1 + quarter;    // the two warps that hold this row's halves
+        const uint32_t row_bar = 1 + quarter;     // the kNQ warps that hold this row's key parts
+        constexpr uint32_t kRowThreads = 32 * kNQ;
         const float sl2 = p.scale_log2;
-        uint8_t *pbase = smem + LY::OFF_P;
-        uint32_t u = 0, pk = 0;
+        // this thread's 16-byte chunks of its row in its P half (buffer 0)
+        uint8_t *pbuf0 = smem + LY::OFF_P + half * LY::PH_BYTES + row * 128;
+        const int chunk0 = ((kq * kKQ) % kPH) / 8;
+        uint32_t cnt[4] = {0, 0, 0, 0};    // uses of each TMEM slot so far
+        uint32_t pk = 0;
         GItem it;
         for (int rr = 0; gitem_of(p, S, rr, G, cid, it); ++rr) {
             const int qrow = it.q0 + row;
@@ -353,92 +428,121 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             for (int h = 0; h < S; ++h) lam[h] = p.lambda[it.h0 + h];
             bool ok = true;
 
-            // load this thread's 32 logits of use u into rr; release the slot
-            auto load_use = [&](uint32_t (&x)[32]) {
-                const uint32_t slot = u % NSLOT;
-                if (!warp_wait(&ctl->s_full[slot], (u / NSLOT) & 1, p.err, abort_flag)) ok = false;
+            // load this thread's kKQ logits from TMEM slot `slot` into x; release the slot
+            auto load_use = [&](uint32_t (&x)[kKQ], uint32_t slot) {
+                const uint32_t k = bump(cnt, slot);
+                if (!warp_wait_fast(&ctl->s_full[slot], k & 1, p.err, abort_flag)) ok = false;
                 tc_fence_after();
-                tmem_ld32(tmem + lane_off + tSlot0 + slot * kGBN + half * 32, x);
-                tmem_ld_wait_regs(x);
+#pragma unroll
+                for (int c = 0; c < kKQ / 32; ++c)
+                    tmem_ld32(tmem + lane_off + slot * 128 + kq * kKQ + c * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+                tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+                if constexpr (kKQ == 64) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
                 tc_fence_before();
                 warp_arrive(&ctl->s_free[slot], lane);
-                ++u;
             };
 
             // ---------------------------------------------- phase A: row statistics
+            // Each key quarter of the row keeps a reference mx (the exact maximum of its
+            // first tile with a visible key) and the sum ls of 2^(s c - mx); later tiles
+            // exponentiate against the reference directly, so no per-tile maximum sits on
+            // the critical path.  A tile whose sum exceeds 2^16 (or is not finite) is redone
+            // with its own maximum as the new reference and the running sum is rescaled.
             float mx[M], ls[M];
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 mx[m] = -INFINITY;
                 ls[m] = 0.f;
             }
+            auto tile_max = [&](const uint32_t (&x)[kKQ]) -> float {
+                float m4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) m4[i] = __uint_as_float(x[i]);
+#pragma unroll
+                for (int e = 4; e + 8 <= kKQ + 4; e += 8)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        m4[i] = max3f(m4[i], __uint_as_float(x[e + 2 * i]), __uint_as_float(x[e + 2 * i + 1]));
+                return max3f(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;
+            };
+            auto tile_sum = [&](const uint32_t (&x)[kKQ], float ref) -> float {
+                const float neg = -ref;
+                float sa = 0.f, sb = 0.f, sc = 0.f, sd = 0.f;
+#pragma unroll
+                for (int e = 0; e < kKQ; e += 4) {
+                    float x0 = __uint_as_float(x[e]), x1 = __uint_as_float(x[e + 1]);
+                    float x2 = __uint_as_float(x[e + 2]), x3 = __uint_as_float(x[e + 3]);
+                    ffma2(x0, x1, sl2, sl2, neg, neg);
+                    ffma2(x2, x3, sl2, sl2, neg, neg);
+                    fadd2(sa, sb, fast_exp2(x0), fast_exp2(x1));
+                    fadd2(sc, sd, fast_exp2(x2), fast_exp2(x3));
+                }
+                return (sa + sb) + (sc + sd);
+            };
             for (int j = 0; j < it.nkv; ++j) {
-                const int k0 = j * kGBN + half * 32;
-                const bool need_mask = k0 + 31 > last_key;
+                const int k0 = j * kGBN + kq * kKQ;
+                const bool need_mask = k0 + kKQ - 1 > last_key;
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
-                    uint32_t x[32];
-                    load_use(x);
+                    uint32_t x[kKQ];
+                    load_use(x, slot_a<S>(j * M + m));
                     if (need_mask) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
+                        for (int e = 0; e < kKQ; ++e)
                             if (k0 + e > last_key) x[e] = __float_as_uint(-INFINITY);
                     }
-                    float m4[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) m4[i] = __uint_as_float(x[i]);
-#pragma unroll
-                    for (int e = 4; e < 32; e += 8)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            m4[i] = max3f(m4[i], __uint_as_float(x[e + 2 * i]), __uint_as_float(x[e + 2 * i + 1]));
-                    const float tmax = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;
-                    const float mn = fmaxf(mx[m], tmax);
-                    if (mn != -INFINITY) {
-                        const float neg = -mn;
-                        float sa = 0.f, sb = 0.f, sc = 0.f, sd = 0.f;
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4) {
-                            float x0 = __uint_as_float(x[e]), x1 = __uint_as_float(x[e + 1]);
-                            float x2 = __uint_as_float(x[e + 2]), x3 = __uint_as_float(x[e + 3]);
-                            ffma2(x0, x1, sl2, sl2, neg, neg);
-                            ffma2(x2, x3, sl2, sl2, neg, neg);
-                            fadd2(sa, sb, fast_exp2(x0), fast_exp2(x1));
-                            fadd2(sc, sd, fast_exp2(x2), fast_exp2(x3));
+                    if (mx[m] == -INFINITY) mx[m] = tile_max(x);      // first tile with a visible key
+                    if (mx[m] != -INFINITY) {
+                        float ts = tile_sum(x, mx[m]);
+                        if (!(ts <= 65536.f)) {
+                            const float tm = tile_max(x);
+                            if (tm > mx[m]) {
+                                ls[m] *= fast_exp2(mx[m] - tm);
+                                mx[m] = tm;
+                            }
+                            ts = tile_sum(x, mx[m]);
                         }
-                        ls[m] = ls[m] * fast_exp2(mx[m] - mn) + ((sa + sb) + (sc + sd));
-                        mx[m] = mn;
+                        ls[m] += ts;
                     }
                 }
             }
-            // combine the two column halves of the row: lse = max + log2(sum), base 2
+            // combine the four key quarters of the row: lse = max + log2(sum), base 2.  The
+            // exchange lives in the P buffers: the previous item's value MMAs are complete
+            // (its epilogue waited for them) and this item writes no P before the second
+            // barrier below.
 #pragma unroll
             for (int m = 0; m < M; ++m) {
-                ctl->xm[half][m][row] = mx[m];
-                ctl->xl[half][m][row] = ls[m];
+                xch->xm[kq][m][row] = mx[m];
+                xch->xl[kq][m][row] = ls[m];
             }
-            named_bar_sync(pair_bar, 64);
+            named_bar_sync(row_bar, kRowThreads);
             float nlse[M];                        // -lse of each map (-inf for rows past L: every P is 0)
 #pragma unroll
             for (int m = 0; m < M; ++m) {
-                const float m0 = ctl->xm[0][m][row], m1 = ctl->xm[1][m][row];
-                const float mm = fmaxf(m0, m1);
+                float mm = -INFINITY;
+#pragma unroll
+                for (int q = 0; q < kNQ; ++q) mm = fmaxf(mm, xch->xm[q][m][row]);
                 float lsum = 0.f;
-                if (m0 != -INFINITY) lsum += ctl->xl[0][m][row] * fast_exp2(m0 - mm);
-                if (m1 != -INFINITY) lsum += ctl->xl[1][m][row] * fast_exp2(m1 - mm);
+#pragma unroll
+                for (int q = 0; q < kNQ; ++q) {
+                    const float mq = xch->xm[q][m][row];
+                    if (mq != -INFINITY) lsum += xch->xl[q][m][row] * fast_exp2(mq - mm);
+                }
                 nlse[m] = in ? -(mm + __log2f(lsum)) : -INFINITY;
             }
+            named_bar_sync(row_bar, kRowThreads); // all have read the exchange before P overwrites it
 
             // ---------------------------------------------- phase B: P_h = A1_h - lambda_h A2, P_h V_h
             for (int j = 0; j < it.nkv; ++j) {
-                const int k0 = j * kGBN + half * 32;
-                const bool need_mask = k0 + 31 > last_key;
-                float p2[32];
+                const int k0 = j * kGBN + kq * kKQ;
+                const bool need_mask = k0 + kKQ - 1 > last_key;
+                float p2[kKQ];
                 {
-                    uint32_t x[32];
-                    load_use(x);
+                    uint32_t x[kKQ];
+                    load_use(x, S + (j * M) % NB);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
+                    for (int e = 0; e < kKQ; e += 2) {
                         float y0 = __uint_as_float(x[e]), y1 = __uint_as_float(x[e + 1]);
                         ffma2(y0, y1, sl2, sl2, nlse[0], nlse[0]);
                         p2[e] = fast_exp2(y0);
@@ -447,81 +551,88 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                 }
 #pragma unroll
                 for (int h = 0; h < S; ++h) {
-                    uint32_t x[32];
-                    load_use(x);
                     const float nl = nlse[1 + h], nlam = -lam[h];
-                    uint32_t pw[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float y0 = __uint_as_float(x[e]), y1 = __uint_as_float(x[e + 1]);
-                        ffma2(y0, y1, sl2, sl2, nl, nl);
-                        float q0 = fmaf(nlam, p2[e], fast_exp2(y0));
-                        float q1 = fmaf(nlam, p2[e + 1], fast_exp2(y1));
-                        if (need_mask) {
-                            if (k0 + e > last_key) q0 = 0.f;
-                            if (k0 + e + 1 > last_key) q1 = 0.f;
-                        }
-                        pw[e / 2] = pack_bf16x2(q0, q1);
-                    }
-                    // P tile in the K-major 128-byte-swizzled layout of the value MMA's
-                    // A operand: 16-byte chunk c of row t at chunk c ^ (t % 8)
-                    const uint32_t buf = pk % NP;
-                    if (pk >= NP && !warp_wait(&ctl->p_empty[buf], ((pk / NP) - 1) & 1, p.err, abort_flag))
+                    uint32_t x[kKQ];
+                    load_use(x, S + (j * M + 1 + h) % NB);   // the slot is free again
+                    // this thread's keys of its P half, in the K-major 128-byte-swizzled layout
+                    // of the value MMA's A operand (16-byte chunk c of row t at chunk c ^ (t % 8));
+                    // written once the value MMA two P tiles back has read the buffer
+                    const uint32_t pb = pk & 1;
+                    if (pk >= 2 && !warp_wait_fast(&ctl->p_empty[pb][half], ((pk >> 1) - 1) & 1, p.err, abort_flag))
                         ok = false;
-                    uint8_t *prow = pbase + buf * LY::P_BYTES + row * 128;
+                    uint8_t *prow = pbuf0 + pb * 2 * LY::PH_BYTES;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int ch = half * 4 + c;
-                        *reinterpret_cast<uint4 *>(prow + ((ch ^ (row & 7)) << 4)) =
-                            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+                    for (int pc = 0; pc < kKQ / 32; ++pc) {
+                        uint32_t pw[16];
+#pragma unroll
+                        for (int e2 = 0; e2 < 32; e2 += 2) {
+                            const int e = pc * 32 + e2;
+                            float y0 = __uint_as_float(x[e]), y1 = __uint_as_float(x[e + 1]);
+                            ffma2(y0, y1, sl2, sl2, nl, nl);
+                            float q0 = p2[e], q1 = p2[e + 1];
+                            ffma2(q0, q1, nlam, nlam, fast_exp2(y0), fast_exp2(y1));   // P = p1 - lambda p2
+                            if (need_mask) {
+                                if (k0 + e > last_key) q0 = 0.f;
+                                if (k0 + e + 1 > last_key) q1 = 0.f;
+                            }
+                            pw[e2 / 2] = pack_bf16x2(q0, q1);
+                        }
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const int ch = chunk0 + pc * 4 + c;
+                            *reinterpret_cast<uint4 *>(prow + ((ch ^ (row & 7)) << 4)) =
+                                make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+                        }
                     }
                     fence_proxy_async_smem();
-                    warp_arrive(&ctl->p_full[buf], lane);
+                    warp_arrive(&ctl->p_full[pb][half], lane);
                     ++pk;
                 }
             }
 
             // ---------------------------------------------- epilogue: headwise norm of each head
             ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
-            if (ok) ok = warp_wait(&ctl->o_final, rr & 1, p.err, abort_flag);
+            if (ok) ok = warp_wait_fast(&ctl->o_final, rr & 1, p.err, abort_flag);
             tc_fence_after();
+            // the item's value MMAs are complete: the P buffers may hold the exchange again;
+            // this thread's output columns of each head are [kKQ kq, kKQ kq + kKQ)
 #pragma unroll
             for (int h = 0; h < S; ++h) {
                 float ss = 0.f;
                 if (ok) {
-                    const uint32_t tO = tmem + lane_off + 128 * h + half * 64;
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
+                    for (int c = 0; c < kKQ / 32; ++c) {
                         uint32_t o[32];
-                        tmem_ld32(tO + cc * 32, o);
+                        tmem_ld32(tmem + lane_off + 128 * h + kq * kKQ + c * 32, o);
                         tmem_ld_wait_regs(o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) ss = fmaf(__uint_as_float(o[e]), __uint_as_float(o[e]), ss);
                     }
                 }
-                ctl->ss[half][h][row] = ss;
+                xch->ss[kq][h][row] = ss;
             }
-            named_bar_sync(pair_bar, 64);
+            named_bar_sync(row_bar, kRowThreads);
             ok = __all_sync(0xffffffffu, ok);
 #pragma unroll
             for (int h = 0; h < S; ++h) {
-                const float ss_tot = ctl->ss[0][h][row] + ctl->ss[1][h][row];
+                float ss_tot = 0.f;
+#pragma unroll
+                for (int q = 0; q < kNQ; ++q) ss_tot += xch->ss[q][h][row];
                 const float yscale = p.no_norm ? 1.f : (1.f - p.lambda_init) * rsqrtf(ss_tot / 128.f + p.eps);
                 if (ok) {
-                    const uint32_t tO = tmem + lane_off + 128 * h + half * 64;
-                    __nv_bfloat16 *orow =
-                        p.out + ((static_cast<size_t>(it.b) * p.L + qrow) * p.hs + it.h0 + h) * 128 + half * 64;
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
+                    for (int c = 0; c < kKQ / 32; ++c) {
                         uint32_t o[32];
-                        tmem_ld32(tO + cc * 32, o);
+                        tmem_ld32(tmem + lane_off + 128 * h + kq * kKQ + c * 32, o);
                         tmem_ld_wait_regs(o);
                         uint32_t pko[16];
 #pragma unroll
                         for (int e = 0; e < 32; e += 2)
                             pko[e / 2] = pack_bf16x2(__uint_as_float(o[e]) * yscale, __uint_as_float(o[e + 1]) * yscale);
                         if (in) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+                            uint4 *dst = reinterpret_cast<uint4 *>(
+                                p.out + ((static_cast<size_t>(it.b) * p.L + qrow) * p.hs + it.h0 + h) * 128 + kq * kKQ +
+                                c * 32);
 #pragma unroll
                             for (int v4 = 0; v4 < 4; ++v4)
                                 dst[v4] = make_uint4(pko[4 * v4], pko[4 * v4 + 1], pko[4 * v4 + 2], pko[4 * v4 + 3]);
@@ -532,8 +643,10 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             // the accumulators may now be overwritten by the next item's first value MMA
             tc_fence_before();
             warp_arrive(&ctl->o_free, lane);
-            // both warps of the pair agree on whether to go on (pairs share no named barrier)
-            if (bar_red_or(pair_bar, 64, !ok || *abort_flag)) break;
+            // the four warps of the row agree on whether to go on (rows share no named
+            // barrier); this also orders the reads of the exchange above before the next
+            // item's writes
+            if (bar_red_or(row_bar, kRowThreads, !ok || *abort_flag)) break;
         }
     }
 
@@ -574,7 +687,7 @@ int launch_group_impl(const PrefillArgs &a, cudaStream_t stream) {
     {
         const uint64_t dv4[4] = {128, hs, Lk, B};
         const uint64_t sv[3] = {256, hs * 256, Lk * hs * 256};
-        const uint32_t box[4] = {64, 1, kGBN, 1};
+        const uint32_t box[4] = {64, 1, kPH, 1};
         if (!encode_tmap_4d_bf16(&mV, a.v, dv4, sv, box)) return GDA_ERR_CUDA;
     }
     GParams p;
