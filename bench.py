@@ -42,8 +42,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM counters of one ncu capture per kernel, valid while the kernel's
 # sources hash to the recorded value
 PROFILES = {
-    "prefill": (os.path.join(ROOT, "profiles", "prefill_tc_counters.json"),
-                ["grouped_differential_attention_gb300/csrc/gda_prefill_tc.cu",
+    "prefill": (os.path.join(ROOT, "profiles", "prefill_group_counters.json"),
+                ["grouped_differential_attention_gb300/csrc/gda_prefill_group.cu",
                  "grouped_differential_attention_gb300/csrc/gda_prefill_common.cuh",
                  "grouped_differential_attention_gb300/csrc/gda_device.cuh"]),
     "decode": (os.path.join(ROOT, "profiles", "decode_split_counters.json"),
@@ -745,7 +745,8 @@ def run_gda(args, world, rank, local):
             "parallelism": f"{world} independent replica(s), no collective on the data path",
         },
         "roofline": {
-            "kernel": "gda_prefill_tc_kernel<64>",
+            "kernel": "gda_prefill_group_kernel<3>" if (w.d == 64 and w.dv == 128 and w.h_s == 3 * w.h_n)
+                      else "gda_prefill_tc_kernel",
             "bound": "tensor",
             "achieved": achieved,
             "peak": peaks["bf16_tflops"],
@@ -781,7 +782,7 @@ def run_gda(args, world, rank, local):
                          "roofline": {"bound": "hbm", "achieved": dec_bytes / (dp_ms_step * 1e-3) / 1e9,
                                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": dec_bytes / (dp_ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"]}},
-        "launch_stats": {"kernel": "gda_prefill_tc_kernel<64>", "launches": len(lat_us), "warmup": 10,
+        "launch_stats": {"kernel": "gda_attn_fwd (grouped kernel at d = 64, dv = 128)", "launches": len(lat_us), "warmup": 10,
                          "us_min": lat_us[0], "us_median": lat_us[len(lat_us) // 2],
                          "us_p90": lat_us[int(0.9 * (len(lat_us) - 1))],
                          "tflops_at_median": flops / (lat_us[len(lat_us) // 2] * 1e-6) / 1e12,

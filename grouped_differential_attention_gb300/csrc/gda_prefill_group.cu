@@ -733,7 +733,18 @@ bool prefill_group_supported(const PrefillArgs &a) { return a.d == 64 && a.dv ==
 
 int launch_prefill_group(const PrefillArgs &a, cudaStream_t stream) {
     if (!prefill_group_supported(a)) return GDA_ERR_UNSUPPORTED;
-    switch (heads_per_item(a.hs / a.hn)) {
+    int S = heads_per_item(a.hs / a.hn);
+    if (S > 1) {
+        // Few query tiles (a short chunk, a small batch): items of one signal head each
+        // when whole groups would leave more than half of the SMs without an item.
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return record_cuda_error(e);
+        const long long nqt = (a.L + kBM - 1) / kBM;
+        if (2 * nqt * a.B * (a.hs / S) < sms) S = 1;
+    }
+    switch (S) {
         case 3: return launch_group_impl<3>(a, stream);
         case 2: return launch_group_impl<2>(a, stream);
         default: return launch_group_impl<1>(a, stream);
