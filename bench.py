@@ -402,6 +402,21 @@ def run_gda(args, world, rank, local):
     dp8_ms_step = ev8.elapsed_time(ev9) / dec_steps
     del dpg8
 
+    # ---- the headline workload held to the per-signal-head single-pass kernel (for comparison)
+    for i in range(3):
+        step_sp = sets[i % N_INPUT_SETS]
+        gda.gda_attn_fwd(*step_sp, w.lambda_init, causal=w.causal, eps=w.eps, out=out, flags=gda.GDA_FLAG_SINGLE_PASS)
+    torch.cuda.synchronize(dev)
+    sp_steps = 10
+    eva, evb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    eva.record(stream)
+    for i in range(sp_steps):
+        gda.gda_attn_fwd(*sets[i % N_INPUT_SETS], w.lambda_init, causal=w.causal, eps=w.eps, out=out,
+                         flags=gda.GDA_FLAG_SINGLE_PASS)
+    evb.record(stream)
+    torch.cuda.synchronize(dev)
+    sp_ms = eva.elapsed_time(evb) / sp_steps
+
     # ---- the 3:1 B=4 L=2048 workload through gda_attn_fwd (rotating input sets, > L2)
     w2 = W.GDA3_PREFILL_L2048
     sets2 = []
@@ -826,6 +841,10 @@ def run_gda(args, world, rank, local):
                          "roofline": {"bound": "tensor", "achieved": fl4 / (ms4["two_pass"] * 1e-3) / 1e12,
                                       "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                       "frac": fl4 / (ms4["two_pass"] * 1e-3) / 1e12 / peaks["bf16_tflops"]}},
+        "headline_single_pass": {"workload": w.name + " through gda_attn_fwd with GDA_FLAG_SINGLE_PASS (noise map "
+                                              "recomputed per signal head, P1 and P2 rounded separately)",
+                                 "ms_per_step": sp_ms, "steps": sp_steps,
+                                 "value": flops / (sp_ms * 1e-3) / 1e12, "unit": "TFLOP/s"},
         "prefill_3to1_L2048": {"workload": w2.name + " through gda_attn_fwd",
                                "value": tf2, "unit": "TFLOP/s", "ms_per_step": ms2["default"], "steps": 200,
                                "tflops_min_count": fl2_min / (ms2["default"] * 1e-3) / 1e12,
