@@ -600,9 +600,9 @@ cudaError_t launch_split(dim3 grid, int threads, size_t smem, cudaStream_t strea
 
 }  // namespace
 
-// Upper bound on the split kernel's CTAs (three per SM on a 152-SM part); the
+// Upper bound on the split kernel's CTAs (four per SM on a 152-SM part); the
 // workspace holds one partial state per (CTA + sequence) slot.
-constexpr int kDecodeMaxCtas = 456;
+constexpr int kDecodeMaxCtas = 608;
 
 DecodePlan decode_plan(int B, int Lcap, int hs, int hn, int dv) {
     (void)Lcap;
@@ -662,14 +662,18 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     const size_t row_bytes = p.es * (static_cast<size_t>(a.hs) * a.d + static_cast<size_t>(a.hn) * a.d +
                                      static_cast<size_t>(a.hs) * a.dv);
     const int nheads = a.hs + a.hn;
-    // ring budget: three CTAs per SM when a CTA has at most 256 threads, two
-    // up to 512, else one (each with its static arrays within 228 KB); the
-    // largest stage of 8, 4 or 2 positions of which at least four fit (a
-    // stage also holds its P weights and rescale factor per head)
-    const int per_sm = threads <= 256 ? 3 : (threads <= 512 ? 2 : 1);
-    const size_t budget = per_sm == 3 ? 70 * 1024 : (per_sm == 2 ? 100 * 1024 : 200 * 1024);
+    // ring budget: four CTAs per SM for an fp8 cache whose CTA has at most
+    // 192 threads (measured 4.74 against 4.48 TB/s with three CTAs of three
+    // stages: the widening and multiply-adds need the extra warps), three
+    // when a CTA has at most 256 threads, two up to 512, else one (each with
+    // its static arrays within 228 KB); the largest stage of 8, 4 or 2
+    // positions of which at least the minimum count fits (a stage also holds
+    // its P weights and rescale factor per head)
+    const int per_sm = (f8 && threads <= 192) ? 4 : (threads <= 256 ? 3 : (threads <= 512 ? 2 : 1));
+    const size_t budget =
+        per_sm == 4 ? 52 * 1024 : (per_sm == 3 ? 70 * 1024 : (per_sm == 2 ? 100 * 1024 : 200 * 1024));
     int P = 8;
-    const size_t min_stages = per_sm == 3 ? 3 : 4;
+    const size_t min_stages = per_sm == 4 ? 2 : (per_sm == 3 ? 3 : 4);
     while (P > 2 && (row_bytes * P + nheads * (P + 1) * 4) * min_stages > budget) P /= 2;
     const size_t per_stage = row_bytes * P + static_cast<size_t>(nheads) * (P + 1) * 4;
     int stages = static_cast<int>(budget / per_stage);

@@ -342,8 +342,8 @@ int gda_attn_decode_paged_fp8(const void *q_sig, const void *q_noise, const void
  *   loads the library until the process exits.
  *   Returns GDA_ERR_WORKSPACE if gda_attn_decode_workspace_size(B, Lcap, h_s,
  *   h_n, dv) exceeds GDA_DECODE_SCRATCH_BYTES (e.g. 64 sequences with
- *   12 + 4 heads and dv = 128 need about 6.5 MB whatever their lengths;
- *   more than about 2200 such sequences do not fit).
+ *   12 + 4 heads and dv = 128 need about 8.3 MB whatever their lengths;
+ *   more than about 2000 such sequences do not fit).
  *   The first call on a device looks up the scratch array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
  *   before any stream capture.  If the lookup fails the call returns

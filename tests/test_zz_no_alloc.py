@@ -48,9 +48,9 @@ def test_no_alloc_decode_matches_workspace_decode(lib):
     gda.gda_device_error(clear=True)
     w = W.GDA3_DECODE_B64
     B, Lcap = 64, 8192
-    # the 64-sequence decode workload's split partials: about 6.5 MB of the 32 MiB array
+    # the 64-sequence decode workload's split partials: about 8.3 MB of the 32 MiB array
     need = gda.gda_attn_decode_workspace_size(B, Lcap, w.h_s, w.h_n, w.dv)
-    assert 6_000_000 < need < 7_000_000
+    assert 8_000_000 < need < 8_700_000
     assert need <= SCRATCH_BYTES
     q1, q2, k1c, k2c, vc, lens, lam = (t.cuda() for t in W.make_decode_inputs(w, seed=11))
     ref = gda.gda_attn_decode(q1, q2, k1c, k2c, vc, lens, lam, w.lambda_init, eps=w.eps)
