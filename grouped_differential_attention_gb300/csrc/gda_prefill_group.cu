@@ -55,6 +55,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 #include <cmath>
+#include <type_traits>
 
 #include "gda.h"
 #include "gda_device.cuh"
@@ -72,7 +73,17 @@ constexpr int kPH = 64;                // keys per P half / V tile
 constexpr int kKQ = GDA_GROUP_KEYS_PER_THREAD;   // keys of a 128-key tile per compute thread
 constexpr int kNQ = kGBN / kKQ;                  // compute threads per query row
 constexpr int kGComputeWarps = 4 * kNQ;
-constexpr int kGThreads = 32 * (2 + kGComputeWarps);
+// warps 0-3: TMA producer (0), MMA issuer (1), two idle; warps 4..: compute.  The first
+// warpgroup hands registers to the compute warpgroups (setmaxnreg): 640 threads launch with
+// 96 registers each (the most five warps per SM sub-partition allow) and the split below
+// uses exactly that pool: 4 x 32 x 32 + 16 x 32 x 112 = 640 x 96.
+constexpr int kGCtrlWarps = 4;
+constexpr int kGThreads = 32 * (kGCtrlWarps + kGComputeWarps);
+constexpr int kGLaunchRegs = 96;
+constexpr int kGCtrlRegs = 32;
+constexpr int kGComputeRegs = 112;
+static_assert(kGCtrlRegs * 32 * kGCtrlWarps + kGComputeRegs * 32 * kGComputeWarps <= kGLaunchRegs * kGThreads,
+              "register split exceeds the launch pool");
 static_assert(kKQ == 32 || kKQ == 64, "a thread takes 32 or 64 keys of each tile");
 
 template <int S> struct GLayout {
@@ -112,15 +123,6 @@ __device__ __forceinline__ uint32_t bump(uint32_t (&cnt)[4], uint32_t slot) {
         }
     return k;
 }
-
-// Per-item exchange between the warps that hold a row's key parts.  It
-// lives in the P buffers, which no MMA reads at the times it is used (after
-// the item's last value MMA, or before its first P tile is written).
-struct GExchange {
-    float xm[kNQ][4][kBM];     // [key part][map][row]: phase-A reference maximum
-    float xl[kNQ][4][kBM];     // [key part][map][row]: phase-A sum against it
-    float ss[kNQ][3][kBM];     // [column part][head][row]: epilogue sums of squares
-};
 
 struct GCtrl {
     uint64_t q_full, q_empty;
@@ -173,6 +175,15 @@ __device__ __forceinline__ bool gitem_of(const GParams &p, int S, int rr, int G,
 }
 
 // Per-warp arrival on a barrier that counts warps.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void warp_arrive(uint64_t *bar, uint32_t lane) {
     __syncwarp();
     if (lane == 0) mbar_arrive(bar);
@@ -211,8 +222,6 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     GCtrl *ctl = reinterpret_cast<GCtrl *>(smem + LY::TILES);
-    GExchange *xch = reinterpret_cast<GExchange *>(smem + LY::OFF_P);
-    static_assert(sizeof(GExchange) <= 2 * LY::PH_BYTES, "exchange fits the P buffers");
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int cid = blockIdx.x;
@@ -250,7 +259,9 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort_flag = &ctl->abort_flag;
 
-    if (warp == 0) {
+    if (warp < kGCtrlWarps) {
+      regs_dec<kGCtrlRegs>();
+      if (warp == 0) {
         // ================================================= TMA producer
         if (elect_one()) {
             tma_prefetch_desc(&tmQ1);
@@ -403,9 +414,11 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             drain_wait(&ctl->mma_idle, 0, p.err);
         }
         __syncwarp();
+      }
     } else {
         // ================================================= compute warps
-        const int kq = (warp - 2) / 4;            // keys [kKQ kq, kKQ kq + kKQ) of every 128-key tile
+        regs_inc<kGComputeRegs>();
+        const int kq = (warp - kGCtrlWarps) / 4;  // keys [kKQ kq, kKQ kq + kKQ) of every 128-key tile
         const int half = (kq * kKQ) / kPH;        // the P half (value MMA) those keys belong to
         const int quarter = warp % 4;
         const int row = quarter * 32 + lane;
@@ -416,6 +429,17 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
         // this thread's 16-byte chunks of its row in its P half (buffer 0)
         uint8_t *pbuf0 = smem + LY::OFF_P + half * LY::PH_BYTES + row * 128;
         const int chunk0 = ((kq * kKQ) % kPH) / 8;
+        // Per-item exchange between the kNQ warps that hold a row's key parts: 32 words in the
+        // row's own 128 bytes of P buffer 0, half 0 (phase-A maximum and sum of each part and
+        // map) and half 1 (epilogue sums of squares of each part and head).  Only the warps of
+        // the row's quarter touch those bytes, and they are synchronised by the row barrier;
+        // no value MMA reads them while the exchange is in use (before the item's first P tile
+        // of the row, after its last value MMA).  Word e sits at (e + row) % 32, so a warp's 32
+        // rows fall into 32 banks.
+        static_assert(kNQ * 8 <= 32 && kNQ * 4 <= 32 && kGBN == kBM, "exchange layout");
+        float *const xrow_a = reinterpret_cast<float *>(smem + LY::OFF_P + row * 128);
+        float *const xrow_b = reinterpret_cast<float *>(smem + LY::OFF_P + LY::PH_BYTES + row * 128);
+        auto xslot = [&](float *base, int e) -> float & { return base[(e + row) & 31]; };
         uint32_t cnt[4] = {0, 0, 0, 0};    // uses of each TMEM slot so far
         uint32_t pk = 0;
         GItem it;
@@ -428,42 +452,57 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             for (int h = 0; h < S; ++h) lam[h] = p.lambda[it.h0 + h];
             bool ok = true;
 
-            // load this thread's kKQ logits from TMEM slot `slot` into x; release the slot
-            auto load_use = [&](uint32_t (&x)[kKQ], uint32_t slot) {
-                const uint32_t k = bump(cnt, slot);
-                if (!warp_wait_fast(&ctl->s_full[slot], k & 1, p.err, abort_flag)) ok = false;
-                tc_fence_after();
+            // this thread's kKQ logits of TMEM slot `slot` into x
+            auto read_slot = [&](uint32_t (&x)[kKQ], uint32_t slot) {
 #pragma unroll
                 for (int c = 0; c < kKQ / 32; ++c)
                     tmem_ld32(tmem + lane_off + slot * 128 + kq * kKQ + c * 32,
                               *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
                 tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
                 if constexpr (kKQ == 64) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+            };
+            // wait for the logit MMA of the slot's next use, then read it
+            auto acquire = [&](uint32_t (&x)[kKQ], uint32_t slot) {
+                const uint32_t k = bump(cnt, slot);
+                if (!warp_wait_fast(&ctl->s_full[slot], k & 1, p.err, abort_flag)) ok = false;
+                tc_fence_after();
+                read_slot(x, slot);
+            };
+            auto release = [&](uint32_t slot) {
                 tc_fence_before();
                 warp_arrive(&ctl->s_free[slot], lane);
             };
+            auto load_use = [&](uint32_t (&x)[kKQ], uint32_t slot) {
+                acquire(x, slot);
+                release(slot);
+            };
+            // key tiles [0, jfull) hold no key past the last visible key of any row of this
+            // warp (its first row has the smallest); only the tiles from jfull on take the
+            // per-key compare
+            const int min_last = p.causal ? min(p.koff + it.q0 + quarter * 32, p.Lk - 1) : p.Lk - 1;
+            const int tfull = min_last - kq * kKQ - (kKQ - 1);
+            const int jfull = tfull < 0 ? 0 : min(it.nkv, tfull / kGBN + 1);
 
             // ---------------------------------------------- phase A: row statistics
-            // Each key quarter of the row keeps a reference mx (the exact maximum of its
-            // first tile with a visible key) and the sum ls of 2^(s c - mx); later tiles
-            // exponentiate against the reference directly, so no per-tile maximum sits on
-            // the critical path.  A tile whose sum exceeds 2^16 (or is not finite) is redone
-            // with its own maximum as the new reference and the running sum is rescaled.
+            // Each key quarter of the row keeps a reference mx and the sum ls of 2^(s c - mx).
+            // The reference is the exact maximum of the first tile, floored at -1e30 so that a
+            // quarter without a visible key sums zeros; later tiles exponentiate against it
+            // directly, so no per-tile maximum sits on the critical path.  When a tile's sum
+            // exceeds 2^16 (or is not finite) in any row of the warp, the warp reads the tile
+            // from TMEM again (its slot is released only after the check), moves the reference
+            // to the tile's maximum, rescales the running sum and sums the tile afresh.
             float mx[M], ls[M];
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-                mx[m] = -INFINITY;
-                ls[m] = 0.f;
-            }
             auto tile_max = [&](const uint32_t (&x)[kKQ]) -> float {
                 float m4[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) m4[i] = __uint_as_float(x[i]);
 #pragma unroll
-                for (int e = 4; e + 8 <= kKQ + 4; e += 8)
+                for (int e = 4; e + 8 <= kKQ; e += 8)
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         m4[i] = max3f(m4[i], __uint_as_float(x[e + 2 * i]), __uint_as_float(x[e + 2 * i + 1]));
+#pragma unroll
+                for (int i = 0; i < 4; ++i) m4[i] = fmaxf(m4[i], __uint_as_float(x[kKQ - 4 + i]));
                 return max3f(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;
             };
             auto tile_sum = [&](const uint32_t (&x)[kKQ], float ref) -> float {
@@ -480,41 +519,51 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                 }
                 return (sa + sb) + (sc + sd);
             };
-            for (int j = 0; j < it.nkv; ++j) {
+            auto mask_x = [&](uint32_t (&x)[kKQ], int k0) {
+#pragma unroll
+                for (int e = 0; e < kKQ; ++e)
+                    if (k0 + e > last_key) x[e] = __float_as_uint(-INFINITY);
+            };
+            auto stats_tile = [&](int j, auto first, auto masked) {
                 const int k0 = j * kGBN + kq * kKQ;
-                const bool need_mask = k0 + kKQ - 1 > last_key;
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
+                    const uint32_t slot = slot_a<S>(j * M + m);
                     uint32_t x[kKQ];
-                    load_use(x, slot_a<S>(j * M + m));
-                    if (need_mask) {
-#pragma unroll
-                        for (int e = 0; e < kKQ; ++e)
-                            if (k0 + e > last_key) x[e] = __float_as_uint(-INFINITY);
-                    }
-                    if (mx[m] == -INFINITY) mx[m] = tile_max(x);      // first tile with a visible key
-                    if (mx[m] != -INFINITY) {
+                    acquire(x, slot);
+                    if constexpr (decltype(masked)::value) mask_x(x, k0);
+                    if constexpr (decltype(first)::value) {
+                        mx[m] = fmaxf(tile_max(x), -1e30f);
+                        ls[m] = tile_sum(x, mx[m]);
+                    } else {
                         float ts = tile_sum(x, mx[m]);
-                        if (!(ts <= 65536.f)) {
-                            const float tm = tile_max(x);
-                            if (tm > mx[m]) {
-                                ls[m] *= fast_exp2(mx[m] - tm);
-                                mx[m] = tm;
-                            }
-                            ts = tile_sum(x, mx[m]);
+                        if (__any_sync(0xffffffffu, !(ts <= 65536.f))) {
+                            read_slot(x, slot);
+                            if constexpr (decltype(masked)::value) mask_x(x, k0);
+                            const float nr = fmaxf(mx[m], tile_max(x));
+                            ls[m] *= fast_exp2(mx[m] - nr);
+                            mx[m] = nr;
+                            ts = tile_sum(x, nr);
                         }
                         ls[m] += ts;
                     }
+                    release(slot);
                 }
+            };
+            constexpr std::true_type kYes{};
+            constexpr std::false_type kNo{};
+            if (jfull > 0) {
+                stats_tile(0, kYes, kNo);
+                for (int j = 1; j < jfull; ++j) stats_tile(j, kNo, kNo);
+            } else {
+                stats_tile(0, kYes, kYes);
             }
-            // combine the four key quarters of the row: lse = max + log2(sum), base 2.  The
-            // exchange lives in the P buffers: the previous item's value MMAs are complete
-            // (its epilogue waited for them) and this item writes no P before the second
-            // barrier below.
+            for (int j = jfull > 1 ? jfull : 1; j < it.nkv; ++j) stats_tile(j, kNo, kYes);
+            // combine the four key quarters of the row: lse = max + log2(sum), base 2
 #pragma unroll
             for (int m = 0; m < M; ++m) {
-                xch->xm[kq][m][row] = mx[m];
-                xch->xl[kq][m][row] = ls[m];
+                xslot(xrow_a, kq * 8 + m) = mx[m];
+                xslot(xrow_a, kq * 8 + 4 + m) = ls[m];
             }
             named_bar_sync(row_bar, kRowThreads);
             float nlse[M];                        // -lse of each map (-inf for rows past L: every P is 0)
@@ -522,21 +571,19 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             for (int m = 0; m < M; ++m) {
                 float mm = -INFINITY;
 #pragma unroll
-                for (int q = 0; q < kNQ; ++q) mm = fmaxf(mm, xch->xm[q][m][row]);
+                for (int q = 0; q < kNQ; ++q) mm = fmaxf(mm, xslot(xrow_a, q * 8 + m));
                 float lsum = 0.f;
 #pragma unroll
-                for (int q = 0; q < kNQ; ++q) {
-                    const float mq = xch->xm[q][m][row];
-                    if (mq != -INFINITY) lsum += xch->xl[q][m][row] * fast_exp2(mq - mm);
-                }
+                for (int q = 0; q < kNQ; ++q) lsum += xslot(xrow_a, q * 8 + 4 + m) * fast_exp2(xslot(xrow_a, q * 8 + m) - mm);
                 nlse[m] = in ? -(mm + __log2f(lsum)) : -INFINITY;
             }
             named_bar_sync(row_bar, kRowThreads); // all have read the exchange before P overwrites it
 
             // ---------------------------------------------- phase B: P_h = A1_h - lambda_h A2, P_h V_h
-            for (int j = 0; j < it.nkv; ++j) {
+            // one key tile: the noise map's probabilities, then each head's P tile (the per-key
+            // compare only in the masked instance)
+            auto diff_tile = [&](int j, auto need_mask) {
                 const int k0 = j * kGBN + kq * kKQ;
-                const bool need_mask = k0 + kKQ - 1 > last_key;
                 float p2[kKQ];
                 {
                     uint32_t x[kKQ];
@@ -571,7 +618,7 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                             ffma2(y0, y1, sl2, sl2, nl, nl);
                             float q0 = p2[e], q1 = p2[e + 1];
                             ffma2(q0, q1, nlam, nlam, fast_exp2(y0), fast_exp2(y1));   // P = p1 - lambda p2
-                            if (need_mask) {
+                            if constexpr (decltype(need_mask)::value) {
                                 if (k0 + e > last_key) q0 = 0.f;
                                 if (k0 + e + 1 > last_key) q1 = 0.f;
                             }
@@ -588,13 +635,15 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                     warp_arrive(&ctl->p_full[pb][half], lane);
                     ++pk;
                 }
-            }
+            };
+            for (int j = 0; j < jfull; ++j) diff_tile(j, kNo);
+            for (int j = jfull; j < it.nkv; ++j) diff_tile(j, kYes);
 
             // ---------------------------------------------- epilogue: headwise norm of each head
             ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
             if (ok) ok = warp_wait_fast(&ctl->o_final, rr & 1, p.err, abort_flag);
             tc_fence_after();
-            // the item's value MMAs are complete: the P buffers may hold the exchange again;
+            // the item's value MMAs are complete: the row's P bytes may hold the exchange again;
             // this thread's output columns of each head are [kKQ kq, kKQ kq + kKQ)
 #pragma unroll
             for (int h = 0; h < S; ++h) {
@@ -609,7 +658,7 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                         for (int e = 0; e < 32; ++e) ss = fmaf(__uint_as_float(o[e]), __uint_as_float(o[e]), ss);
                     }
                 }
-                xch->ss[kq][h][row] = ss;
+                xslot(xrow_b, kq * 4 + h) = ss;
             }
             named_bar_sync(row_bar, kRowThreads);
             ok = __all_sync(0xffffffffu, ok);
@@ -617,7 +666,7 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             for (int h = 0; h < S; ++h) {
                 float ss_tot = 0.f;
 #pragma unroll
-                for (int q = 0; q < kNQ; ++q) ss_tot += xch->ss[q][h][row];
+                for (int q = 0; q < kNQ; ++q) ss_tot += xslot(xrow_b, q * 4 + h);
                 const float yscale = p.no_norm ? 1.f : (1.f - p.lambda_init) * rsqrtf(ss_tot / 128.f + p.eps);
                 if (ok) {
 #pragma unroll
@@ -718,6 +767,12 @@ int launch_group_impl(const PrefillArgs &a, cudaStream_t stream) {
     static_assert(smem <= 232448, "shared memory budget");
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return record_cuda_error(e);
+    // the compute warps' setmaxnreg.inc waits until the pool holds its registers: launch only
+    // with the per-thread count the split was sized for
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    if (fa.numRegs != kGLaunchRegs) return GDA_ERR_UNSUPPORTED;
     const long long nitems = static_cast<long long>(p.nqt) * a.B * a.hn * p.nsub;
     if (nitems <= 0 || nitems > 0x7fffffffLL) return GDA_ERR_UNSUPPORTED;
     long long grid = sms;
