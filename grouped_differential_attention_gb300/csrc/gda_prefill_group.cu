@@ -73,15 +73,16 @@ constexpr int kPH = 64;                // keys per P half / V tile
 constexpr int kKQ = GDA_GROUP_KEYS_PER_THREAD;   // keys of a 128-key tile per compute thread
 constexpr int kNQ = kGBN / kKQ;                  // compute threads per query row
 constexpr int kGComputeWarps = 4 * kNQ;
-// warps 0-3: TMA producer (0), MMA issuer (1), two idle; warps 4..: compute.  The first
-// warpgroup hands registers to the compute warpgroups (setmaxnreg): 640 threads launch with
-// 96 registers each (the most five warps per SM sub-partition allow) and the split below
-// uses exactly that pool: 4 x 32 x 32 + 16 x 32 x 112 = 640 x 96.
+// warps 0-3: TMA producer (0), logit MMA issuer (1), value MMA issuer (2), one idle; warps
+// 4..: compute.  The first warpgroup hands registers to the compute warpgroups (setmaxnreg).
+// With 16 compute warps, 640 threads launch with 96 registers each (the most five warps per
+// SM sub-partition allow): 4 x 32 x 32 + 16 x 32 x 112 = 640 x 96.  With 8 compute warps,
+// 384 threads launch with 168: 4 x 32 x 40 + 8 x 32 x 232 <= 384 x 168.
 constexpr int kGCtrlWarps = 4;
 constexpr int kGThreads = 32 * (kGCtrlWarps + kGComputeWarps);
-constexpr int kGLaunchRegs = 96;
-constexpr int kGCtrlRegs = 32;
-constexpr int kGComputeRegs = 112;
+constexpr int kGLaunchRegs = kGComputeWarps == 16 ? 96 : 168;
+constexpr int kGCtrlRegs = kGComputeWarps == 16 ? 32 : 40;
+constexpr int kGComputeRegs = kGComputeWarps == 16 ? 112 : 232;
 static_assert(kGCtrlRegs * 32 * kGCtrlWarps + kGComputeRegs * 32 * kGComputeWarps <= kGLaunchRegs * kGThreads,
               "register split exceeds the launch pool");
 static_assert(kKQ == 32 || kKQ == 64, "a thread takes 32 or 64 keys of each tile");
@@ -175,6 +176,35 @@ __device__ __forceinline__ bool gitem_of(const GParams &p, int S, int rr, int G,
 }
 
 // Per-warp arrival on a barrier that counts warps.
+// Shared-memory matrix descriptor (128-byte swizzle) as two words: the low word holds
+// the start address and the leading byte offset, the high word the stride byte offset,
+// the descriptor version and the layout.  Advancing the start by b bytes (b a multiple
+// of 16, the tile inside shared memory) adds b / 16 to the low word.
+__host__ __device__ constexpr uint32_t sw128_desc_hi(uint32_t sbo) {
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t addr, uint32_t lbo) {
+    return ((addr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t desc_words(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+
+// Position in the K / V ring: slot and the parity of its fill.
+template <int NR>
+struct RingPos {
+    uint32_t st = 0, ph = 0;
+    __device__ __forceinline__ void advance(uint32_t n) {
+        st += n;
+        while (st >= static_cast<uint32_t>(NR)) {
+            st -= NR;
+            ph ^= 1u;
+        }
+    }
+};
+
 template <uint32_t N>
 __device__ __forceinline__ void regs_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
@@ -245,7 +275,7 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             }
         mbar_init(&ctl->o_final, 1);
         mbar_init(&ctl->o_free, kGComputeWarps);
-        mbar_init(&ctl->mma_idle, 1);
+        mbar_init(&ctl->mma_idle, 2);                              // one commit per MMA issuer
         ctl->abort_flag = 0;
         fence_mbar_init();
     }
@@ -335,14 +365,14 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ================================================= MMA issuer
+        // ================================================= logit MMA issuer
         if (elect_one()) {
-            const uint32_t qa0 = smem_u32(smem + LY::OFF_Q);
-            const uint32_t ra0 = smem_u32(smem + LY::OFF_R);
-            const uint32_t pa0 = smem_u32(smem + LY::OFF_P);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, 128, 1);
+            const uint32_t qlo0 = sw128_desc_lo(smem_u32(smem + LY::OFF_Q), 16);
+            const uint32_t klo0 = sw128_desc_lo(smem_u32(smem + LY::OFF_R), 16);
+            constexpr uint32_t hi_k = sw128_desc_hi(1024);
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kGBN, 0);
             uint32_t cnt[4] = {0, 0, 0, 0};    // uses of each TMEM slot so far
-            uint32_t ct = 0, pk = 0;
+            RingPos<NR> rp;
             bool ok = true;
             GItem it;
             int nitem = 0;
@@ -353,43 +383,21 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                 o_ready = true;
                 return nitem == 0 || wait_fast(&ctl->o_free, (nitem - 1) & 1, p.err, abort_flag);
             };
-            // logit MMA of map m into TMEM slot `slot`
+            // logit MMA of map m into TMEM slot `slot`: 128 x 128 x 64 as four K = 16 steps
             auto qk = [&](int m, uint32_t slot) -> bool {
                 const uint32_t k = bump(cnt, slot);
                 if (slot < static_cast<uint32_t>(S) && !need_o()) return false;
                 if (k >= 1 && !wait_fast(&ctl->s_free[slot], (k - 1) & 1, p.err, abort_flag)) return false;
-                const uint32_t st = ct % NR;
-                if (!wait_fast(&ctl->r_full[st], (ct / NR) & 1, p.err, abort_flag)) return false;
+                if (!wait_fast(&ctl->r_full[rp.st], rp.ph, p.err, abort_flag)) return false;
                 tc_fence_after();
-                issue_qk<64, kGBN>(tmem + slot * 128, qa0 + m * LY::Q_BYTES, ra0 + st * LY::R_BYTES);
-                mma_commit(&ctl->s_full[slot]);
-                mma_commit(&ctl->r_empty[st]);
-                ++ct;
-                return true;
-            };
-            // value MMAs of P-use v (phase-B index) of the current item: O_h += P_h V_h, one
-            // MMA group per 64-key half
-            auto pv = [&](int v) -> bool {
-                const int h = v % (S + 1) - 1, j = v / (S + 1);
-                const uint32_t pb = pk & 1;
-                if (!need_o()) return false;
-                for (int half = 0; half < 2; ++half) {
-                    if (!wait_fast(&ctl->p_full[pb][half], (pk >> 1) & 1, p.err, abort_flag)) return false;
-                    const uint32_t st = ct % NR;
-                    if (!wait_fast(&ctl->r_full[st], (ct / NR) & 1, p.err, abort_flag)) return false;
-                    tc_fence_after();
-                    const uint32_t pa = pa0 + (pb * 2 + half) * LY::PH_BYTES, va = ra0 + st * LY::R_BYTES;
+                const uint32_t qlo = qlo0 + m * (LY::Q_BYTES >> 4), klo = klo0 + rp.st * (LY::R_BYTES >> 4);
 #pragma unroll
-                    for (int k = 0; k < kPH / 16; ++k) {
-                        const uint64_t a = smem_desc_sw128(pa + k * 32, 16, 1024);
-                        const uint64_t b = smem_desc_sw128(va + k * 2048, kPH * 128, 1024);
-                        mma_ss(tmem + 128 * h, a, b, idesc_pv, (j > 0 || half > 0 || k > 0) ? 1u : 0u);
-                    }
-                    mma_commit(&ctl->p_empty[pb][half]);
-                    mma_commit(&ctl->r_empty[st]);
-                    ++ct;
-                }
-                ++pk;
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss(tmem + slot * 128, desc_words(qlo + 2 * kk, hi_k), desc_words(klo + 2 * kk, hi_k), idesc_qk,
+                           kk > 0 ? 1u : 0u);
+                mma_commit(&ctl->s_full[slot]);
+                mma_commit(&ctl->r_empty[rp.st]);
+                rp.advance(1);
                 return true;
             };
             for (int rr = 0; ok && gitem_of(p, S, rr, G, cid, it); ++rr) {
@@ -401,7 +409,66 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                 for (int i = 0; ok && i < nB; ++i) {
                     ok = qk(i % M, S + i % NB);
                     if (ok && i == nB - 1) mma_commit(&ctl->q_empty);     // the item's last logit MMA
-                    if (ok && i >= LAG && (i - LAG) % M != 0) ok = pv(i - LAG);
+                    if (i >= LAG && (i - LAG) % M != 0) rp.advance(2);     // the value issuer's two V tiles
+                }
+                for (int v = (nB > LAG ? nB - LAG : 0); v < nB; ++v)
+                    if (v % M != 0) rp.advance(2);
+                ++nitem;
+            }
+            // every issued MMA completes before TMEM is released
+            mma_commit(&ctl->mma_idle);
+            drain_wait(&ctl->mma_idle, 0, p.err);
+        }
+        __syncwarp();
+      } else if (warp == 2) {
+        // ================================================= value MMA issuer
+        if (elect_one()) {
+            const uint32_t plo0 = sw128_desc_lo(smem_u32(smem + LY::OFF_P), 16);
+            const uint32_t vlo0 = sw128_desc_lo(smem_u32(smem + LY::OFF_R), kPH * 128);
+            constexpr uint32_t hi_pv = sw128_desc_hi(1024);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, 128, 1);
+            uint32_t pk = 0;
+            RingPos<NR> rp;
+            bool ok = true;
+            GItem it;
+            int nitem = 0;
+            bool o_ready = true;
+            auto need_o = [&]() -> bool {
+                if (o_ready) return true;
+                o_ready = true;
+                return nitem == 0 || wait_fast(&ctl->o_free, (nitem - 1) & 1, p.err, abort_flag);
+            };
+            // value MMAs of P-use v (phase-B index) of the current item: O_h += P_h V_h, one
+            // MMA group per 64-key half
+            auto pv = [&](int v) -> bool {
+                const int h = v % (S + 1) - 1, j = v / (S + 1);
+                const uint32_t pb = pk & 1;
+                if (!need_o()) return false;
+                for (int half = 0; half < 2; ++half) {
+                    if (!wait_fast(&ctl->p_full[pb][half], (pk >> 1) & 1, p.err, abort_flag)) return false;
+                    if (!wait_fast(&ctl->r_full[rp.st], rp.ph, p.err, abort_flag)) return false;
+                    tc_fence_after();
+                    const uint32_t plo = plo0 + (pb * 2 + half) * (LY::PH_BYTES >> 4);
+                    const uint32_t vlo = vlo0 + rp.st * (LY::R_BYTES >> 4);
+#pragma unroll
+                    for (int k = 0; k < kPH / 16; ++k)
+                        mma_ss(tmem + 128 * h, desc_words(plo + 2 * k, hi_pv), desc_words(vlo + 128 * k, hi_pv), idesc_pv,
+                               (j > 0 || half > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(&ctl->p_empty[pb][half]);
+                    mma_commit(&ctl->r_empty[rp.st]);
+                    rp.advance(1);
+                }
+                ++pk;
+                return true;
+            };
+            for (int rr = 0; ok && gitem_of(p, S, rr, G, cid, it); ++rr) {
+                o_ready = false;
+                const int nA = it.nkv * M;
+                rp.advance(nA);                                          // the phase-A K tiles
+                const int nB = it.nkv * M;
+                for (int i = 0; ok && i < nB; ++i) {
+                    rp.advance(1);                                       // K tile of logit use i
+                    if (i >= LAG && (i - LAG) % M != 0) ok = pv(i - LAG);
                 }
                 for (int v = (nB > LAG ? nB - LAG : 0); ok && v < nB; ++v)
                     if (v % M != 0) ok = pv(v);
@@ -409,7 +476,6 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                 mma_commit(&ctl->o_final);
                 ++nitem;
             }
-            // every issued MMA completes before TMEM is released
             mma_commit(&ctl->mma_idle);
             drain_wait(&ctl->mma_idle, 0, p.err);
         }
