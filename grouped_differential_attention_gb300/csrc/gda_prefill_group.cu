@@ -249,8 +249,9 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
     constexpr int NB = LY::NB, LAG = LY::LAG, NR = LY::NR;
     constexpr int M = S + 1;                 // maps per item: noise map (0), signal heads (1..S)
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned; offsetting the shared array itself (no integer round trip) keeps
+    // every access below in the shared state space (32-bit addresses, LDS / STS)
+    uint8_t *smem = smem_raw + ((0u - smem_u32(smem_raw)) & 1023u);
     GCtrl *ctl = reinterpret_cast<GCtrl *>(smem + LY::TILES);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
