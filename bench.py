@@ -816,14 +816,14 @@ def run_gda(args, world, rank, local):
                              "roofline": {"bound": "hbm", "achieved": d8_bytes / (dp8_ms_step * 1e-3) / 1e9,
                                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                           "frac": d8_bytes / (dp8_ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"]}},
-        "prefill_chunk": {"workload": f"B={w.B}, {ck_L} new rows after a {ck_Lk - ck_L}-row cached prefix, "
-                                      f"{w.h_s}+{w.h_n} heads, d={w.d}, dv={w.dv}",
+        "prefill_chunk": {"workload": f"B={w2.B}, {ck_L} new rows after a {ck_Lk - ck_L}-row cached prefix, "
+                                      f"{w2.h_s}+{w2.h_n} heads, d={w2.d}, dv={w2.dv}",
                           "value": ck_flops / (ck_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ck_ms,
                           "steps": ck_steps,
                           "roofline": {"bound": "tensor", "achieved": ck_flops / (ck_ms * 1e-3) / 1e12,
                                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                        "frac": ck_flops / (ck_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}},
-        "prefill_2pass": {"workload": w.name + ": pass 1 row log-sum-exp of every signal and noise map, "
+        "prefill_2pass": {"workload": w2.name + ": pass 1 row log-sum-exp of every signal and noise map, "
                                             "pass 2 one P V product per head with P = A1 - lambda A2",
                           "value": tp_tflops, "unit": "TFLOP/s", "ms_per_step": tp_ms, "steps": tp_steps,
                           "gpu_launches": 2 * tp_steps,
@@ -854,26 +854,26 @@ def run_gda(args, world, rank, local):
                                "roofline": {"bound": "tensor", "achieved": tf2, "peak": peaks["bf16_tflops"],
                                             "unit": "TFLOP/s", "frac": tf2 / peaks["bf16_tflops"]}},
         "backward_bf16": {"workload": f"tensor-core gradients of q_sig, k_sig, q_noise, k_noise, v, lambda from bf16 "
-                                      f"inputs at B={w.B}, L={w.L}, {w.h_s}+{w.h_n} heads, d={w.d}, dv={w.dv}, causal",
+                                      f"inputs at B={w2.B}, L={w2.L}, {w2.h_s}+{w2.h_n} heads, d={w2.d}, dv={w2.dv}, causal",
                           "value": bb_tflops, "unit": "TFLOP/s", "ms_per_step": bb_ms, "steps": bb_steps,
                           "gpu_launches": 5 * bb_steps,
                           "speedup_vs_f32": bw_ms / bb_ms,
                           "roofline": {"bound": "tensor", "achieved": bb_tflops, "peak": peaks["bf16_tflops"],
                                        "unit": "TFLOP/s", "frac": bb_tflops / peaks["bf16_tflops"]}},
-        "train_step": {"workload": f"gda_attn_fwd then gda_attn_bwd_bf16 at B={w.B}, L={w.L}, {w.h_s}+{w.h_n} heads, "
-                                   f"d={w.d}, dv={w.dv}, causal",
-                       "value": w.B * w.L / (tr_ms * 1e-3), "unit": "tokens/s", "ms_per_step": tr_ms,
+        "train_step": {"workload": f"gda_attn_fwd then gda_attn_bwd_bf16 at B={w2.B}, L={w2.L}, {w2.h_s}+{w2.h_n} heads, "
+                                   f"d={w2.d}, dv={w2.dv}, causal",
+                       "value": w2.B * w2.L / (tr_ms * 1e-3), "unit": "tokens/s", "ms_per_step": tr_ms,
                        "steps": tr_steps, "gpu_launches": 6 * tr_steps,
-                       "tflops": (prefill_flops(w.B, w.L, w.h_s, w.h_n, w.d, w.dv, w.causal)
-                                  + backward_flops(w.B, w.L, w.h_s, w.h_n, w.d, w.dv)) / (tr_ms * 1e-3) / 1e12},
+                       "tflops": (prefill_flops(w2.B, w2.L, w2.h_s, w2.h_n, w2.d, w2.dv, w2.causal)
+                                  + backward_flops(w2.B, w2.L, w2.h_s, w2.h_n, w2.d, w2.dv)) / (tr_ms * 1e-3) / 1e12},
         "backward_f32": {"workload": f"float32 gradients of q_sig, k_sig, q_noise, k_noise, v, lambda at "
-                                     f"B={w.B}, L={w.L}, {w.h_s}+{w.h_n} heads, d={w.d}, dv={w.dv}, causal",
+                                     f"B={w2.B}, L={w2.L}, {w2.h_s}+{w2.h_n} heads, d={w2.d}, dv={w2.dv}, causal",
                          "value": bw_tflops, "unit": "TFLOP/s", "ms_per_step": bw_ms, "steps": bw_steps,
                          "gpu_launches": 3 * bw_steps,
                          "roofline": {"bound": "alu", "achieved": bw_tflops, "peak": FP32_SIMT_TFLOPS,
                                       "unit": "TFLOP/s", "frac": bw_tflops / FP32_SIMT_TFLOPS,
                                       "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz"}},
-        "lambda_reparam": {"workload": f"h_s={w.h_s} heads, d={w.d}", "us_per_call": lam_us,
+        "lambda_reparam": {"workload": f"h_s={w2.h_s} heads, d={w2.d}", "us_per_call": lam_us,
                            "calls": lam_steps, "gpu_launches": lam_steps,
                            "bound": "host launch rate: back-to-back calls through the Python binding "
                                     "(16 B x h_s x d read per call)"},
