@@ -175,8 +175,9 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
     using LY = PrepLayout;
     constexpr int KS = LY::KS, VS = LY::VS;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned, offset from the shared array itself so that accesses stay in the
+    // shared state space (32-bit addresses)
+    uint8_t *smem = smem_raw + ((0u - smem_u32(smem_raw)) & 1023u);
     PrepCtrl *ctl = reinterpret_cast<PrepCtrl *>(smem + LY::TILES);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int cid = blockIdx.x, G = gridDim.x;
@@ -560,8 +561,9 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
     using LY = KvLayout;
     constexpr int QS = LY::QS;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned, offset from the shared array itself so that accesses stay in the
+    // shared state space (32-bit addresses)
+    uint8_t *smem = smem_raw + ((0u - smem_u32(smem_raw)) & 1023u);
     KvCtrl *ctl = reinterpret_cast<KvCtrl *>(smem + LY::TILES);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int cid = blockIdx.x, G = gridDim.x;
@@ -911,8 +913,9 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
     using LY = QLayout;
     constexpr int KS = LY::KS;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned, offset from the shared array itself so that accesses stay in the
+    // shared state space (32-bit addresses)
+    uint8_t *smem = smem_raw + ((0u - smem_u32(smem_raw)) & 1023u);
     QCtrl *ctl = reinterpret_cast<QCtrl *>(smem + LY::TILES);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int cid = blockIdx.x, G = gridDim.x;

@@ -120,8 +120,9 @@ gda_lse_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
     constexpr int KS = LY::KS;
     const int heads = p.hs + p.hn;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned, offset from the shared array itself so that accesses stay in the
+    // shared state space (32-bit addresses)
+    uint8_t *smem = smem_raw + ((0u - smem_u32(smem_raw)) & 1023u);
     LseCtrl *ctl = reinterpret_cast<LseCtrl *>(smem + LY::TILES);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -375,8 +376,9 @@ gda_diffmap_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_con
     constexpr int KS = LY::KS;
     constexpr int VS = LY::VS;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned, offset from the shared array itself so that accesses stay in the
+    // shared state space (32-bit addresses)
+    uint8_t *smem = smem_raw + ((0u - smem_u32(smem_raw)) & 1023u);
     DmCtrl *ctl = reinterpret_cast<DmCtrl *>(smem + LY::TILES);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;

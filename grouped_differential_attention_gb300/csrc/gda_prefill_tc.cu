@@ -151,8 +151,9 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
     constexpr int VS = LY::VS;
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned, offset from the shared array itself so that accesses stay in the
+    // shared state space (32-bit addresses)
+    uint8_t *smem = smem_raw + ((0u - smem_u32(smem_raw)) & 1023u);
     Ctrl *ctl = reinterpret_cast<Ctrl *>(smem + LY::TILES);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
