@@ -34,21 +34,24 @@
 // (313 cycles at N = 128) is faster than one reading it from TMEM (439).
 //
 // TMEM (512 columns): accumulators O_h at [128 h, 128 h + 128) for h < S,
-// then NSLOT slots of 128 columns for 128-key logit tiles (one at S = 3).
-// A slot is released as soon as the compute warps have loaded its tile into
-// registers (P goes to shared memory).
-// Warp roles (persistent CTA, one per SM):
-//   warp 0      TMA producer: Q2 and the S Q1 tiles once per item, a ring of
-//               128-key K tiles (one head each) and a ring of 64-key V tiles
-//               (one head each) in exactly the order the MMAs consume them;
-//   warp 1      TMEM allocator and MMA issuer: logit MMAs (SS, K-major, N =
-//               128) into the slot ring, value MMAs (SS: P from shared
-//               memory, V as an MN-major operand) NSLOT uses behind;
-//   warps 2-17  compute (thread = query row = TMEM lane; warps 2-5 take keys
-//               0-31 of each 128-key tile, warps 6-9 keys 32-63, 10-13 keys
-//               64-95, 14-17 keys 96-127: four compute warps per SM
-//               sub-partition, so one warp's exponential latency hides behind
-//               the others): running statistics, P, and the item's epilogue.
+// then NB = 4 - S slots of 128 columns for 128-key logit tiles (one at S = 3);
+// phase A also uses the accumulator columns as logit slots.  A slot is released
+// as soon as the compute warps have loaded its tile into registers (P goes to
+// shared memory).
+// Warp roles (persistent CTA, one per SM, 20 warps):
+//   warp 0      TMA producer: Q2 and the S Q1 tiles once per item, then one ring
+//               of 16 KB slots carrying 128-key K tiles and 64-key V tiles in
+//               exactly the order the MMAs consume them;
+//   warp 1      TMEM allocator and logit-MMA issuer (SS, K-major, N = 128);
+//   warp 2      value-MMA issuer (SS: P from shared memory, V as an MN-major
+//               operand), LAG uses behind the logits; the two issuers sit on
+//               different SM sub-partitions and each skips the other's ring
+//               entries;
+//   warp 3      idle (completes the first warpgroup, which hands registers to
+//               the compute warpgroups with setmaxnreg);
+//   warps 4-19  compute (thread = query row = TMEM lane; warp w takes keys
+//               [32 k, 32 k + 32) of each tile, k = (w - 4) / 4: four compute
+//               warps per SM sub-partition): statistics, P, and the epilogue.
 // Every mbarrier wait is bounded (1 s) and sets GDA_DEVERR_PREFILL_TIMEOUT.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -175,7 +178,6 @@ __device__ __forceinline__ bool gitem_of(const GParams &p, int S, int rr, int G,
     return true;
 }
 
-// Per-warp arrival on a barrier that counts warps.
 // Shared-memory matrix descriptor (128-byte swizzle) as two words: the low word holds
 // the start address and the leading byte offset, the high word the stride byte offset,
 // the descriptor version and the layout.  Advancing the start by b bytes (b a multiple
@@ -214,10 +216,9 @@ __device__ __forceinline__ void regs_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-__device__ __forceinline__ void warp_arrive(uint64_t *bar, uint32_t lane) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar);
-}
+// Every lane of the warp arrives once (the barriers the compute warps release count
+// lanes): no warp-level synchronisation and no single-lane branch on the hot path.
+__device__ __forceinline__ void lanes_arrive(uint64_t *bar) { mbar_arrive(bar); }
 
 // Bounded wait without the suspend-time hint: a wait whose phase has already
 // completed costs about a third as much as the hinted form, which matters on
@@ -267,15 +268,15 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
         }
         for (int s = 0; s < 4; ++s) {
             mbar_init(&ctl->s_full[s], 1);
-            mbar_init(&ctl->s_free[s], kGComputeWarps);
+            mbar_init(&ctl->s_free[s], 32 * kGComputeWarps);
         }
         for (int s = 0; s < 2; ++s)
             for (int hf = 0; hf < 2; ++hf) {
-                mbar_init(&ctl->p_full[s][hf], kGComputeWarps / 2);      // the warps writing the half
+                mbar_init(&ctl->p_full[s][hf], 16 * kGComputeWarps);     // the lanes writing the half
                 mbar_init(&ctl->p_empty[s][hf], 1);
             }
         mbar_init(&ctl->o_final, 1);
-        mbar_init(&ctl->o_free, kGComputeWarps);
+        mbar_init(&ctl->o_free, 32 * kGComputeWarps);
         mbar_init(&ctl->mma_idle, 2);                              // one commit per MMA issuer
         ctl->abort_flag = 0;
         fence_mbar_init();
@@ -531,13 +532,13 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             // wait for the logit MMA of the slot's next use, then read it
             auto acquire = [&](uint32_t (&x)[kKQ], uint32_t slot) {
                 const uint32_t k = bump(cnt, slot);
-                if (!warp_wait_fast(&ctl->s_full[slot], k & 1, p.err, abort_flag)) ok = false;
+                if (!wait_fast(&ctl->s_full[slot], k & 1, p.err, abort_flag)) ok = false;   // no vote: only sets the flag
                 tc_fence_after();
                 read_slot(x, slot);
             };
             auto release = [&](uint32_t slot) {
                 tc_fence_before();
-                warp_arrive(&ctl->s_free[slot], lane);
+                lanes_arrive(&ctl->s_free[slot]);
             };
             auto load_use = [&](uint32_t (&x)[kKQ], uint32_t slot) {
                 acquire(x, slot);
@@ -672,7 +673,7 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                     // of the value MMA's A operand (16-byte chunk c of row t at chunk c ^ (t % 8));
                     // written once the value MMA two P tiles back has read the buffer
                     const uint32_t pb = pk & 1;
-                    if (pk >= 2 && !warp_wait_fast(&ctl->p_empty[pb][half], ((pk >> 1) - 1) & 1, p.err, abort_flag))
+                    if (pk >= 2 && !wait_fast(&ctl->p_empty[pb][half], ((pk >> 1) - 1) & 1, p.err, abort_flag))
                         ok = false;
                     uint8_t *prow = pbuf0 + pb * 2 * LY::PH_BYTES;
 #pragma unroll
@@ -699,7 +700,7 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                         }
                     }
                     fence_proxy_async_smem();
-                    warp_arrive(&ctl->p_full[pb][half], lane);
+                    lanes_arrive(&ctl->p_full[pb][half]);
                     ++pk;
                 }
             };
@@ -758,7 +759,7 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             }
             // the accumulators may now be overwritten by the next item's first value MMA
             tc_fence_before();
-            warp_arrive(&ctl->o_free, lane);
+            lanes_arrive(&ctl->o_free);
             // the four warps of the row agree on whether to go on (rows share no named
             // barrier); this also orders the reads of the exchange above before the next
             // item's writes
