@@ -165,6 +165,27 @@ __device__ __forceinline__ bool prep_item(const BwdTcParams &p, int r, int G, in
     return true;
 }
 
+// Bounded wait that first polls without the suspend-time hint (a wait whose phase has
+// already completed costs about a third as much that way, which matters on the
+// single-thread MMA issuers), then falls back to the bounded hinted wait.
+__device__ __forceinline__ bool wait_quick(uint64_t *bar, uint32_t parity, unsigned *err, volatile int *abort) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0 || wait_bar(bar, parity, err, abort);
+}
+
+// The same for a whole warp, which agrees on the result by vote.
+__device__ __forceinline__ bool warp_wait_quick(uint64_t *bar, uint32_t parity, unsigned *err,
+                                                volatile int *abort) {
+    return __all_sync(0xffffffffu, wait_quick(bar, parity, err, abort));
+}
+
 constexpr int kEwP = 512;           // prep elementwise threads: 16 warps, four column groups
 constexpr int kThrP = 64 + kEwP;
 
@@ -229,7 +250,7 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
             int b, h, q0, nkv;
             for (int r = 0; ok && prep_item(p, r, G, cid, b, h, q0, nkv); ++r) {
                 const int g = h / r_grp;
-                if (r > 0 && !wait_bar(&ctl->q_empty, (r - 1) & 1, p.err, abort_flag)) break;
+                if (r > 0 && !wait_quick(&ctl->q_empty, (r - 1) & 1, p.err, abort_flag)) break;
                 mbar_arrive_expect_tx(&ctl->q_full, 2 * LY::Q_BYTES);
                 tma_load_4d(smem + LY::OFF_Q1, &tmQ1, &ctl->q_full, 0, h, q0, b);
                 tma_load_4d(smem + LY::OFF_Q2, &tmQ2, &ctl->q_full, 0, g, q0, b);
@@ -237,7 +258,7 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                 auto load_k = [&](int j) -> bool {
                     const uint32_t gk = kt + j;
                     const int st = gk % KS;
-                    if (gk >= KS && !wait_bar(&ctl->k_empty[st], ((gk / KS) - 1) & 1, p.err, abort_flag))
+                    if (gk >= KS && !wait_quick(&ctl->k_empty[st], ((gk / KS) - 1) & 1, p.err, abort_flag))
                         return false;
                     uint8_t *sb = smem + LY::OFF_K + st * LY::KST_BYTES;
                     mbar_arrive_expect_tx(&ctl->k_full[st], LY::KST_BYTES);
@@ -248,7 +269,7 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                 auto load_v = [&](int j) -> bool {
                     const uint32_t gv = vt + j;
                     const int st = gv % VS;
-                    if (gv >= VS && !wait_bar(&ctl->v_empty[st], ((gv / VS) - 1) & 1, p.err, abort_flag))
+                    if (gv >= VS && !wait_quick(&ctl->v_empty[st], ((gv / VS) - 1) & 1, p.err, abort_flag))
                         return false;
                     uint8_t *sb = smem + LY::OFF_V + st * LY::V_BYTES;
                     mbar_arrive_expect_tx(&ctl->v_full[st], LY::V_BYTES);
@@ -288,10 +309,10 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
             bool ok = true;
             int b, h, q0, nkv;
             for (int r = 0; ok && prep_item(p, r, G, cid, b, h, q0, nkv); ++r) {
-                if (!wait_bar(&ctl->q_full, r & 1, p.err, abort_flag)) break;
+                if (!wait_quick(&ctl->q_full, r & 1, p.err, abort_flag)) break;
                 for (int t = 0; t < 2 && t < nkv; ++t) {
                     const uint32_t gk = kt + t, gs = gt + t;
-                    if (!wait_bar(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t ka = k0a + (gk % KS) * LY::KST_BYTES;
                     issue_qk<kD, kN>(tmem + tS1_0 + (gs & 1) * kN, q1a, ka);
@@ -301,12 +322,12 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                 }
                 if (!ok) break;
                 if (nkv <= 2) mma_commit(&ctl->q_empty);
-                if (r > 0 && !wait_bar(&ctl->o_free, (r - 1) & 1, p.err, abort_flag)) break;
+                if (r > 0 && !wait_quick(&ctl->o_free, (r - 1) & 1, p.err, abort_flag)) break;
                 for (int j = 0; j < nkv; ++j) {
                     const uint32_t gs = gt + j, gv = vt + j;
                     const int bb = gs & 1;
-                    if (!wait_bar(&ctl->p_full[bb], (gs >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
-                    if (!wait_bar(&ctl->v_full[gv % VS], (gv / VS) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->p_full[bb], (gs >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->v_full[gv % VS], (gv / VS) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t va = v0a + (gv % VS) * LY::V_BYTES;
                     issue_ts64q<kDV>(tmem, tmem + tS1_0 + bb * kN, va, j > 0);
@@ -315,7 +336,7 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                     const int jn = j + 2;
                     if (jn < nkv) {
                         const uint32_t gk = kt + jn;
-                        if (!wait_bar(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
+                        if (!wait_quick(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t ka = k0a + (gk % KS) * LY::KST_BYTES;
                         issue_qk<kD, kN>(tmem + tS1_0 + bb * kN, q1a, ka);
@@ -365,7 +386,7 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
             for (int j = 0; j < nkv; ++j) {
                 const uint32_t gs = gt + j;
                 const int bb = gs & 1;
-                if (!warp_wait(&ctl->s_full[bb], (gs >> 1) & 1, p.err, abort_flag)) {
+                if (!warp_wait_quick(&ctl->s_full[bb], (gs >> 1) & 1, p.err, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -616,13 +637,13 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
             bool ok = true;
             int b, g, k0, i0, nq;
             for (int r = 0; ok && kv_item(p, r, G, cid, b, g, k0, i0, nq); ++r) {
-                if (r > 0 && !wait_bar(&ctl->g_empty, (r - 1) & 1, p.err, abort_flag)) break;
+                if (r > 0 && !wait_quick(&ctl->g_empty, (r - 1) & 1, p.err, abort_flag)) break;
                 mbar_arrive_expect_tx(&ctl->g_full, LY::K_BYTES);
                 tma_load_4d(smem + LY::OFF_K2, &tmK2, &ctl->g_full, 0, g, k0, b);
                 ++ng;
                 for (int hi = 0; ok && hi < r_grp; ++hi) {
                     const int h = g * r_grp + hi;
-                    if (nh > 0 && !wait_bar(&ctl->h_empty, (nh - 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (nh > 0 && !wait_quick(&ctl->h_empty, (nh - 1) & 1, p.err, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(&ctl->h_full, LY::K_BYTES + LY::V_BYTES);
                     tma_load_4d(smem + LY::OFF_K1, &tmK1, &ctl->h_full, 0, h, k0, b);
                     tma_load_4d(smem + LY::OFF_V, &tmV, &ctl->h_full, 0, h, k0, b);
@@ -631,7 +652,7 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
                     for (int i = 0; i < nq; ++i) {
                         const int q0 = (i0 + i) * kN;
                         const int st = gq % QS;
-                        if (gq >= QS && !wait_bar(&ctl->q_empty[st], ((gq / QS) - 1) & 1, p.err, abort_flag)) {
+                        if (gq >= QS && !wait_quick(&ctl->q_empty[st], ((gq / QS) - 1) & 1, p.err, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -670,10 +691,10 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
             // those while the elementwise threads still work on tile t
             auto finish = [&](uint32_t t, int i, int hi, int r) -> bool {
                 const int st = t % QS;
-                if (!wait_bar(&ctl->p_full, t & 1, p.err, abort_flag)) return false;
+                if (!wait_quick(&ctl->p_full, t & 1, p.err, abort_flag)) return false;
                 // accumulators of the previous head / item have been read
-                if (i == 0 && nh > 0 && !wait_bar(&ctl->acc_free, (nh - 1) & 1, p.err, abort_flag)) return false;
-                if (i == 0 && hi == 0 && r > 0 && !wait_bar(&ctl->k2_free, (r - 1) & 1, p.err, abort_flag))
+                if (i == 0 && nh > 0 && !wait_quick(&ctl->acc_free, (nh - 1) & 1, p.err, abort_flag)) return false;
+                if (i == 0 && hi == 0 && r > 0 && !wait_quick(&ctl->k2_free, (r - 1) & 1, p.err, abort_flag))
                     return false;
                 tc_fence_after();
                 const uint32_t sq = q0a + st * LY::QST_BYTES;
@@ -685,14 +706,14 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
                 return true;
             };
             for (int r = 0; ok && kv_item(p, r, G, cid, b, g, k0, i0, nq); ++r) {
-                if (!wait_bar(&ctl->g_full, r & 1, p.err, abort_flag)) break;
+                if (!wait_quick(&ctl->g_full, r & 1, p.err, abort_flag)) break;
                 for (int hi = 0; ok && hi < r_grp; ++hi) {
-                    if (!wait_bar(&ctl->h_full, nh & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->h_full, nh & 1, p.err, abort_flag)) { ok = false; break; }
                     for (int i = 0; i < nq; ++i) {
                         const int st = gq % QS;
-                        if (!wait_bar(&ctl->q_full[st], (gq / QS) & 1, p.err, abort_flag)) { ok = false; break; }
+                        if (!wait_quick(&ctl->q_full[st], (gq / QS) & 1, p.err, abort_flag)) { ok = false; break; }
                         // the previous tile's logits have been read into registers
-                        if (gq > 0 && !wait_bar(&ctl->s_free, (gq - 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                        if (gq > 0 && !wait_quick(&ctl->s_free, (gq - 1) & 1, p.err, abort_flag)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t sq = q0a + st * LY::QST_BYTES;
                         issue_nt<kD>(tmem + tS1, k1a, sq);                         // S1^T = K1 Q1^T
@@ -746,8 +767,8 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
                     const int q0 = (i0 + i) * kN + grp * 16;     // this group's first query column
                     const int st = gq % QS;
                     // the stage's vectors were written by the copy engine: observe its barrier too
-                    if (!warp_wait(&ctl->s_full, gq & 1, p.err, abort_flag) ||
-                        !warp_wait(&ctl->q_full[st], (gq / QS) & 1, p.err, abort_flag)) {
+                    if (!warp_wait_quick(&ctl->s_full, gq & 1, p.err, abort_flag) ||
+                        !warp_wait_quick(&ctl->q_full[st], (gq / QS) & 1, p.err, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -794,7 +815,7 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
                         pd2[e / 2] = pack_bf16x2(c2[0], c2[1]);
                     }
                     // the previous tile's products have read W / dS1 / dS2
-                    if (gq > 0 && !warp_wait(&ctl->w_free, (gq - 1) & 1, p.err, abort_flag)) {
+                    if (gq > 0 && !warp_wait_quick(&ctl->w_free, (gq - 1) & 1, p.err, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -970,13 +991,13 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
             bool ok = true;
             int b, g, q0, nkv;
             for (int r = 0; ok && q_item(p, r, G, cid, b, g, q0, nkv); ++r) {
-                if (r > 0 && !wait_bar(&ctl->g_empty, (r - 1) & 1, p.err, abort_flag)) break;
+                if (r > 0 && !wait_quick(&ctl->g_empty, (r - 1) & 1, p.err, abort_flag)) break;
                 mbar_arrive_expect_tx(&ctl->g_full, LY::Q_BYTES);
                 tma_load_4d(smem + LY::OFF_Q2, &tmQ2, &ctl->g_full, 0, g, q0, b);
                 ++ng;
                 for (int hi = 0; ok && hi < r_grp; ++hi) {
                     const int h = g * r_grp + hi;
-                    if (nh > 0 && !wait_bar(&ctl->h_empty, (nh - 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (nh > 0 && !wait_quick(&ctl->h_empty, (nh - 1) & 1, p.err, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(&ctl->h_full, LY::Q_BYTES + LY::DO_BYTES);
                     tma_load_4d(smem + LY::OFF_Q1, &tmQ1, &ctl->h_full, 0, h, q0, b);
                     tma_load_4d(smem + LY::OFF_DO, &tmdO, &ctl->h_full, 0, h, q0, b);
@@ -984,7 +1005,7 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                     ++nh;
                     for (int j = 0; j < nkv; ++j) {
                         const int st = gk % KS;
-                        if (gk >= KS && !wait_bar(&ctl->k_empty[st], ((gk / KS) - 1) & 1, p.err, abort_flag)) {
+                        if (gk >= KS && !wait_quick(&ctl->k_empty[st], ((gk / KS) - 1) & 1, p.err, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -1012,14 +1033,14 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
             bool ok = true;
             int b, g, q0, nkv;
             for (int r = 0; ok && q_item(p, r, G, cid, b, g, q0, nkv); ++r) {
-                if (!wait_bar(&ctl->g_full, r & 1, p.err, abort_flag)) break;
+                if (!wait_quick(&ctl->g_full, r & 1, p.err, abort_flag)) break;
                 for (int hi = 0; ok && hi < r_grp; ++hi) {
-                    if (!wait_bar(&ctl->h_full, nh & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->h_full, nh & 1, p.err, abort_flag)) { ok = false; break; }
                     // logits of tile t into S buffer (gk + t) & 1
                     auto issue_s = [&](int t) -> bool {
                         const uint32_t gt = gk + t;
                         const int st = gt % KS;
-                        if (!wait_bar(&ctl->k_full[st], (gt / KS) & 1, p.err, abort_flag)) return false;
+                        if (!wait_quick(&ctl->k_full[st], (gt / KS) & 1, p.err, abort_flag)) return false;
                         tc_fence_after();
                         const uint32_t sk = k0a + st * LY::KST_BYTES;
                         const uint32_t sb = tmem + (gt & 1) * kSB;
@@ -1034,12 +1055,12 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                         const uint32_t gj = gk + j;
                         const int st = gj % KS;
                         const int bb = gj & 1;
-                        if (!wait_bar(&ctl->p_full[bb], (gj >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
-                        if (j == 0 && nh > 0 && !wait_bar(&ctl->acc_free, (nh - 1) & 1, p.err, abort_flag)) {
+                        if (!wait_quick(&ctl->p_full[bb], (gj >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                        if (j == 0 && nh > 0 && !wait_quick(&ctl->acc_free, (nh - 1) & 1, p.err, abort_flag)) {
                             ok = false;
                             break;
                         }
-                        if (j == 0 && hi == 0 && r > 0 && !wait_bar(&ctl->q2_free, (r - 1) & 1, p.err, abort_flag)) {
+                        if (j == 0 && hi == 0 && r > 0 && !wait_quick(&ctl->q2_free, (r - 1) & 1, p.err, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -1101,7 +1122,7 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                 const float D2 = in ? p.D2[(static_cast<size_t>(b) * p.hs + h) * p.Lp + qrow] : 0.f;
                 for (int j = 0; j < nkv; ++j) {
                     const uint32_t sb = tmem + lane_off + (gk & 1) * kSB + grp * 16;
-                    if (!warp_wait(&ctl->s_full[gk & 1], (gk >> 1) & 1, p.err, abort_flag)) {
+                    if (!warp_wait_quick(&ctl->s_full[gk & 1], (gk >> 1) & 1, p.err, abort_flag)) {
                         ok = false;
                         break;
                     }
