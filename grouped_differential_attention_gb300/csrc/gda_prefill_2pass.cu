@@ -42,6 +42,21 @@
 namespace gda {
 namespace {
 
+// Bounded wait that first polls without the suspend-time hint (a wait whose phase has
+// already completed costs about a third as much that way, which matters on the
+// single-thread MMA issuer), then falls back to the bounded hinted wait.
+__device__ __forceinline__ bool wait_quick(uint64_t *bar, uint32_t parity, unsigned *err, volatile int *abort) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0 || wait_bar(bar, parity, err, abort);
+}
+
 constexpr int kWarps2 = 10;
 constexpr int kThreads2 = 32 * kWarps2;
 constexpr int kSmThreads = 256;     // softmax threads (8 warps)
@@ -170,7 +185,7 @@ gda_lse_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                 const void *tq = sig ? static_cast<const void *>(&tmQ1) : static_cast<const void *>(&tmQ2);
                 const void *tk = sig ? static_cast<const void *>(&tmK1) : static_cast<const void *>(&tmK2);
                 const int hh = sig ? it.head : it.head - p.hs;
-                if (r > 0 && !wait_bar(&ctl->q_empty, (r - 1) & 1, p.err, abort_flag)) break;
+                if (r > 0 && !wait_quick(&ctl->q_empty, (r - 1) & 1, p.err, abort_flag)) break;
                 mbar_arrive_expect_tx(&ctl->q_full, LY::Q_BYTES);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk)
@@ -180,7 +195,7 @@ gda_lse_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                 for (int j = 0; j < it.nkv; ++j) {
                     const uint32_t gk = kt + j;
                     const int st = gk % KS;
-                    if (gk >= KS && !wait_bar(&ctl->k_empty[st], ((gk / KS) - 1) & 1, p.err, abort_flag)) {
+                    if (gk >= KS && !wait_quick(&ctl->k_empty[st], ((gk / KS) - 1) & 1, p.err, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -207,13 +222,13 @@ gda_lse_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
             bool ok = true;
             Item2 it;
             for (int r = 0; ok && item2_of(p, heads, r, G, cid, it); ++r) {
-                if (!wait_bar(&ctl->q_full, r & 1, p.err, abort_flag)) break;
+                if (!wait_quick(&ctl->q_full, r & 1, p.err, abort_flag)) break;
                 for (int j = 0; j < it.nkv; ++j) {
                     const uint32_t gk = kt + j, gs = gt + j;
                     const int bb = gs & 1;
                     const uint32_t u = gs >> 1;
-                    if (!wait_bar(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
-                    if (u >= 1 && !wait_bar(&ctl->s_free[bb], (u - 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (u >= 1 && !wait_quick(&ctl->s_free[bb], (u - 1) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     issue_qk<D, kBN2>(tmem + bb * kBN2, qa, k0a + (gk % KS) * LY::K_BYTES);
                     mma_commit(&ctl->s_full[bb]);
@@ -433,7 +448,7 @@ gda_diffmap_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_con
             Item2 it;
             for (int r = 0; ok && item2_of(p, p.hs, r, G, cid, it); ++r) {
                 const int h = it.head, g = h / r_grp;
-                if (r > 0 && !wait_bar(&ctl->q_empty, (r - 1) & 1, p.err, abort_flag)) break;
+                if (r > 0 && !wait_quick(&ctl->q_empty, (r - 1) & 1, p.err, abort_flag)) break;
                 mbar_arrive_expect_tx(&ctl->q_full, 2 * LY::Q_BYTES);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk) {
@@ -444,7 +459,7 @@ gda_diffmap_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_con
                 auto load_k = [&](int j) -> bool {
                     const uint32_t gk = kt + j;
                     const int st = gk % KS;
-                    if (gk >= KS && !wait_bar(&ctl->k_empty[st], ((gk / KS) - 1) & 1, p.err, abort_flag))
+                    if (gk >= KS && !wait_quick(&ctl->k_empty[st], ((gk / KS) - 1) & 1, p.err, abort_flag))
                         return false;
                     uint8_t *sb = smem + LY::OFF_K + st * LY::KST_BYTES;
                     mbar_arrive_expect_tx(&ctl->k_full[st], LY::KST_BYTES);
@@ -459,7 +474,7 @@ gda_diffmap_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_con
                 auto load_v = [&](int j) -> bool {
                     const uint32_t gv = vt + j;
                     const int st = gv % VS;
-                    if (gv >= VS && !wait_bar(&ctl->v_empty[st], ((gv / VS) - 1) & 1, p.err, abort_flag))
+                    if (gv >= VS && !wait_quick(&ctl->v_empty[st], ((gv / VS) - 1) & 1, p.err, abort_flag))
                         return false;
                     uint8_t *sb = smem + LY::OFF_V + st * LY::V_BYTES;
                     mbar_arrive_expect_tx(&ctl->v_full[st], LY::V_BYTES);
@@ -505,11 +520,11 @@ gda_diffmap_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_con
             Item2 it;
             for (int r = 0; ok && item2_of(p, p.hs, r, G, cid, it); ++r) {
                 const int nkv = it.nkv;
-                if (!wait_bar(&ctl->q_full, r & 1, p.err, abort_flag)) break;
+                if (!wait_quick(&ctl->q_full, r & 1, p.err, abort_flag)) break;
                 // logits of the first two tiles (overlaps the previous epilogue)
                 for (int t = 0; t < 2 && t < nkv; ++t) {
                     const uint32_t gk = kt + t, gs = gt + t;
-                    if (!wait_bar(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t ka = k0a + (gk % KS) * LY::KST_BYTES;
                     issue_qk<D, kBN2>(tmem + tS1_0 + (gs & 1) * kBN2, q1a, ka);
@@ -519,19 +534,19 @@ gda_diffmap_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_con
                 }
                 if (!ok) break;
                 if (nkv <= 2) mma_commit(&ctl->q_empty);
-                if (r > 0 && !wait_bar(&ctl->o_free, (r - 1) & 1, p.err, abort_flag)) break;
+                if (r > 0 && !wait_quick(&ctl->o_free, (r - 1) & 1, p.err, abort_flag)) break;
                 for (int j = 0; j < nkv; ++j) {
                     const uint32_t gs = gt + j, gv = vt + j;
                     const int bb = gs & 1;
-                    if (!wait_bar(&ctl->p_full[bb], (gs >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
-                    if (!wait_bar(&ctl->v_full[gv % VS], (gv / VS) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->p_full[bb], (gs >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->v_full[gv % VS], (gv / VS) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     issue_pv_split<DV>(tmem, tmem + tS1_0 + bb * kBN2, v0a + (gv % VS) * LY::V_BYTES, j > 0);
                     mma_commit(&ctl->v_empty[gv % VS]);
                     const int jn = j + 2;
                     if (jn < nkv) {
                         const uint32_t gk = kt + jn;
-                        if (!wait_bar(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
+                        if (!wait_quick(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t ka = k0a + (gk % KS) * LY::KST_BYTES;
                         issue_qk<D, kBN2>(tmem + tS1_0 + bb * kBN2, q1a, ka);

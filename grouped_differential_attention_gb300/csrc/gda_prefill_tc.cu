@@ -53,6 +53,21 @@
 namespace gda {
 namespace {
 
+// Bounded wait that first polls without the suspend-time hint (a wait whose phase has
+// already completed costs about a third as much that way, which matters on the
+// single-thread MMA issuer), then falls back to the bounded hinted wait.
+__device__ __forceinline__ bool wait_quick(uint64_t *bar, uint32_t parity, unsigned *err, volatile int *abort) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0 || wait_bar(bar, parity, err, abort);
+}
+
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = 32 * (2 + kSoftmaxWarps);
 constexpr float kSumLimit = 65536.0f;       // per-tile P sum that triggers a new reference
@@ -211,7 +226,7 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
             Item it;
             for (int r = 0; ok && item_of(p, r, G, cid, BN, it); ++r) {
                 // Q of the previous item must have been read by its last QK
-                if (r > 0 && !wait_bar(&ctl->q_empty, (r - 1) & 1, p.err, abort_flag)) break;
+                if (r > 0 && !wait_quick(&ctl->q_empty, (r - 1) & 1, p.err, abort_flag)) break;
                 mbar_arrive_expect_tx(&ctl->q_full, 2 * LY::Q_BYTES);
 #pragma unroll
                 for (int blk = 0; blk < D / 64; ++blk) {
@@ -224,7 +239,7 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                 auto load_k = [&](int j) -> bool {
                     const uint32_t gk = kt + j;
                     const int st = gk % KS;
-                    if (gk >= KS && !wait_bar(&ctl->k_empty[st], ((gk / KS) - 1) & 1, p.err, abort_flag))
+                    if (gk >= KS && !wait_quick(&ctl->k_empty[st], ((gk / KS) - 1) & 1, p.err, abort_flag))
                         return false;
                     uint8_t *sb = smem + LY::OFF_K + st * LY::KST_BYTES;
                     mbar_arrive_expect_tx(&ctl->k_full[st], LY::KST_BYTES);
@@ -239,7 +254,7 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                 auto load_v = [&](int j) -> bool {
                     const uint32_t gv = vt + j;
                     const int st = gv % VS;
-                    if (gv >= VS && !wait_bar(&ctl->v_empty[st], ((gv / VS) - 1) & 1, p.err, abort_flag))
+                    if (gv >= VS && !wait_quick(&ctl->v_empty[st], ((gv / VS) - 1) & 1, p.err, abort_flag))
                         return false;
                     uint8_t *sb = smem + LY::OFF_V + st * LY::V_BYTES;
                     mbar_arrive_expect_tx(&ctl->v_full[st], LY::V_BYTES);
@@ -289,13 +304,13 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
             Item it;
             for (int r = 0; ok && item_of(p, r, G, cid, BN, it); ++r) {
                 const int nkv = it.nkv;
-                if (!wait_bar(&ctl->q_full, r & 1, p.err, abort_flag)) break;
+                if (!wait_quick(&ctl->q_full, r & 1, p.err, abort_flag)) break;
                 // QK of the item's first two tiles; their S buffers were last
                 // read by PVs already issued.  This overlaps the previous
                 // item's epilogue.
                 for (int t = 0; t < 2 && t < nkv; ++t) {
                     const uint32_t gk = kt + t, gs = gt + t;
-                    if (!wait_bar(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t ka = k0a + (gk % KS) * LY::KST_BYTES;
                     issue_qk<D, BN>(tS1 + (gs & 1) * BN, q1a, ka);
@@ -307,7 +322,7 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                 if (!ok) break;
                 if (nkv <= 2) mma_commit(&ctl->q_empty);
                 // the accumulators are free once the previous item's epilogue has read them
-                if (r > 0 && !wait_bar(&ctl->o_free, (r - 1) & 1, p.err, abort_flag)) break;
+                if (r > 0 && !wait_quick(&ctl->o_free, (r - 1) & 1, p.err, abort_flag)) break;
                 for (int j = 0; j < nkv; ++j) {
                     const uint32_t gs = gt + j, gv = vt + j;
                     const int bb = gs & 1;
@@ -317,19 +332,19 @@ gda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ1,
                     const uint32_t gk = kt + jn;
                     const uint32_t kan = k0a + (gk % KS) * LY::KST_BYTES;
                     // signal map: PV1(j), then QK1(j+2) into the S1 buffer PV1(j) just read
-                    if (!wait_bar(&ctl->p_full[0][bb], (gs >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
-                    if (!wait_bar(&ctl->v_full[gv % VS], (gv / VS) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->p_full[0][bb], (gs >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->v_full[gv % VS], (gv / VS) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     issue_pv<BN>(tO1, tS1 + bb * BN, va, j > 0);
                     mma_commit(&ctl->o_done[0]);
                     if (more) {
-                        if (!wait_bar(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
+                        if (!wait_quick(&ctl->k_full[gk % KS], (gk / KS) & 1, p.err, abort_flag)) { ok = false; break; }
                         tc_fence_after();
                         issue_qk<D, BN>(tS1 + bb * BN, q1a, kan);
                         mma_commit(&ctl->s_full[0][bb]);
                     }
                     // noise map: PV2(j), release V(j), then QK2(j+2) and release K(j+2)
-                    if (!wait_bar(&ctl->p_full[1][bb], (gs >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
+                    if (!wait_quick(&ctl->p_full[1][bb], (gs >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     issue_pv<BN>(tO2, tS2 + bb * BN, va, j > 0);
                     mma_commit(&ctl->o_done[1]);
