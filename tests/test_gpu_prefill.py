@@ -212,11 +212,14 @@ def test_prefill_f32_equal_maps_cancel():
 
 
 @pytest.mark.parametrize("causal", [True, False])
-def test_prefill_bf16_rising_and_falling_scores(oracle_mod, causal):
+@pytest.mark.parametrize("B,L", [(1, 600), (8, 1280)], ids=["one_head_items", "whole_group_items"])
+def test_prefill_bf16_rising_and_falling_scores(oracle_mod, causal, B, L):
     """Scores that climb ~230 log2 units along the keys (2^230 overflows float32
     unless the kernel moves its reference maximum as the row goes on) for the
-    signal map, and fall as steeply for the noise map (later keys underflow)."""
-    B, L, hs, hn, d, dv = 1, 600, 3, 1, 64, 128
+    signal map, and fall as steeply for the noise map (later keys underflow).
+    B=1, L=600 gives the grouped kernel items of one signal head; B=8, L=1280
+    (160 whole-group items) items of the whole 3-head group."""
+    hs, hn, d, dv = 3, 1, 64, 128
     g = torch.Generator().manual_seed(23)
     t = torch.linspace(-1.0, 20.0, L)
     q1 = torch.ones(B, L, hs, d) + 0.05 * torch.randn(B, L, hs, d, generator=g)
