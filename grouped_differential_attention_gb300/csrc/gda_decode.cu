@@ -545,6 +545,9 @@ gda_decode_split_kernel(const DecParams p, int stages) {
 // grid (h_s, B), block dv threads: merge the segments of one (sequence, head).
 __global__ void __launch_bounds__(256)
 gda_decode_combine_kernel(const DecParams p) {
+    // launched as a programmatic dependent of the split kernel: its launch overlaps the split
+    // kernel's tail, and this wait returns once that grid has completed with its writes visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ float red[8];
     const int h = blockIdx.x, b = blockIdx.y, col = threadIdx.x;
     const int g = h / (p.hs / p.hn);
@@ -706,8 +709,18 @@ int launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     if (e0 != cudaSuccess) return record_cuda_error(e0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return record_cuda_error(e);
-    gda_decode_combine_kernel<<<dim3(a.hs, a.B), a.dv, 0, stream>>>(p);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(a.hs, a.B);
+    cfg.blockDim = dim3(a.dv);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gda_decode_combine_kernel, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? GDA_OK : record_cuda_error(e);
 }
 
