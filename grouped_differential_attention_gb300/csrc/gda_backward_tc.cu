@@ -186,6 +186,27 @@ __device__ __forceinline__ bool warp_wait_quick(uint64_t *bar, uint32_t parity, 
     return __all_sync(0xffffffffu, wait_quick(bar, parity, err, abort));
 }
 
+// Kernels after the first are programmatic dependent launches: each sets up its barriers
+// and TMEM while the previous kernel finishes, then waits here for that grid's completion
+// (its writes visible) before reading anything it produced.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 constexpr int kEwP = 512;           // prep elementwise threads: 16 warps, four column groups
 constexpr int kThrP = 64 + kEwP;
 
@@ -232,6 +253,7 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_wait();      // the previous kernel's outputs (launched as its programmatic dependent)
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort_flag = &ctl->abort_flag;
     // TMEM: O1 [0,128) | O2 [128,256) | S1 x 2 [256,384) | S2 x 2 [384,512)
@@ -619,6 +641,7 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_wait();      // the previous kernel's outputs (launched as its programmatic dependent)
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort_flag = &ctl->abort_flag;
     // TMEM: S1^T [0,64) | S2^T [64,128) | dP^T [128,192) | dV [192,320) | dK1 [320,384) | dK2 [384,448)
@@ -971,6 +994,7 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_wait();      // the previous kernel's outputs (launched as its programmatic dependent)
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort_flag = &ctl->abort_flag;
     // TMEM: two S buffers of S1 | S2 | dP (64 columns each) at [0,192) and
@@ -1202,6 +1226,7 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
 
 // dlambda_h = -sum over (b, rows < L) of D2, in a fixed order
 __global__ void __launch_bounds__(256) gda_bwd_dlambda_kernel(const BwdTcParams p) {
+    griddep_wait();
     __shared__ float red[256];
     const int h = blockIdx.x;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight loads in flight per thread
@@ -1312,15 +1337,18 @@ int launch_backward_tc(const BackwardTcArgs &a, cudaStream_t stream) {
 
     long long gp = nqt * a.B * a.hs;
     if (gp > sms) gp = sms;
-    gda_bwd_prep_kernel<<<static_cast<unsigned>(gp), kThrP, smem_p, stream>>>(q1_128, k1_64, q2_128, k2_64, v_64, p);
+    e = launch_dependent(gda_bwd_prep_kernel, static_cast<unsigned>(gp), kThrP, smem_p, stream, q1_128, k1_64,
+                         q2_128, k2_64, v_64, p);
     long long gkv = nqt * a.B * a.hn;
     if (gkv > sms) gkv = sms;
-    gda_bwd_dkdv_kernel<<<static_cast<unsigned>(gkv), kThrKv, smem_kv, stream>>>(k1_128, k2_128, v_128, q1_64, q2_64,
-                                                                               do_64, p);
-    gda_bwd_dq_kernel<<<static_cast<unsigned>(gkv), kThrQ, smem_q, stream>>>(q1_128, q2_128, do_128, k1_64, k2_64,
-                                                                            v_64, p);
-    gda_bwd_dlambda_kernel<<<a.hs, 256, 0, stream>>>(p);
-    e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = launch_dependent(gda_bwd_dkdv_kernel, static_cast<unsigned>(gkv), kThrKv, smem_kv, stream, k1_128,
+                             k2_128, v_128, q1_64, q2_64, do_64, p);
+    if (e == cudaSuccess)
+        e = launch_dependent(gda_bwd_dq_kernel, static_cast<unsigned>(gkv), kThrQ, smem_q, stream, q1_128, q2_128,
+                             do_128, k1_64, k2_64, v_64, p);
+    if (e == cudaSuccess) e = launch_dependent(gda_bwd_dlambda_kernel, a.hs, 256, 0, stream, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? GDA_OK : record_cuda_error(e);
 }
 
