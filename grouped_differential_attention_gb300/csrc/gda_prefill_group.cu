@@ -220,9 +220,9 @@ __device__ __forceinline__ void regs_inc() {
 // lanes): no warp-level synchronisation and no single-lane branch on the hot path.
 __device__ __forceinline__ void lanes_arrive(uint64_t *bar) { mbar_arrive(bar); }
 
-// Bounded wait without the suspend-time hint: a wait whose phase has already
-// completed costs about a third as much as the hinted form, which matters on
-// the single MMA-issuing thread.
+// Bounded wait that first polls once without the suspend-time hint (a wait whose phase
+// has already completed costs about a third as much as the hinted form), then takes the
+// bounded hinted wait.
 __device__ __forceinline__ bool wait_fast(uint64_t *bar, uint32_t parity, unsigned *err, volatile int *abort) {
     const uint32_t a = smem_u32(bar);
     uint32_t ok;
