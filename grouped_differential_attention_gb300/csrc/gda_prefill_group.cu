@@ -52,6 +52,9 @@
 //   warps 4-19  compute (thread = query row = TMEM lane; warp w takes keys
 //               [32 k, 32 k + 32) of each tile, k = (w - 4) / 4: four compute
 //               warps per SM sub-partition): statistics, P, and the epilogue.
+// Epilogue: items of at most kStageOutTiles key tiles stage the output rows in the
+// P buffers and write them with TMA stores (one thread per row quarter); longer
+// items, where the epilogue is a small share, store each thread's row segment.
 // Every mbarrier wait is bounded (1 s) and sets GDA_DEVERR_PREFILL_TIMEOUT.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -69,6 +72,7 @@ namespace gda {
 namespace {
 
 constexpr int kGBN = 128;              // keys per logit tile
+constexpr int kStageOutTiles = 32;     // longest item (key tiles) that takes the staged epilogue
 constexpr int kPH = 64;                // keys per P half / V tile
 #ifndef GDA_GROUP_KEYS_PER_THREAD
 #define GDA_GROUP_KEYS_PER_THREAD 32
@@ -262,11 +266,12 @@ __device__ __forceinline__ bool warp_wait_fast(uint64_t *bar, uint32_t parity, u
     return __all_sync(0xffffffffu, wait_fast(bar, parity, err, abort));
 }
 
-template <int S>
+template <int S, bool kStageOut>
 __global__ void __launch_bounds__(kGThreads, 1)
 gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CUtensorMap tmK1,
                          const __grid_constant__ CUtensorMap tmQ2, const __grid_constant__ CUtensorMap tmK2,
-                         const __grid_constant__ CUtensorMap tmV, const GParams p) {
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                         const GParams p) {
     using LY = GLayout<S>;
     constexpr int NB = LY::NB, LAG = LY::LAG, NR = LY::NR;
     constexpr int M = S + 1;                 // maps per item: noise map (0), signal heads (1..S)
@@ -322,6 +327,7 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             tma_prefetch_desc(&tmQ2);
             tma_prefetch_desc(&tmK2);
             tma_prefetch_desc(&tmV);
+            if constexpr (kStageOut) tma_prefetch_desc(&tmO);
             uint32_t ct = 0;
             int nq = 0;
             bool ok = true;
@@ -651,7 +657,13 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                 stats_tile(0, kYes, kYes);
             }
             for (int j = jfull > 1 ? jfull : 1; j < it.nkv; ++j) stats_tile(j, kNo, kYes);
-            // combine the four key quarters of the row: lse = max + log2(sum), base 2
+            // combine the four key quarters of the row: lse = max + log2(sum), base 2; the
+            // exchange (P buffer 0) is written once the previous item's output stores have read
+            // the P buffers
+            if (kStageOut && rr > 0) {
+                if (kq == 0 && lane == 0) bulk_wait_group_read<0>();
+                named_bar_sync(row_bar, kRowThreads);
+            }
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 xslot(xrow_a, kq * 8 + m) = mx[m];
@@ -754,36 +766,116 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             }
             named_bar_sync(row_bar, kRowThreads);
             ok = __all_sync(0xffffffffu, ok);
+            if constexpr (kStageOut) {
+                float yscale[S];
 #pragma unroll
-            for (int h = 0; h < S; ++h) {
-                float ss_tot = 0.f;
+                for (int h = 0; h < S; ++h) {
+                    float ss_tot = 0.f;
 #pragma unroll
-                for (int q = 0; q < kNQ; ++q) ss_tot += xslot(xrow_b, q * 4 + h);
-                const float yscale = p.no_norm ? 1.f : (1.f - p.lambda_init) * rsqrtf(ss_tot / 128.f + p.eps);
-                if (ok) {
+                    for (int q = 0; q < kNQ; ++q) ss_tot += xslot(xrow_b, q * 4 + h);
+                    yscale[h] = p.no_norm ? 1.f : (1.f - p.lambda_init) * rsqrtf(ss_tot / 128.f + p.eps);
+                }
+                // The row quarter's output tile of head h is staged in P buffer 1 (h even) or 0 (h odd),
+                // in the same 128-byte-swizzled halves as a P tile, and written by two TMA stores of
+                // 32 rows x 64 columns issued by one thread of the quarter (rows past L are clipped).
+                // Per-thread row stores would send each warp instruction to 32 different cache lines.
+                named_bar_sync(row_bar, kRowThreads);   // the exchange has been read: buffer 0 is free
+                const bool leader = kq == 0 && lane == 0;
+                const bool rows_in = it.q0 + quarter * 32 < p.L;
+                // head h's kKQ columns of this thread, normalised and packed to bf16
+                auto pack = [&](int h, uint32_t (&pko)[kKQ / 2]) {
 #pragma unroll
                     for (int c = 0; c < kKQ / 32; ++c) {
                         uint32_t o[32];
-                        tmem_ld32(tmem + lane_off + 128 * h + kq * kKQ + c * 32, o);
-                        tmem_ld_wait_regs(o);
-                        uint32_t pko[16];
+                        if (ok) {
+                            tmem_ld32(tmem + lane_off + 128 * h + kq * kKQ + c * 32, o);
+                            tmem_ld_wait_regs(o);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = 0u;
+                        }
 #pragma unroll
                         for (int e = 0; e < 32; e += 2)
-                            pko[e / 2] = pack_bf16x2(__uint_as_float(o[e]) * yscale, __uint_as_float(o[e + 1]) * yscale);
-                        if (in) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(
-                                p.out + ((static_cast<size_t>(it.b) * p.L + qrow) * p.hs + it.h0 + h) * 128 + kq * kKQ +
-                                c * 32);
+                            pko[c * 16 + e / 2] =
+                                pack_bf16x2(__uint_as_float(o[e]) * yscale[h], __uint_as_float(o[e + 1]) * yscale[h]);
+                    }
+                };
+                auto put = [&](int h, const uint32_t (&pko)[kKQ / 2]) {
+                    uint8_t *prow = pbuf0 + ((h & 1) ? 0 : 2 * LY::PH_BYTES);
 #pragma unroll
-                            for (int v4 = 0; v4 < 4; ++v4)
-                                dst[v4] = make_uint4(pko[4 * v4], pko[4 * v4 + 1], pko[4 * v4 + 2], pko[4 * v4 + 3]);
+                    for (int v4 = 0; v4 < kKQ / 8; ++v4)
+                        *reinterpret_cast<uint4 *>(prow + (((chunk0 + v4) ^ (row & 7)) << 4)) =
+                            make_uint4(pko[4 * v4], pko[4 * v4 + 1], pko[4 * v4 + 2], pko[4 * v4 + 3]);
+                };
+                auto store = [&](int h) {
+                    if (!leader || !ok || !rows_in) return;
+                    const uint8_t *src = smem + LY::OFF_P + ((h & 1) ? 0 : 2 * LY::PH_BYTES) + quarter * 32 * 128;
+                    tma_store_4d(&tmO, src, 0, it.h0 + h, it.q0 + quarter * 32, it.b);
+                    tma_store_4d(&tmO, src + LY::PH_BYTES, kPH, it.h0 + h, it.q0 + quarter * 32, it.b);
+                    bulk_commit_group();
+                };
+                {
+                    uint32_t pko[kKQ / 2];
+                    pack(0, pko);
+                    put(0, pko);
+                    if constexpr (S > 1) {
+                        pack(1, pko);
+                        put(1, pko);
+                    }
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(row_bar, kRowThreads);
+                store(0);
+                if constexpr (S > 1) store(1);
+                uint32_t pk2[kKQ / 2];
+                if constexpr (S > 2) pack(2, pk2);
+                // the accumulators may now be overwritten by the next item's first value MMA
+                tc_fence_before();
+                lanes_arrive(&ctl->o_free);
+                if constexpr (S > 2) {
+                    if (leader) bulk_wait_group_read<1>();   // head 0's store has read buffer 1
+                    named_bar_sync(row_bar, kRowThreads);
+                    put(2, pk2);
+                    fence_proxy_async_smem();
+                    named_bar_sync(row_bar, kRowThreads);
+                    store(2);
+                }
+            } else {
+                // short epilogue for long items: each thread stores its own row segments
+#pragma unroll
+                for (int h = 0; h < S; ++h) {
+                    float ss_tot = 0.f;
+#pragma unroll
+                    for (int q = 0; q < kNQ; ++q) ss_tot += xslot(xrow_b, q * 4 + h);
+                    const float yscale =
+                        p.no_norm ? 1.f : (1.f - p.lambda_init) * rsqrtf(ss_tot / 128.f + p.eps);
+                    if (ok) {
+#pragma unroll
+                        for (int c = 0; c < kKQ / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tmem + lane_off + 128 * h + kq * kKQ + c * 32, o);
+                            tmem_ld_wait_regs(o);
+                            uint32_t pko[16];
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2)
+                                pko[e / 2] =
+                                    pack_bf16x2(__uint_as_float(o[e]) * yscale, __uint_as_float(o[e + 1]) * yscale);
+                            if (in) {
+                                uint4 *dst = reinterpret_cast<uint4 *>(
+                                    p.out + ((static_cast<size_t>(it.b) * p.L + qrow) * p.hs + it.h0 + h) * 128 +
+                                    kq * kKQ + c * 32);
+#pragma unroll
+                                for (int v4 = 0; v4 < 4; ++v4)
+                                    dst[v4] =
+                                        make_uint4(pko[4 * v4], pko[4 * v4 + 1], pko[4 * v4 + 2], pko[4 * v4 + 3]);
+                            }
                         }
                     }
                 }
+                // the accumulators may now be overwritten by the next item's first value MMA
+                tc_fence_before();
+                lanes_arrive(&ctl->o_free);
             }
-            // the accumulators may now be overwritten by the next item's first value MMA
-            tc_fence_before();
-            lanes_arrive(&ctl->o_free);
             // the four warps of the row agree on whether to go on (rows share no named
             // barrier); this also orders the reads of the exchange above before the next
             // item's writes
@@ -791,6 +883,8 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
         }
     }
 
+    // the store leaders (the first warp of each row quarter's column parts): stores complete
+    if (kStageOut && warp >= kGCtrlWarps && warp < kGCtrlWarps + 4 && lane == 0) bulk_wait_group0();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -807,9 +901,9 @@ int heads_per_item(int r) {
     return 1;
 }
 
-template <int S>
+template <int S, bool kStageOut>
 int launch_group_impl(const PrefillArgs &a, cudaStream_t stream) {
-    CUtensorMap mQ1, mK1, mQ2, mK2, mV;
+    CUtensorMap mQ1, mK1, mQ2, mK2, mV, mO;
     const uint64_t B = a.B, L = a.L, Lk = a.Lk > 0 ? a.Lk : a.L, hs = a.hs, hn = a.hn;
     {
         const uint64_t dq[4] = {64, hs, L, B}, dk[4] = {64, hs, Lk, B};
@@ -830,6 +924,12 @@ int launch_group_impl(const PrefillArgs &a, cudaStream_t stream) {
         const uint64_t sv[3] = {256, hs * 256, Lk * hs * 256};
         const uint32_t box[4] = {64, 1, kPH, 1};
         if (!encode_tmap_4d_bf16(&mV, a.v, dv4, sv, box)) return GDA_ERR_CUDA;
+    }
+    {
+        const uint64_t dout[4] = {128, hs, L, B};
+        const uint64_t so[3] = {256, hs * 256, L * hs * 256};
+        const uint32_t box[4] = {kPH, 1, 32, 1};
+        if (!encode_tmap_4d_bf16(&mO, a.out, dout, so, box)) return GDA_ERR_CUDA;
     }
     GParams p;
     p.lambda = a.lambda;
@@ -854,7 +954,7 @@ int launch_group_impl(const PrefillArgs &a, cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return record_cuda_error(e);
-    auto kern = gda_prefill_group_kernel<S>;
+    auto kern = gda_prefill_group_kernel<S, kStageOut>;
     constexpr int smem = group_smem_bytes<S>();
     static_assert(smem <= 232448, "shared memory budget");
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -869,7 +969,7 @@ int launch_group_impl(const PrefillArgs &a, cudaStream_t stream) {
     if (nitems <= 0 || nitems > 0x7fffffffLL) return GDA_ERR_UNSUPPORTED;
     long long grid = sms;
     if (grid > nitems) grid = nitems;
-    kern<<<static_cast<unsigned>(grid), kGThreads, smem, stream>>>(mQ1, mK1, mQ2, mK2, mV, p);
+    kern<<<static_cast<unsigned>(grid), kGThreads, smem, stream>>>(mQ1, mK1, mQ2, mK2, mV, mO, p);
     e = cudaGetLastError();
     return e == cudaSuccess ? GDA_OK : record_cuda_error(e);
 }
@@ -891,10 +991,15 @@ int launch_prefill_group(const PrefillArgs &a, cudaStream_t stream) {
         const long long nqt = (a.L + kBM - 1) / kBM;
         if (2 * nqt * a.B * (a.hs / S) < sms) S = 1;
     }
+    // Items of at most kStageOutTiles key tiles end in the staged epilogue (TMA stores of the
+    // output): there the epilogue is a large share of an item.  Longer items keep the per-row
+    // stores, which drain while the next item's statistics sweep runs.
+    const long long Lk = a.Lk > 0 ? a.Lk : a.L;
+    const bool staged = (Lk + kGBN - 1) / kGBN <= kStageOutTiles;
     switch (S) {
-        case 3: return launch_group_impl<3>(a, stream);
-        case 2: return launch_group_impl<2>(a, stream);
-        default: return launch_group_impl<1>(a, stream);
+        case 3: return staged ? launch_group_impl<3, true>(a, stream) : launch_group_impl<3, false>(a, stream);
+        case 2: return staged ? launch_group_impl<2, true>(a, stream) : launch_group_impl<2, false>(a, stream);
+        default: return staged ? launch_group_impl<1, true>(a, stream) : launch_group_impl<1, false>(a, stream);
     }
 }
 

@@ -10,14 +10,17 @@ signal heads per item and ragged item lengths, and checks on every schedule that
 - every wait names a phase at most one ahead of the barrier's completed phases (a
   parity wait cannot tell phase k from phase k + 2);
 - no asynchronous write (TMA into a ring slot, a logit MMA into a TMEM slot, a value MMA
-  into an accumulator) overlaps another access to the same storage, and no P tile or
-  row-exchange word is written while a value MMA reads its buffer.
+  into an accumulator) overlaps another access to the same storage, and no P tile,
+  row-exchange word or staged output row is written while a value MMA or an output TMA
+  store reads its buffer.
 
 The model mirrors the kernel's loops: slot assignment of the statistics sweep, the one
 K / V ring consumed in order by two issuers that skip each other's entries, the P
 buffers [buffer][half], the per-row exchange in the row's own bytes of P buffer 0, and
-the per-item barriers (q_full / q_empty, o_final / o_free).  Compute warps are modelled
-as units of two row quarters x four key quarters.
+the per-item barriers (q_full / q_empty, o_final / o_free), and both epilogues: per-row
+output stores (items longer than 32 key tiles) and the staged one, whose output rows go
+through the P buffers to TMA stores issued by one thread of each row quarter.  Compute
+warps are modelled as units of two row quarters x four key quarters.
 """
 import random
 
@@ -47,14 +50,17 @@ class Bar:
 
 def compatible(k1, k2):
     """May two accesses to the same storage overlap in time?  Kinds: "r" (read), "w"
-    (exclusive write), "pw" (compute warps writing their own chunks of P rows), "ex" (the
-    row exchange's words) and ("mma", issuer, "r" | "w") for an MMA between its issue and
-    its completion: one issuer's MMAs run in order, two issuers' MMAs are unordered."""
+    (exclusive write), "pw" (compute warps writing their own chunks of P rows or staged
+    output rows), "ex" (the row exchange's words), "ar" (an output TMA store reading staged
+    rows) and ("mma", issuer, "r" | "w") for an MMA between its issue and its completion:
+    one issuer's MMAs run in order, two issuers' MMAs are unordered."""
     if isinstance(k1, tuple) and isinstance(k2, tuple):
         return k1[1] == k2[1] or (k1[2] == "r" and k2[2] == "r")
     if isinstance(k1, tuple) or isinstance(k2, tuple):
         m, o = (k1, k2) if isinstance(k1, tuple) else (k2, k1)
-        return m[2] == "r" and o == "r"
+        return m[2] == "r" and o in ("r", "ar")
+    if "ar" in (k1, k2):
+        return k1 in ("r", "ar") and k2 in ("r", "ar")
     return k1 == k2 and k1 in ("r", "pw", "ex")
 
 
@@ -75,12 +81,15 @@ class Storage:
         self.active[key].remove((kind, owner))
 
 
-def simulate(S, items, seed, skip_p_empty_wait=False, exchange_over_all_rows=False, skip_logit_o_free=False):
-    """Runs one random schedule.  The keyword switches plant protocol errors (for the
+def simulate(S, items, seed, staged=False, skip_p_empty_wait=False, exchange_over_all_rows=False,
+             skip_logit_o_free=False, skip_store_wait=False):
+    """Runs one random schedule (`staged`: the epilogue that stages the output in the P
+    buffers for TMA stores).  The other keyword switches plant protocol errors (for the
     checker's own tests): compute warps that do not wait for p_empty, a row exchange
     spread over every row of the P buffer (each quarter's words in all quarters' rows),
     a logit issuer that writes the accumulator columns in the statistics sweep without
-    waiting for the previous item's epilogue."""
+    waiting for the previous item's epilogue, a store leader that does not wait for its
+    TMA stores to read a buffer before it is written again."""
     M, NB = S + 1, 4 - S
     LAG = NB + 1
     rng = random.Random(seed)
@@ -285,6 +294,29 @@ def simulate(S, items, seed, skip_p_empty_wait=False, exchange_over_all_rows=Fal
         half = kq * 2 // KQ
         cnt = [0] * 4
         pk = 0
+        leader = kq == 0
+        groups = []                          # the leader's store groups: [done flag]
+        tag = "X" if half == 0 else "Y"
+
+        def store(pb):
+            """one bulk group: TMA stores of both halves of the quarter's rows of buffer pb"""
+            keys = [("X", pb, quarter), ("Y", pb, quarter)]
+            for key in keys:
+                mem.begin(key, "ar", f"st{quarter}")
+            g = [False]
+            groups.append(g)
+
+            def done():
+                for key in keys:
+                    mem.end(key, "ar", f"st{quarter}")
+                g[0] = True
+            later(rng.randint(1, 80), done)
+
+        def wait_read(n):
+            """cp.async.bulk.wait_group.read n: every group but the n most recent has read"""
+            if skip_store_wait:
+                return
+            yield ("cond", lambda: all(g[0] for g in groups[:len(groups) - n]))
 
         def acquire(slot):
             k = cnt[slot]
@@ -308,7 +340,12 @@ def simulate(S, items, seed, skip_p_empty_wait=False, exchange_over_all_rows=Fal
                     yield from acquire(slot)
                     yield from math()
                     release(slot)
-            # row exchange in this quarter's rows of P buffer 0, half 0
+            # row exchange in this quarter's rows of P buffer 0, half 0 (staged: once the
+            # previous item's output stores have read the P buffers)
+            if staged and rr > 0:
+                if leader:
+                    yield from wait_read(0)
+                yield ("bar", quarter)
             xq = range(QUARTERS) if exchange_over_all_rows else [quarter]
             for q in xq:
                 mem.begin(("X", 0, q), "ex", me)
@@ -348,10 +385,36 @@ def simulate(S, items, seed, skip_p_empty_wait=False, exchange_over_all_rows=Fal
             yield from math()
             for q in xq:
                 mem.end(("Y", 0, q), "ex", me)
+            if staged:
+                # heads 0 and 2 staged in P buffer 1, head 1 in buffer 0 (this unit's half of
+                # the quarter's rows); the leader stores them after the quarter's barrier
+                yield ("bar", quarter)
+                for h in range(min(S, 2)):
+                    key = (tag, 1 - h % 2, quarter)
+                    mem.begin(key, "pw", me)
+                    yield from math()
+                    mem.end(key, "pw", me)
+                yield ("bar", quarter)
+                if leader:
+                    for h in range(min(S, 2)):
+                        store(1 - h % 2)
             for h in range(S):
                 mem.end(("T", h), "r", me)
             bars["o_free"].arrive(1)
+            if staged and S > 2:
+                if leader:
+                    yield from wait_read(1)
+                yield ("bar", quarter)
+                key = (tag, 1, quarter)
+                mem.begin(key, "pw", me)
+                yield from math()
+                mem.end(key, "pw", me)
+                yield ("bar", quarter)
+                if leader:
+                    store(1)
             yield ("bar", quarter)
+        if staged and leader:
+            yield from wait_read(0)
 
     # The P-buffer rows a quarter's units write (and its exchange words) conflict with a value
     # MMA that reads the whole buffer: map the MMA's read of ("P", pb, half) onto every quarter.
@@ -398,6 +461,9 @@ def simulate(S, items, seed, skip_p_empty_wait=False, exchange_over_all_rows=Fal
             elif op[0] == "bar":
                 if bar_gen[op[1]] > bar_mine[name]:
                     runnable.append(name)
+            elif op[0] == "cond":
+                if op[1]():
+                    runnable.append(name)
         if not runnable or (events and rng.random() < 0.3):
             if not events:
                 wake = [blocked[n][1] for n in roles if n not in done and blocked[n] and blocked[n][0] == "sleep"]
@@ -431,15 +497,17 @@ def simulate(S, items, seed, skip_p_empty_wait=False, exchange_over_all_rows=Fal
     return steps
 
 
+@pytest.mark.parametrize("staged", [False, True], ids=["row_stores", "staged_stores"])
 @pytest.mark.parametrize("S", [1, 2, 3])
-def test_group_protocol_random_schedules(S):
+def test_group_protocol_random_schedules(S, staged):
     rng = random.Random(100 + S)
     for seed in range(40):
         items = [rng.randint(1, 7) for _ in range(rng.randint(1, 4))]
-        simulate(S, items, seed=1000 * S + seed)
+        simulate(S, items, seed=1000 * S + seed, staged=staged)
 
 
-@pytest.mark.parametrize("mutation", ["skip_p_empty_wait", "exchange_over_all_rows", "skip_logit_o_free"])
+@pytest.mark.parametrize("mutation", ["skip_p_empty_wait", "exchange_over_all_rows", "skip_logit_o_free",
+                                      "skip_store_wait"])
 def test_group_protocol_checker_catches_planted_errors(mutation):
     """The checker itself: each planted protocol error must fail on some schedule
     (the exchange spread over all rows is the layout that let a fast row quarter's P
@@ -448,7 +516,7 @@ def test_group_protocol_checker_catches_planted_errors(mutation):
     for seed in range(90):
         S = 1 + seed % 3
         try:
-            simulate(S, [1, 2, 1, 3, 1], seed, **{mutation: True})
+            simulate(S, [1, 2, 1, 3, 1], seed, staged=mutation == "skip_store_wait", **{mutation: True})
         except AssertionError:
             caught += 1
     assert caught > 0
