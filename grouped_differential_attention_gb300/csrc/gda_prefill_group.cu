@@ -417,10 +417,12 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
             auto qk = [&](int m, uint32_t slot, bool spin) -> bool {
                 const uint32_t k = bump(cnt, slot);
                 if (slot < static_cast<uint32_t>(S) && !need_o()) return false;
+                // the K tile is nearly always in the ring by now: its wait comes first, so that
+                // only the slot's release stands between that release and the MMA
+                if (!wait_fast(&ctl->r_full[rp.st], rp.ph, p.err, abort_flag)) return false;
                 if (k >= 1 && !(spin ? wait_spin(&ctl->s_free[slot], (k - 1) & 1, p.err, abort_flag)
                                      : wait_fast(&ctl->s_free[slot], (k - 1) & 1, p.err, abort_flag)))
                     return false;
-                if (!wait_fast(&ctl->r_full[rp.st], rp.ph, p.err, abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t qlo = qlo0 + m * (LY::Q_BYTES >> 4), klo = klo0 + rp.st * (LY::R_BYTES >> 4);
 #pragma unroll

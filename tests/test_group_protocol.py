@@ -224,10 +224,10 @@ def simulate(S, items, seed, staged=False, skip_p_empty_wait=False, exchange_ove
                     o_ready = True
                     if nitem > 0 and not skip_logit_o_free:
                         yield W("o_free", nitem - 1)
-                if k >= 1:
-                    yield W(f"s_free{slot}", k - 1)
                 st = ct % NR
                 yield W(f"r_full{st}", ct // NR)
+                if k >= 1:
+                    yield W(f"s_free{slot}", k - 1)
                 mma("qk", [(("T", slot), "w"), (("Q", m), "r"), (("R", st), "r")], rng.randint(4, 20))
                 commit("qk", f"s_full{slot}")
                 commit("qk", f"r_empty{st}")
