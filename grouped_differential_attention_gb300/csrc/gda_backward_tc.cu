@@ -41,6 +41,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 #include <cmath>
+#include <type_traits>
 
 #include "gda.h"
 #include "gda_device.cuh"
@@ -421,25 +422,31 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
                 tmem_ld_wait_regs16(r1);
                 reg_fence16(r2);
                 const int k0 = j * kN + grp * 16;
-                const bool need_mask = k0 + 15 > last_key;
                 uint32_t pk1[8], pk2[8];
+                auto probs = [&](auto masked) {
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    float x0 = __uint_as_float(r1[e]), x1 = __uint_as_float(r1[e + 1]);
-                    float y0 = __uint_as_float(r2[e]), y1 = __uint_as_float(r2[e + 1]);
-                    ffma2(x0, x1, sl2, sl2, neg1, neg1);
-                    ffma2(y0, y1, sl2, sl2, neg2, neg2);
-                    x0 = fast_exp2(x0);
-                    x1 = fast_exp2(x1);
-                    y0 = fast_exp2(y0);
-                    y1 = fast_exp2(y1);
-                    if (need_mask) {
-                        if (k0 + e > last_key) x0 = y0 = 0.f;
-                        if (k0 + e + 1 > last_key) x1 = y1 = 0.f;
+                    for (int e = 0; e < 16; e += 2) {
+                        float x0 = __uint_as_float(r1[e]), x1 = __uint_as_float(r1[e + 1]);
+                        float y0 = __uint_as_float(r2[e]), y1 = __uint_as_float(r2[e + 1]);
+                        ffma2(x0, x1, sl2, sl2, neg1, neg1);
+                        ffma2(y0, y1, sl2, sl2, neg2, neg2);
+                        x0 = fast_exp2(x0);
+                        x1 = fast_exp2(x1);
+                        y0 = fast_exp2(y0);
+                        y1 = fast_exp2(y1);
+                        if constexpr (decltype(masked)::value) {
+                            if (k0 + e > last_key) x0 = y0 = 0.f;
+                            if (k0 + e + 1 > last_key) x1 = y1 = 0.f;
+                        }
+                        pk1[e / 2] = pack_bf16x2(x0, x1);
+                        pk2[e / 2] = pack_bf16x2(y0, y1);
                     }
-                    pk1[e / 2] = pack_bf16x2(x0, x1);
-                    pk2[e / 2] = pack_bf16x2(y0, y1);
-                }
+                };
+                // the per-key test only where some row of the warp has keys past its last one
+                if (__any_sync(0xffffffffu, k0 + 15 > last_key))
+                    probs(std::true_type{});
+                else
+                    probs(std::false_type{});
                 tmem_st8(tS1, pk1);
                 tmem_st8(tS2, pk2);
                 tmem_st_wait();
@@ -811,32 +818,45 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
                     // every (key, query) pair of this warp and group is visible: no per-element mask
                     const bool clean = q0 + 15 < p.L && wkey_last < p.L && (!p.causal || wkey_last <= q0);
                     uint32_t pw[8], pd1[8], pd2[8];
+                    // W = a1 - lambda a2, dS1 = a1 (dP - D1), dS2 = -lambda a2 (dP - D2) for
+                    // pairs of query columns in packed float32 arithmetic; the per-pair
+                    // visibility test only in the masked instance
+                    auto pairs = [&](auto masked) {
 #pragma unroll
-                    for (int e = 0; e < 16; e += 2) {
-                        float w2[2], a2[2], c2[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const float p1 = fast_exp2(fmaf(__uint_as_float(s1[e + u]), sl2, -vec[e + u]));
-                            const float np2 = nlam * fast_exp2(fmaf(__uint_as_float(s2[e + u]), sl2, -vec[64 + e + u]));
-                            const float dpv = __uint_as_float(dp[e + u]);
-                            w2[u] = p1 + np2;
-                            a2[u] = p1 * (dpv - vec[128 + e + u]);
-                            c2[u] = np2 * (dpv - vec[192 + e + u]);
-                        }
-                        if (!clean) {
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int q = q0 + e + u;
-                                const bool vis = q < p.L && key < p.L && (!p.causal || key <= q);
-                                w2[u] = vis ? w2[u] : 0.f;
-                                a2[u] = vis ? a2[u] : 0.f;
-                                c2[u] = vis ? c2[u] : 0.f;
+                        for (int e = 0; e < 16; e += 2) {
+                            const float p1a = fast_exp2(fmaf(__uint_as_float(s1[e]), sl2, -vec[e]));
+                            const float p1b = fast_exp2(fmaf(__uint_as_float(s1[e + 1]), sl2, -vec[e + 1]));
+                            float n2a = fast_exp2(fmaf(__uint_as_float(s2[e]), sl2, -vec[64 + e]));
+                            float n2b = fast_exp2(fmaf(__uint_as_float(s2[e + 1]), sl2, -vec[64 + e + 1]));
+                            fmul2(n2a, n2b, nlam, nlam);
+                            float wa = p1a, wb = p1b;
+                            fadd2(wa, wb, n2a, n2b);
+                            float ta = __uint_as_float(dp[e]), tb = __uint_as_float(dp[e + 1]);
+                            float ua = ta, ub = tb;
+                            fsub2(ta, tb, vec[128 + e], vec[128 + e + 1]);
+                            fsub2(ua, ub, vec[192 + e], vec[192 + e + 1]);
+                            fmul2(ta, tb, p1a, p1b);
+                            fmul2(ua, ub, n2a, n2b);
+                            if constexpr (decltype(masked)::value) {
+                                const int q = q0 + e;
+                                const bool va = q < p.L && key < p.L && (!p.causal || key <= q);
+                                const bool vb = q + 1 < p.L && key < p.L && (!p.causal || key <= q + 1);
+                                wa = va ? wa : 0.f;
+                                ta = va ? ta : 0.f;
+                                ua = va ? ua : 0.f;
+                                wb = vb ? wb : 0.f;
+                                tb = vb ? tb : 0.f;
+                                ub = vb ? ub : 0.f;
                             }
+                            pw[e / 2] = pack_bf16x2(wa, wb);
+                            pd1[e / 2] = pack_bf16x2(ta, tb);
+                            pd2[e / 2] = pack_bf16x2(ua, ub);
                         }
-                        pw[e / 2] = pack_bf16x2(w2[0], w2[1]);
-                        pd1[e / 2] = pack_bf16x2(a2[0], a2[1]);
-                        pd2[e / 2] = pack_bf16x2(c2[0], c2[1]);
-                    }
+                    };
+                    if (clean)
+                        pairs(std::false_type{});
+                    else
+                        pairs(std::true_type{});
                     // the previous tile's products have read W / dS1 / dS2
                     if (gq > 0 && !warp_wait_quick(&ctl->w_free, (gq - 1) & 1, p.err, abort_flag)) {
                         ok = false;
@@ -1162,28 +1182,38 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                     // every (query, key) pair of this warp and group is visible: no per-element mask
                     const bool clean = wrow_first + 31 < p.L && kc0 + 15 < p.L && (!p.causal || kc0 + 15 <= wrow_first);
                     uint32_t pd1[8], pd2[8];
+                    // dS1 = a1 (dP - D1), dS2 = -lambda a2 (dP - D2) for pairs of key columns in
+                    // packed float32 arithmetic; the visibility test only in the masked instance
+                    auto pairs = [&](auto masked) {
 #pragma unroll
-                    for (int e = 0; e < 16; e += 2) {
-                        float a2[2], c2[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const float p1 = fast_exp2(fmaf(__uint_as_float(s1[e + u]), sl2, nlse1));
-                            const float np2 = nlam * fast_exp2(fmaf(__uint_as_float(s2[e + u]), sl2, nlse2));
-                            const float dpv = __uint_as_float(dp[e + u]);
-                            a2[u] = p1 * (dpv - D1);
-                            c2[u] = np2 * (dpv - D2);
-                        }
-                        if (!clean) {
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const bool vis = in && kc0 + e + u <= last_key;
-                                a2[u] = vis ? a2[u] : 0.f;
-                                c2[u] = vis ? c2[u] : 0.f;
+                        for (int e = 0; e < 16; e += 2) {
+                            const float p1a = fast_exp2(fmaf(__uint_as_float(s1[e]), sl2, nlse1));
+                            const float p1b = fast_exp2(fmaf(__uint_as_float(s1[e + 1]), sl2, nlse1));
+                            float n2a = fast_exp2(fmaf(__uint_as_float(s2[e]), sl2, nlse2));
+                            float n2b = fast_exp2(fmaf(__uint_as_float(s2[e + 1]), sl2, nlse2));
+                            fmul2(n2a, n2b, nlam, nlam);
+                            float ta = __uint_as_float(dp[e]), tb = __uint_as_float(dp[e + 1]);
+                            float ua = ta, ub = tb;
+                            fsub2(ta, tb, D1, D1);
+                            fsub2(ua, ub, D2, D2);
+                            fmul2(ta, tb, p1a, p1b);
+                            fmul2(ua, ub, n2a, n2b);
+                            if constexpr (decltype(masked)::value) {
+                                const bool va = in && kc0 + e <= last_key;
+                                const bool vb = in && kc0 + e + 1 <= last_key;
+                                ta = va ? ta : 0.f;
+                                ua = va ? ua : 0.f;
+                                tb = vb ? tb : 0.f;
+                                ub = vb ? ub : 0.f;
                             }
+                            pd1[e / 2] = pack_bf16x2(ta, tb);
+                            pd2[e / 2] = pack_bf16x2(ua, ub);
                         }
-                        pd1[e / 2] = pack_bf16x2(a2[0], a2[1]);
-                        pd2[e / 2] = pack_bf16x2(c2[0], c2[1]);
-                    }
+                    };
+                    if (clean)
+                        pairs(std::false_type{});
+                    else
+                        pairs(std::true_type{});
                     tmem_st8(sb + tS1, pd1);
                     tmem_st8(sb + tS2, pd2);
                     tmem_st_wait();

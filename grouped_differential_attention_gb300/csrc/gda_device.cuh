@@ -369,6 +369,28 @@ __device__ __forceinline__ void ffma2_acc(float &d0, float &d1, float a0, float 
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// (a0, a1) -= (b0, b1) as one packed sub.f32x2.
+__device__ __forceinline__ void fsub2(float &a0, float &a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 x, y;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mov.b64 y, {%2, %3};\n\t"
+        "sub.f32x2 x, x, y;\n\t"
+        "mov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+
+// (a0, a1) *= (b0, b1) as one packed mul.f32x2.
+__device__ __forceinline__ void fmul2(float &a0, float &a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 x, y;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mov.b64 y, {%2, %3};\n\t"
+        "mul.f32x2 x, x, y;\n\t"
+        "mov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+
 // (a0, a1) += (b0, b1) as one packed add.f32x2.
 __device__ __forceinline__ void fadd2(float &a0, float &a1, float b0, float b1) {
     asm("{\n\t.reg .b64 x, y;\n\t"
