@@ -106,6 +106,17 @@ def test_prefill_3to1_workload_every_element(oracle_mod):
     assert_bf16_close(got, ref, w.name)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_whole_group_items_ragged_tail(oracle_mod, causal):
+    """Items of the whole 3-head group (B=8, L=1200: 160 items) with the output staged for
+    TMA stores; the last query tile holds 48 rows, so one row quarter's store is clipped at
+    L and two quarters have no rows at all."""
+    inp = W.make_prefill_inputs(W.GDA3_PREFILL_L2048, B=8, L=1200, h_s=3, h_n=1, seed=1201)
+    got = run_bf16(inp, 0.8, causal)
+    ref = oracle_mod.prefill(*inp, 0.8, causal=causal)
+    assert_bf16_close(got, ref, "whole-group items, ragged tail")
+
+
 @pytest.mark.parametrize("w", [W.GDA4_PREFILL_L8192, W.GDA3_PREFILL_L32768], ids=lambda x: x.name)
 def test_prefill_full_size_sampled_rows(oracle_mod, w):
     """1024 or more seeded query rows (all sequences and heads) of the 4:1 and
