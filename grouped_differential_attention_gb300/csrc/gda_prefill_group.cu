@@ -624,30 +624,73 @@ gda_prefill_group_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_
                 for (int e = 0; e < kKQ; ++e)
                     if (k0 + e > last_key) x[e] = __float_as_uint(-INFINITY);
             };
-            auto stats_tile = [&](int j, auto first, auto masked) {
+            // map m of key tile j, with that map's running statistics (mxm, lsm); the unrolled
+            // loop below spells the same steps out with the statistics indexed by map
+            auto stats_map = [&](int j, int m, float &mxm, float &lsm, auto first, auto masked) {
                 const int k0 = j * kGBN + kq * kKQ;
-#pragma unroll
-                for (int m = 0; m < M; ++m) {
-                    const uint32_t slot = slot_a<S>(j * M + m);
-                    uint32_t x[kKQ];
-                    acquire(x, slot);
-                    if constexpr (decltype(masked)::value) mask_x(x, k0);
-                    if constexpr (decltype(first)::value) {
-                        mx[m] = fmaxf(tile_max(x), -1e30f);
-                        ls[m] = tile_sum(x, mx[m]);
-                    } else {
-                        float ts = tile_sum(x, mx[m]);
-                        if (__any_sync(0xffffffffu, !(ts <= 65536.f))) {
-                            read_slot(x, slot);
-                            if constexpr (decltype(masked)::value) mask_x(x, k0);
-                            const float nr = fmaxf(mx[m], tile_max(x));
-                            ls[m] *= fast_exp2(mx[m] - nr);
-                            mx[m] = nr;
-                            ts = tile_sum(x, nr);
-                        }
-                        ls[m] += ts;
+                const uint32_t slot = slot_a<S>(j * M + m);
+                uint32_t x[kKQ];
+                acquire(x, slot);
+                if constexpr (decltype(masked)::value) mask_x(x, k0);
+                if constexpr (decltype(first)::value) {
+                    mxm = fmaxf(tile_max(x), -1e30f);
+                    lsm = tile_sum(x, mxm);
+                } else {
+                    float ts = tile_sum(x, mxm);
+                    if (__any_sync(0xffffffffu, !(ts <= 65536.f))) {
+                        read_slot(x, slot);
+                        if constexpr (decltype(masked)::value) mask_x(x, k0);
+                        const float nr = fmaxf(mxm, tile_max(x));
+                        lsm *= fast_exp2(mxm - nr);
+                        mxm = nr;
+                        ts = tile_sum(x, nr);
                     }
-                    release(slot);
+                    lsm += ts;
+                }
+                release(slot);
+            };
+            // Short items (the staged-epilogue instance) keep the map loop rolled, the maps'
+            // statistics rotating through registers: the smaller code measured 8 % faster at
+            // L = 2048, the unrolled loop 7 % faster at L = 32768.
+            auto stats_tile = [&](int j, auto first, auto masked) {
+                if constexpr (kStageOut) {
+#pragma unroll 1
+                    for (int m = 0; m < M; ++m) {
+                        stats_map(j, m, mx[0], ls[0], first, masked);
+                        const float m0 = mx[0], l0 = ls[0];
+#pragma unroll
+                        for (int q = 0; q + 1 < M; ++q) {
+                            mx[q] = mx[q + 1];
+                            ls[q] = ls[q + 1];
+                        }
+                        mx[M - 1] = m0;
+                        ls[M - 1] = l0;
+                    }
+                } else {
+                    const int k0 = j * kGBN + kq * kKQ;
+#pragma unroll
+                    for (int m = 0; m < M; ++m) {
+                        const uint32_t slot = slot_a<S>(j * M + m);
+                        uint32_t x[kKQ];
+                        acquire(x, slot);
+                        if constexpr (decltype(masked)::value) mask_x(x, k0);
+                        if constexpr (decltype(first)::value) {
+                            mx[m] = fmaxf(tile_max(x), -1e30f);
+                            ls[m] = tile_sum(x, mx[m]);
+                        } else {
+                            float ts = tile_sum(x, mx[m]);
+                            if (__any_sync(0xffffffffu, !(ts <= 65536.f))) {
+                                read_slot(x, slot);
+                                if constexpr (decltype(masked)::value) mask_x(x, k0);
+                                const float nr = fmaxf(mx[m], tile_max(x));
+                                ls[m] *= fast_exp2(mx[m] - nr);
+                                mx[m] = nr;
+                                ts = tile_sum(x, nr);
+                            }
+                            ls[m] += ts;
+                        }
+                        release(slot);
+                    }
                 }
             };
             constexpr std::true_type kYes{};
