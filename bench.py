@@ -760,7 +760,7 @@ def run_gda(args, world, rank, local):
             "parallelism": f"{world} independent replica(s), no collective on the data path",
         },
         "roofline": {
-            "kernel": (f"gda_prefill_group_kernel<3, {int((w.L + 127) // 128 <= 32)}>"
+            "kernel": (f"gda_prefill_group_kernel<3, {int((w.L + 127) // 128 <= 28)}>"
                        if (w.d == 64 and w.dv == 128 and w.h_s == 3 * w.h_n) else "gda_prefill_tc_kernel"),
             "bound": "tensor",
             "achieved": achieved,

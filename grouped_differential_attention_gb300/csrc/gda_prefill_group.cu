@@ -52,9 +52,10 @@
 //   warps 4-19  compute (thread = query row = TMEM lane; warp w takes keys
 //               [32 k, 32 k + 32) of each tile, k = (w - 4) / 4: four compute
 //               warps per SM sub-partition): statistics, P, and the epilogue.
-// Epilogue: items of at most kStageOutTiles key tiles stage the output rows in the
-// P buffers and write them with TMA stores (one thread per row quarter); longer
-// items, where the epilogue is a small share, store each thread's row segment.
+// Short items (at most kStageOutTiles key tiles) stage the output rows in the P
+// buffers and write them with TMA stores (one thread per row quarter) and keep the
+// statistics sweep's map loop rolled; longer items, where the epilogue is a small
+// share, store each thread's row segment and unroll that loop.
 // Every mbarrier wait is bounded (1 s) and sets GDA_DEVERR_PREFILL_TIMEOUT.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -72,7 +73,7 @@ namespace gda {
 namespace {
 
 constexpr int kGBN = 128;              // keys per logit tile
-constexpr int kStageOutTiles = 32;     // longest item (key tiles) that takes the staged epilogue
+constexpr int kStageOutTiles = 28;     // longest item (key tiles) that takes the short-item instance
 constexpr int kPH = 64;                // keys per P half / V tile
 #ifndef GDA_GROUP_KEYS_PER_THREAD
 #define GDA_GROUP_KEYS_PER_THREAD 32
@@ -1036,9 +1037,10 @@ int launch_prefill_group(const PrefillArgs &a, cudaStream_t stream) {
         const long long nqt = (a.L + kBM - 1) / kBM;
         if (2 * nqt * a.B * (a.hs / S) < sms) S = 1;
     }
-    // Items of at most kStageOutTiles key tiles end in the staged epilogue (TMA stores of the
-    // output): there the epilogue is a large share of an item.  Longer items keep the per-row
-    // stores, which drain while the next item's statistics sweep runs.
+    // Items of at most kStageOutTiles key tiles take the short-item instance: the staged
+    // epilogue (TMA stores of the output; there the epilogue is a large share of an item) and a
+    // rolled statistics loop (smaller code).  Longer items keep the per-row stores, which drain
+    // while the next item's statistics sweep runs, and the unrolled loop.
     const long long Lk = a.Lk > 0 ? a.Lk : a.L;
     const bool staged = (Lk + kGBN - 1) / kGBN <= kStageOutTiles;
     switch (S) {

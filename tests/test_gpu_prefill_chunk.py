@@ -37,7 +37,7 @@ def chunk_case(B, L, Lk, hs, hn, d, dv, seed):
     (2, 200, 200, 4, 2, 128, 256, True),
     (1, 64, 130, 4, 4, 64, 128, False),
     (1, 300, 2048, 8, 2, 128, 128, True),
-    # more than 32 key tiles per item: the grouped kernel's per-row output stores instead of
+    # more than 28 key tiles per item: the grouped kernel's per-row output stores instead of
     # the staged (TMA) epilogue, with items of two signal heads and of one
     (4, 640, 4200, 8, 2, 64, 128, True),
     (1, 100, 4500, 3, 1, 64, 128, True),

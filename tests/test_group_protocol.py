@@ -18,7 +18,7 @@ The model mirrors the kernel's loops: slot assignment of the statistics sweep, t
 K / V ring consumed in order by two issuers that skip each other's entries, the P
 buffers [buffer][half], the per-row exchange in the row's own bytes of P buffer 0, and
 the per-item barriers (q_full / q_empty, o_final / o_free), and both epilogues: per-row
-output stores (items longer than 32 key tiles) and the staged one, whose output rows go
+output stores (items longer than 28 key tiles) and the staged one, whose output rows go
 through the P buffers to TMA stores issued by one thread of each row quarter.  Compute
 warps are modelled as units of two row quarters x four key quarters.
 """
