@@ -181,12 +181,6 @@ __device__ __forceinline__ bool wait_quick(uint64_t *bar, uint32_t parity, unsig
     return ok != 0 || wait_bar(bar, parity, err, abort);
 }
 
-// The same for a whole warp, which agrees on the result by vote.
-__device__ __forceinline__ bool warp_wait_quick(uint64_t *bar, uint32_t parity, unsigned *err,
-                                                volatile int *abort) {
-    return __all_sync(0xffffffffu, wait_quick(bar, parity, err, abort));
-}
-
 // Kernels after the first are programmatic dependent launches: each sets up its barriers
 // and TMEM while the previous kernel finishes, then waits here for that grid's completion
 // (its writes visible) before reading anything it produced.
@@ -409,10 +403,9 @@ gda_bwd_prep_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_const
             for (int j = 0; j < nkv; ++j) {
                 const uint32_t gs = gt + j;
                 const int bb = gs & 1;
-                if (!warp_wait_quick(&ctl->s_full[bb], (gs >> 1) & 1, p.err, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+                // per-lane waits: a failed one sets the error word and the flag that ends every
+                // later wait at once; the loop runs on, so the barrier counts stay whole
+                if (!wait_quick(&ctl->s_full[bb], (gs >> 1) & 1, p.err, abort_flag)) ok = false;
                 tc_fence_after();
                 const uint32_t tS1 = tmem + lane_off + tS1_0 + bb * kN + grp * 16;
                 const uint32_t tS2 = tmem + lane_off + tS2_0 + bb * kN + grp * 16;
@@ -797,11 +790,8 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
                     const int q0 = (i0 + i) * kN + grp * 16;     // this group's first query column
                     const int st = gq % QS;
                     // the stage's vectors were written by the copy engine: observe its barrier too
-                    if (!warp_wait_quick(&ctl->s_full, gq & 1, p.err, abort_flag) ||
-                        !warp_wait_quick(&ctl->q_full[st], (gq / QS) & 1, p.err, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!wait_quick(&ctl->s_full, gq & 1, p.err, abort_flag)) ok = false;
+                    if (!wait_quick(&ctl->q_full[st], (gq / QS) & 1, p.err, abort_flag)) ok = false;
                     tc_fence_after();
                     const uint32_t tcol = tmem + lane_off + grp * 16;
                     uint32_t s1[16], s2[16], dp[16];
@@ -858,10 +848,7 @@ gda_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmK1, const __grid_const
                     else
                         pairs(std::true_type{});
                     // the previous tile's products have read W / dS1 / dS2
-                    if (gq > 0 && !warp_wait_quick(&ctl->w_free, (gq - 1) & 1, p.err, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    if (gq > 0 && !wait_quick(&ctl->w_free, (gq - 1) & 1, p.err, abort_flag)) ok = false;
                     // row `row` of each K-major tile: 16-byte chunks 2 grp and 2 grp + 1 (query
                     // columns 16 grp .. 16 grp + 15), 128-byte swizzle: chunk c at c ^ (row % 8)
                     uint8_t *wrow = smem + LY::OFF_W + row * 128;
@@ -1166,10 +1153,7 @@ gda_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
                 const float D2 = in ? p.D2[(static_cast<size_t>(b) * p.hs + h) * p.Lp + qrow] : 0.f;
                 for (int j = 0; j < nkv; ++j) {
                     const uint32_t sb = tmem + lane_off + (gk & 1) * kSB + grp * 16;
-                    if (!warp_wait_quick(&ctl->s_full[gk & 1], (gk >> 1) & 1, p.err, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!wait_quick(&ctl->s_full[gk & 1], (gk >> 1) & 1, p.err, abort_flag)) ok = false;
                     tc_fence_after();
                     uint32_t s1[16], s2[16], dp[16];
                     tmem_ld16(sb + tS1, s1);
