@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 #include <cmath>
+#include <type_traits>
 
 #include "gda.h"
 #include "gda_device.cuh"
@@ -260,10 +261,9 @@ gda_lse_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_constan
             for (int j = 0; j < it.nkv; ++j) {
                 const uint32_t gs = gt + j;
                 const int bb = gs & 1;
-                if (!warp_wait(&ctl->s_full[bb], (gs >> 1) & 1, p.err, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+                // per-lane wait: a failed one sets the error word and the flag that ends every
+                // later wait at once; the loop runs on, so the barrier counts stay whole
+                if (!wait_quick(&ctl->s_full[bb], (gs >> 1) & 1, p.err, abort_flag)) ok = false;
                 tc_fence_after();
                 uint32_t rr[32];
                 tmem_ld32(tmem + lane_off + bb * kBN2 + half * 32, rr);
@@ -590,10 +590,9 @@ gda_diffmap_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_con
             for (int j = 0; j < it.nkv; ++j) {
                 const uint32_t gs = gt + j;
                 const int bb = gs & 1;
-                if (!warp_wait(&ctl->s_full[bb], (gs >> 1) & 1, p.err, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+                // per-lane wait: a failed one sets the error word and the flag that ends every
+                // later wait at once; the loop runs on, so the barrier counts stay whole
+                if (!wait_quick(&ctl->s_full[bb], (gs >> 1) & 1, p.err, abort_flag)) ok = false;
                 tc_fence_after();
                 const uint32_t tS1 = tmem + lane_off + tS1_0 + bb * kBN2 + half * 32;
                 const uint32_t tS2 = tmem + lane_off + tS2_0 + bb * kBN2 + half * 32;
@@ -603,22 +602,28 @@ gda_diffmap_tc_kernel(const __grid_constant__ CUtensorMap tmQ1, const __grid_con
                 tmem_ld_wait_regs(r1);
                 reg_fence(r2);
                 const int k0 = j * kBN2 + half * 32;
-                const bool need_mask = k0 + 31 > last_key;
                 uint32_t pk[16];
+                auto probs = [&](auto masked) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float x0 = __uint_as_float(r1[e]), x1 = __uint_as_float(r1[e + 1]);
-                    float y0 = __uint_as_float(r2[e]), y1 = __uint_as_float(r2[e + 1]);
-                    ffma2(x0, x1, sl2, sl2, neg1, neg1);
-                    ffma2(y0, y1, sl2, sl2, neg2, neg2);
-                    float p0 = fmaf(nlam, fast_exp2(y0), fast_exp2(x0));
-                    float p1 = fmaf(nlam, fast_exp2(y1), fast_exp2(x1));
-                    if (need_mask) {
-                        if (k0 + e > last_key) p0 = 0.f;
-                        if (k0 + e + 1 > last_key) p1 = 0.f;
+                    for (int e = 0; e < 32; e += 2) {
+                        float x0 = __uint_as_float(r1[e]), x1 = __uint_as_float(r1[e + 1]);
+                        float y0 = __uint_as_float(r2[e]), y1 = __uint_as_float(r2[e + 1]);
+                        ffma2(x0, x1, sl2, sl2, neg1, neg1);
+                        ffma2(y0, y1, sl2, sl2, neg2, neg2);
+                        float p0 = fmaf(nlam, fast_exp2(y0), fast_exp2(x0));
+                        float p1 = fmaf(nlam, fast_exp2(y1), fast_exp2(x1));
+                        if constexpr (decltype(masked)::value) {
+                            if (k0 + e > last_key) p0 = 0.f;
+                            if (k0 + e + 1 > last_key) p1 = 0.f;
+                        }
+                        pk[e / 2] = pack_bf16x2(p0, p1);
                     }
-                    pk[e / 2] = pack_bf16x2(p0, p1);
-                }
+                };
+                // the per-key test only where some row of the warp has keys past its last one
+                if (__any_sync(0xffffffffu, k0 + 31 > last_key))
+                    probs(std::true_type{});
+                else
+                    probs(std::false_type{});
                 tmem_st16(tS1, pk);                  // over the S1 columns this half read
                 tmem_st_wait();
                 tc_fence_before();
