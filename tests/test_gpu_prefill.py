@@ -107,14 +107,16 @@ def test_prefill_3to1_workload_every_element(oracle_mod):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-def test_prefill_whole_group_items_ragged_tail(oracle_mod, causal):
-    """Items of the whole 3-head group (B=8, L=1200: 160 items) with the output staged for
-    TMA stores; the last query tile holds 48 rows, so one row quarter's store is clipped at
-    L and two quarters have no rows at all."""
-    inp = W.make_prefill_inputs(W.GDA3_PREFILL_L2048, B=8, L=1200, h_s=3, h_n=1, seed=1201)
+@pytest.mark.parametrize("B,L,hs,hn", [(8, 1200, 3, 1), (4, 600, 8, 2)], ids=["three_heads", "two_heads"])
+def test_prefill_whole_group_items_ragged_tail(oracle_mod, causal, B, L, hs, hn):
+    """Short items of several signal heads (B=8, L=1200, a 3:1 group: 160 items of three
+    heads; B=4, L=600, 4:1 groups: 160 items of two heads) with the output staged for TMA
+    stores; the last query tile holds 48 or 88 rows, so one row quarter's store is clipped
+    at L and the quarters past it have no rows at all."""
+    inp = W.make_prefill_inputs(W.GDA3_PREFILL_L2048, B=B, L=L, h_s=hs, h_n=hn, seed=1201 + L)
     got = run_bf16(inp, 0.8, causal)
     ref = oracle_mod.prefill(*inp, 0.8, causal=causal)
-    assert_bf16_close(got, ref, "whole-group items, ragged tail")
+    assert_bf16_close(got, ref, "short items of several heads, ragged tail")
 
 
 @pytest.mark.parametrize("w", [W.GDA4_PREFILL_L8192, W.GDA3_PREFILL_L32768], ids=lambda x: x.name)
